@@ -1,0 +1,111 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module holds no attention arithmetic: it only names the workloads and
+draws their inputs, so both the CUDA path's tests and the CPU oracle can be fed
+from the same bytes.
+
+Recipe (the same for every workload): a CPU ``torch.Generator`` seeded with
+``seed`` draws float32 standard normals in the order q, k, v, dO, each shaped
+``[T, H, d]`` (token-major, head dimension innermost), and each is rounded to
+bfloat16 (round to nearest even).  ``scale`` is 1/sqrt(d).  Packed
+variable-length workloads list their sequence lengths literally; they were drawn
+once as ``torch.randint(512, 8193, (8,))`` from a CPU generator seeded 0 and are
+frozen here so that no torch version can change them.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_qkv"]
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    N: int  # sequence length (batched) or the longest sequence (packed)
+    d: int
+    causal: bool
+    lengths: tuple = field(default=())  # packed sequences; empty = batched
+    backward: bool = False
+
+    @property
+    def seq_lengths(self) -> list:
+        return list(self.lengths) if self.lengths else [self.N] * self.B
+
+    @property
+    def T(self) -> int:
+        return sum(self.seq_lengths)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def varlen(self) -> bool:
+        return bool(self.lengths)
+
+    def fwd_flops(self) -> float:
+        """Algorithmic forward FLOPs: 4 L^2 d per (sequence, query head),
+        halved under the causal mask."""
+        f = sum(4.0 * L * L * self.d for L in self.seq_lengths) * self.Hq
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        """Algorithmic backward FLOPs: 2.5 x the forward count."""
+        return 2.5 * self.fwd_flops()
+
+
+VARLEN_LENGTHS = (6638, 4932, 6735, 1706, 6830, 4356, 1178, 6860)
+
+WORKLOADS = {
+    "fwd_b1_h1_n256_d64": Workload("fwd_b1_h1_n256_d64", 1, 1, 1, 256, 64, False),
+    "fwd_b4_h16_n2048_d64": Workload("fwd_b4_h16_n2048_d64", 4, 16, 16, 2048, 64, False),
+    "fwd_b2_h32_n4096_d128_causal": Workload(
+        "fwd_b2_h32_n4096_d128_causal", 2, 32, 32, 4096, 128, True),
+    "fwd_varlen8_hq32_hkv8_d128_causal": Workload(
+        "fwd_varlen8_hq32_hkv8_d128_causal", 8, 32, 8, max(VARLEN_LENGTHS), 128, True,
+        VARLEN_LENGTHS),
+    "fwdbwd_b2_h16_n4096_d64_causal": Workload(
+        "fwdbwd_b2_h16_n4096_d64_causal", 2, 16, 16, 4096, 64, True, (), True),
+}
+
+
+def make_qkv(T, Hq, Hkv, d, seed=0, with_do=False, q_mult=1.0):
+    """Draw q [T,Hq,d], k, v [T,Hkv,d] (and dO [T,Hq,d]) as bf16 CPU tensors.
+
+    ``q_mult`` multiplies the float32 draw of q before rounding (stress cases
+    with a wide score range)."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(T, Hq, d, generator=g)
+    k = torch.randn(T, Hkv, d, generator=g)
+    v = torch.randn(T, Hkv, d, generator=g)
+    out = {
+        "q": (q * q_mult).to(torch.bfloat16),
+        "k": k.to(torch.bfloat16),
+        "v": v.to(torch.bfloat16),
+    }
+    if with_do:
+        out["do"] = torch.randn(T, Hq, d, generator=g).to(torch.bfloat16)
+    return out
+
+
+def cu_seqlens_of(lengths) -> torch.Tensor:
+    cu = [0]
+    for L in lengths:
+        cu.append(cu[-1] + int(L))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def make_inputs(w: Workload, seed=0, with_do=None):
+    """Inputs of workload ``w`` on the CPU: q, k, v (, do) bf16 and cu_seqlens int32."""
+    if with_do is None:
+        with_do = w.backward
+    t = make_qkv(w.T, w.Hq, w.Hkv, w.d, seed=seed, with_do=with_do)
+    t["cu_seqlens"] = cu_seqlens_of(w.seq_lengths)
+    return t

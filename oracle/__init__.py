@@ -1,0 +1,13 @@
+"""fp64 CPU oracle for exact attention (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+and reference legs may import this package.  See ``oracle/attention.py``.
+"""
+from .attention import (  # noqa: F401
+    attention_backward,
+    attention_forward,
+    attention_forward_rows,
+    cu_from_lengths,
+    tile_counts,
+    tile_counts_closed_form,
+)

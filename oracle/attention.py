@@ -1,0 +1,253 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` use it.  It shares
+no code, table or constant with the CUDA library; the two meet only through the
+seeded input generator, which holds none of the method's arithmetic.
+
+What it computes is the plain definition of attention, written out with the
+N x N score and probability matrices materialised, exactly the data flow the
+tiled method is built to avoid:
+
+* "FlashAttention：从 Safe Softmax 到分块计算", section 1 (the formula
+  S = QK^T/sqrt(d), P = softmax(S), O = PV and the shapes of each matrix) and
+  section 1.1 (one query row: p_ij = e^{s_ij} / sum_t e^{s_it}, o_i = sum_j p_ij v_j).
+* the same page, section 2 (safe softmax: subtract the row max before the
+  exponential; the result is the same number).
+* the same page, section 5.2 (causal mask: s_ij = -inf when j > i, so the
+  diagonal stays visible).
+* the same page, section 8 (the per-row LogSumExp is the statistic kept for
+  the backward pass).
+* "企业官网建设流程全解析" (the FlashAttention data-flow notes), section 2.3
+  (backward: dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dP * P))); the
+  remaining chain-rule steps dQ = scale dS K and dK = scale dS^T Q follow from
+  S = scale Q K^T.
+* "Attention 算子优化…", section 五 (GQA: consecutive groups of query heads
+  share one K/V head) and section 二 (packed variable-length sequences, no
+  padding).
+
+Readings of points the pages leave open (each one is also listed in the design
+notes):
+
+* ``scale`` multiplies the raw dot products before masking and softmax; the
+  LSE is the natural-log LogSumExp of the *scaled*, masked scores.
+* Causal masking uses positions relative to the start of each sequence, and
+  key j is visible from query i when j <= i.
+* A row with no visible key (only possible for an empty sequence here) gives
+  O = 0 and LSE = -inf.
+* Layout: tokens-major ``[T, H, d]`` for q/k/v/o and their gradients, ``[Hq, T]``
+  for the LSE; sequence s covers tokens ``cu_seqlens[s] .. cu_seqlens[s+1]-1``.
+
+All arithmetic is float64.  Matrix products use numpy's ``@`` (a library
+primitive), with no blocking, fusion or reordering beyond the definition.
+
+Parity pins: every function here is checked in ``tests/test_oracle.py``
+against the worked examples the pages print, closed forms, invariants and
+central finite differences.  The one reading with no pin is that the CUDA
+path rounds P to bf16 before the P.V product; the pages are silent on it and it
+is bounded only by the stated tolerances.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "attention_forward",
+    "attention_forward_rows",
+    "attention_backward",
+    "tile_counts",
+    "tile_counts_closed_form",
+    "cu_from_lengths",
+]
+
+
+def cu_from_lengths(lengths) -> np.ndarray:
+    """Prefix sums [0, L0, L0+L1, ...] of the sequence lengths (int64)."""
+    cu = np.zeros(len(lengths) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(np.asarray(lengths, dtype=np.int64))
+    return cu
+
+
+def _check_shapes(q, k, v, cu):
+    T, Hq, d = q.shape
+    Tk, Hkv, dk = k.shape
+    if v.shape != k.shape or Tk != T or dk != d:
+        raise ValueError("q [T,Hq,d], k and v [T,Hkv,d] expected")
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    cu = np.asarray(cu, dtype=np.int64)
+    if cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must rise from 0 to T")
+    return T, Hq, Hkv, d, cu
+
+
+def _scores(q_rows, k_rows, scale, causal, q_pos, k_len):
+    """Scaled, masked score matrix S for one (sequence, head).
+
+    S[i, j] = scale * <q_i, k_j>; entries with key position > query position
+    are -inf under the causal mask (the diagonal stays visible).
+    """
+    S = scale * (q_rows @ k_rows.T)
+    if causal:
+        k_pos = np.arange(k_len)
+        S = np.where(k_pos[None, :] > np.asarray(q_pos)[:, None], -np.inf, S)
+    return S
+
+
+def _safe_softmax(S):
+    """Row-wise safe softmax of S: returns P and the LSE.
+
+    m_i = max_j S_ij; P_ij = exp(S_ij - m_i) / sum_t exp(S_it - m_i);
+    LSE_i = m_i + ln sum_t exp(S_it - m_i).  A row that is entirely -inf gives
+    P = 0 and LSE = -inf.
+    """
+    m = S.max(axis=1) if S.shape[1] else np.full(S.shape[0], -np.inf)
+    dead = ~np.isfinite(m)
+    m_safe = np.where(dead, 0.0, m)
+    E = np.exp(S - m_safe[:, None])
+    ell = E.sum(axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        P = np.where(dead[:, None], 0.0, E / np.where(dead, 1.0, ell)[:, None])
+        lse = np.where(dead, -np.inf, m_safe + np.log(np.where(dead, 1.0, ell)))
+    return P, lse
+
+
+def attention_forward(q, k, v, cu_seqlens, scale, causal):
+    """O and LSE of exact attention over packed sequences (fp64).
+
+    q: [T, Hq, d]; k, v: [T, Hkv, d]; cu_seqlens: [B+1] prefix sums.
+    Returns o [T, Hq, d] and lse [Hq, T].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    T, Hq, Hkv, d, cu = _check_shapes(q, k, v, cu_seqlens)
+    group = Hq // Hkv
+    o = np.zeros((T, Hq, d), dtype=np.float64)
+    lse = np.full((Hq, T), -np.inf, dtype=np.float64)
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        L = b - a
+        if L == 0:
+            continue
+        pos = np.arange(L)
+        for h in range(Hq):
+            kv = h // group
+            S = _scores(q[a:b, h, :], k[a:b, kv, :], scale, causal, pos, L)
+            P, lse_rows = _safe_softmax(S)
+            o[a:b, h, :] = P @ v[a:b, kv, :]
+            lse[h, a:b] = lse_rows
+    return o, lse
+
+
+def attention_forward_rows(q, k, v, cu_seqlens, scale, causal, tokens, heads):
+    """O and LSE for selected (token, query head) rows only.
+
+    The same definition as :func:`attention_forward`, evaluated one query row
+    at a time, so that single outputs of a full-size problem can be checked.
+    Returns o [n, d] and lse [n].
+    """
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    group = Hq // Hkv
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    heads = np.asarray(heads, dtype=np.int64)
+    o = np.zeros((len(tokens), d), dtype=np.float64)
+    lse = np.full(len(tokens), -np.inf, dtype=np.float64)
+    seq_of = np.searchsorted(cu, tokens, side="right") - 1
+    for n in range(len(tokens)):
+        s = int(seq_of[n])
+        a, b = int(cu[s]), int(cu[s + 1])
+        t, h = int(tokens[n]), int(heads[n])
+        kv = h // group
+        qi = np.asarray(q[t, h, :], dtype=np.float64)[None, :]
+        kk = np.asarray(k[a:b, kv, :], dtype=np.float64)
+        vv = np.asarray(v[a:b, kv, :], dtype=np.float64)
+        S = _scores(qi, kk, scale, causal, [t - a], b - a)
+        P, lse_row = _safe_softmax(S)
+        o[n] = (P @ vv)[0]
+        lse[n] = lse_row[0]
+    return o, lse
+
+
+def attention_backward(q, k, v, do, cu_seqlens, scale, causal, return_rowsum=False):
+    """dQ, dK, dV of exact attention for the upstream gradient dO (fp64).
+
+    Per (sequence, query head), with S and P materialised:
+      dV  = P^T dO
+      dP  = dO V^T
+      dS  = P * (dP - rowsum(dP * P))
+      dQ  = scale * dS K
+      dK  = scale * dS^T Q
+    and dK, dV of a K/V head summed over the query heads that share it.
+    With ``return_rowsum`` the per-row rowsum(dP * P) is also returned, as
+    [Hq, T].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    T, Hq, Hkv, d, cu = _check_shapes(q, k, v, cu_seqlens)
+    group = Hq // Hkv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    rowsum = np.zeros((Hq, T), dtype=np.float64)
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        L = b - a
+        if L == 0:
+            continue
+        pos = np.arange(L)
+        for h in range(Hq):
+            kv = h // group
+            Q, K, V, dO = q[a:b, h, :], k[a:b, kv, :], v[a:b, kv, :], do[a:b, h, :]
+            S = _scores(Q, K, scale, causal, pos, L)
+            P, _ = _safe_softmax(S)
+            dv[a:b, kv, :] += P.T @ dO
+            dP = dO @ V.T
+            r = (dP * P).sum(axis=1)
+            dS = P * (dP - r[:, None])
+            dq[a:b, h, :] = scale * (dS @ K)
+            dk[a:b, kv, :] += scale * (dS.T @ Q)
+            rowsum[h, a:b] = r
+    if return_rowsum:
+        return dq, dk, dv, rowsum
+    return dq, dk, dv
+
+
+def tile_counts(lengths, causal, Br=128, Bc=128):
+    """Number of (query tile, key tile) pairs holding at least one visible score.
+
+    Brute force: for each sequence, enumerate every query tile i and key tile
+    j and test whether some (query row r, key column c) in the pair is inside
+    the sequence and not masked (c <= r when causal).  This is the work that
+    tile skipping leaves ("Attention 算子优化…", section 四: about half of the
+    tiles lie entirely under the causal mask and are skipped).  Returns one
+    count per sequence (per query head).
+    """
+    out = []
+    for L in lengths:
+        L = int(L)
+        n = 0
+        for i in range(-(-L // Br)):
+            r_hi = min(L, (i + 1) * Br) - 1  # last real row of the tile
+            for j in range(-(-L // Bc)):
+                c_lo = j * Bc  # first column of the tile (always < L here)
+                if not causal or c_lo <= r_hi:
+                    n += 1
+        out.append(n)
+    return out
+
+
+def tile_counts_closed_form(L, causal, B=128):
+    """Closed form of :func:`tile_counts` for square tiles Br = Bc = B:
+    sum over query tiles i of min(i + 1, ceil(L / B)) when causal, else
+    ceil(L / B)^2."""
+    n = -(-int(L) // B)
+    if not causal:
+        return n * n
+    return sum(min(i + 1, n) for i in range(n))
+

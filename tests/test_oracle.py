@@ -1,0 +1,357 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: a worked
+example the pages print, a closed form, an invariant of the mathematics, a
+special case with a textbook answer, brute force on a tiny input, or central
+finite differences for the backward pass.  The cases are chosen so that a
+dropped scale, a wrong sign, a transposed operand, an off-by-one causal mask or
+a missing rowsum term each fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.golden_io import load
+
+F = oracle.attention_forward
+BWD = oracle.attention_backward
+
+
+def rnd(T, Hq, Hkv, d, seed):
+    r = np.random.default_rng(seed)
+    return (r.standard_normal((T, Hq, d)), r.standard_normal((T, Hkv, d)),
+            r.standard_normal((T, Hkv, d)), r.standard_normal((T, Hq, d)))
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_online_softmax_two_blocks_example():
+    """"Attention 算子优化…" section 三: [1,2] then [3,1] give l ~= 1.638."""
+    g = load("online_softmax_two_blocks.txt")
+    scores = g["scores_block1"] + g["scores_block2"]
+    # scores as q.k with d = 1, scale = 1
+    n = len(scores)
+    q = np.ones((n, 1, 1))
+    k = np.array(scores, float).reshape(n, 1, 1)
+    v = np.zeros((n, 1, 1))
+    _, lse = F(q, k, v, [0, n], 1.0, False)
+    ell = math.exp(lse[0, 0] - g["page_m_final"])
+    # the page sums terms already rounded to 3 decimals, so its figure is good
+    # to one unit in the last printed digit (exact: 1.63855)
+    assert abs(ell - g["page_l_new"]) <= 10.0 ** -g["page_digits"]
+    assert ell == pytest.approx(g["exact_l_new"], rel=1e-14)
+    # the page's intermediate numbers, recomputed by the recurrence it describes
+    b1, b2 = g["scores_block1"], g["scores_block2"]
+    m_old = max(b1)
+    l_old = sum(math.exp(s - m_old) for s in b1)
+    assert round(l_old, 3) == g["page_l_old"]
+    m_new = max(m_old, max(b2))
+    corr = math.exp(m_old - m_new)
+    assert round(corr, 3) == g["page_correction"]
+    l_new = corr * l_old + sum(math.exp(s - m_new) for s in b2)
+    assert l_new == pytest.approx(ell, rel=1e-15, abs=1e-15)
+
+
+def test_online_softmax_value_example():
+    """"FlashAttention：从 Safe Softmax 到分块计算" section 3.3:
+    [1,2] then [3], v = [10,20,30]: o = u / l with the page's closed forms."""
+    g = load("online_softmax_value_example.txt")
+    n = len(g["scores"])
+    q = np.ones((n, 1, 1))
+    k = np.array(g["scores"], float).reshape(n, 1, 1)
+    v = np.array(g["values"], float).reshape(n, 1, 1)
+    o, lse = F(q, k, v, [0, n], 1.0, False)
+    # every row sees the same scores (non-causal, identical queries)
+    assert o[0, 0, 0] == pytest.approx(g["merged_u"] / g["merged_l"], rel=1e-14)
+    assert lse[0, 0] == pytest.approx(g["m_final"] + math.log(g["merged_l"]), rel=1e-14)
+    # the merge of block states equals the one-pass state (page's identity)
+    assert g["merged_l"] == pytest.approx(sum(math.exp(s - 3) for s in g["scores"]), rel=1e-15)
+    assert g["merged_u"] == pytest.approx(
+        sum(math.exp(s - 3) * x for s, x in zip(g["scores"], g["values"])), rel=1e-15)
+    # a transposed or reversed value order would give another number
+    assert o[0, 0, 0] == pytest.approx(25.752104, abs=1e-6)
+
+
+def test_safe_softmax_example_probabilities():
+    """Same page, section 2.1: [1,2,3] -> (e^-2, e^-1, 1) / sum; V = I reads P."""
+    g = load("safe_softmax_example.txt")
+    n = 3
+    q = np.zeros((n, 1, 3)); q[:, 0, 0] = 1.0
+    k = np.zeros((n, 1, 3)); k[:, 0, 0] = g["scores"]
+    v = np.eye(3).reshape(3, 1, 3)
+    o, _ = F(q, k, v, [0, n], 1.0, False)
+    e = np.array(g["shifted_exp"])
+    np.testing.assert_allclose(o[0, 0], e / e.sum(), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- hand N=4, d=2
+
+def test_hand_zero_query_uniform():
+    """Q = 0: every score is 0, P is uniform, O = column mean of V, LSE = ln 4."""
+    q = np.zeros((4, 1, 2))
+    k = np.array([[1, 2], [3, -1], [0, 5], [-2, 2]], float)[:, None, :]
+    v = np.array([[1, 0], [2, 4], [3, 8], [6, -4]], float)[:, None, :]
+    o, lse = F(q, k, v, [0, 4], 0.5, False)
+    np.testing.assert_allclose(o[:, 0, :], np.tile([3.0, 2.0], (4, 1)), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[0], np.full(4, math.log(4)), rtol=1e-15)
+
+
+def test_hand_equal_keys_uniform():
+    """All K rows equal: scores equal along each row, same uniform result."""
+    q = np.array([[1, 2], [0, 1], [-3, 1], [2, 2]], float)[:, None, :]
+    k = np.tile([[2.0, -1.0]], (4, 1))[:, None, :]
+    v = np.array([[1, 0], [2, 4], [3, 8], [6, -4]], float)[:, None, :]
+    o, lse = F(q, k, v, [0, 4], 1.0, False)
+    np.testing.assert_allclose(o[:, 0, :], np.tile([3.0, 2.0], (4, 1)), atol=1e-14)
+    expect = [1 * 2 - 2 + math.log(4), -1 + math.log(4), -6 - 1 + math.log(4), 4 - 2 + math.log(4)]
+    np.testing.assert_allclose(lse[0], expect, rtol=1e-14)
+
+
+def test_hand_causal_zero_query_prefix_means():
+    """Causal with Q = 0: O_i = mean(V[0..i]) and LSE_i = ln(i+1) (diagonal visible)."""
+    q = np.zeros((4, 1, 2))
+    k = np.array([[1, 2], [3, -1], [0, 5], [-2, 2]], float)[:, None, :]
+    v = np.array([[1, 0], [2, 4], [3, 8], [6, -4]], float)[:, None, :]
+    o, lse = F(q, k, v, [0, 4], 1.0, True)
+    want = np.array([[1, 0], [1.5, 2], [2, 4], [3, 2]], float)
+    np.testing.assert_allclose(o[:, 0, :], want, atol=1e-15)
+    np.testing.assert_allclose(lse[0], [math.log(i + 1) for i in range(4)], rtol=1e-15, atol=1e-15)
+
+
+def test_hand_exponential_weights():
+    """q = [1,0], keys [j,0]: p_j = e^j / sum e^j; with V = [j, 1] O = (E[j], 1)."""
+    q = np.tile([[1.0, 0.0]], (4, 1))[:, None, :]
+    k = np.array([[j, 0] for j in range(4)], float)[:, None, :]
+    v = np.array([[j, 1] for j in range(4)], float)[:, None, :]
+    o, lse = F(q, k, v, [0, 4], 1.0, False)
+    Z = sum(math.exp(j) for j in range(4))
+    mean_j = sum(j * math.exp(j) for j in range(4)) / Z
+    np.testing.assert_allclose(o[:, 0, 0], mean_j, rtol=1e-14)
+    np.testing.assert_allclose(o[:, 0, 1], 1.0, rtol=1e-14)
+    np.testing.assert_allclose(lse[0], math.log(Z), rtol=1e-15)
+    # causal: row i sees keys 0..i only
+    o, lse = F(q, k, v, [0, 4], 1.0, True)
+    for i in range(4):
+        Zi = sum(math.exp(j) for j in range(i + 1))
+        assert o[i, 0, 0] == pytest.approx(sum(j * math.exp(j) for j in range(i + 1)) / Zi, rel=1e-14)
+        assert lse[0, i] == pytest.approx(math.log(Zi), rel=1e-14, abs=1e-15)
+
+
+def test_scale_applies_to_scores():
+    """scale multiplies the scores: scale = 2 on keys [j,0] gives weights e^(2j)."""
+    q = np.tile([[1.0, 0.0]], (3, 1))[:, None, :]
+    k = np.array([[j, 0] for j in range(3)], float)[:, None, :]
+    v = np.array([[j, 1] for j in range(3)], float)[:, None, :]
+    o, lse = F(q, k, v, [0, 3], 2.0, False)
+    Z = sum(math.exp(2 * j) for j in range(3))
+    assert o[0, 0, 0] == pytest.approx(sum(j * math.exp(2 * j) for j in range(3)) / Z, rel=1e-14)
+    assert lse[0, 0] == pytest.approx(math.log(Z), rel=1e-15)
+
+
+# ---------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_of_p_sum_to_one(causal):
+    """With V = I (L = d) the output rows are the rows of P: >= 0, sum 1."""
+    L = 16
+    r = np.random.default_rng(1)
+    q = r.standard_normal((L, 1, L)) * 3
+    k = r.standard_normal((L, 1, L))
+    v = np.eye(L).reshape(L, 1, L)
+    o, _ = F(q, k, v, [0, L], 0.7, causal)
+    P = o[:, 0, :]
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=1e-14)
+    assert (P >= 0).all()
+    if causal:
+        assert np.all(np.triu(P, 1) == 0)
+        assert np.all(np.diag(P) > 0)
+
+
+def test_permuting_keys_and_values_together():
+    q, k, v, _ = rnd(40, 2, 2, 8, 2)
+    perm = np.random.default_rng(3).permutation(40)
+    o1, l1 = F(q, k, v, [0, 40], 0.3, False)
+    o2, l2 = F(q, k[perm], v[perm], [0, 40], 0.3, False)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=1e-13)
+    # permuting only V changes the output (catches a mis-paired PV product)
+    o3, _ = F(q, k, v[perm], [0, 40], 0.3, False)
+    assert np.abs(o3 - o1).max() > 1e-3
+
+
+def test_constant_values_reproduce_value():
+    q, k, _, _ = rnd(33, 3, 1, 8, 4)
+    vrow = np.linspace(-2, 3, 8)
+    v = np.tile(vrow, (33, 1, 1))
+    for causal in (False, True):
+        o, _ = F(q, k, v, [0, 33], 0.35, causal)
+        np.testing.assert_allclose(o, np.broadcast_to(vrow, o.shape), rtol=1e-13, atol=1e-13)
+
+
+def test_key_shift_invariance_and_lse_shift():
+    """k_j -> k_j + c leaves O unchanged and moves LSE_i by scale * q_i . c."""
+    q, k, v, _ = rnd(24, 2, 2, 8, 5)
+    c = np.random.default_rng(6).standard_normal(8)
+    scale = 0.4
+    for causal in (False, True):
+        o1, l1 = F(q, k, v, [0, 24], scale, causal)
+        o2, l2 = F(q, k + c, v, [0, 24], scale, causal)
+        np.testing.assert_allclose(o1, o2, rtol=1e-11, atol=1e-12)
+        shift = scale * np.einsum("thd,d->ht", q, c)
+        np.testing.assert_allclose(l2 - l1, shift, rtol=1e-10, atol=1e-11)
+
+
+def test_last_causal_row_equals_full_row_and_first_row_is_v0():
+    q, k, v, _ = rnd(20, 2, 2, 4, 7)
+    oc, lc = F(q, k, v, [0, 20], 0.5, True)
+    of, lf = F(q, k, v, [0, 20], 0.5, False)
+    np.testing.assert_allclose(oc[-1], of[-1], rtol=1e-14)
+    np.testing.assert_allclose(lc[:, -1], lf[:, -1], rtol=1e-14)
+    np.testing.assert_allclose(oc[0], v[0], rtol=1e-14)
+    np.testing.assert_allclose(lc[:, 0], 0.5 * np.einsum("hd,hd->h", q[0], k[0]), rtol=1e-13)
+    assert np.abs(oc[:-1] - of[:-1]).max() > 1e-3
+
+
+@pytest.mark.parametrize("case", ["wide", "same_query", "query_matches_keys"])
+def test_stress_cases_stay_finite(case):
+    """Wide score range, identical queries, a query equal to every key."""
+    q, k, v, _ = rnd(64, 2, 2, 16, 8)
+    if case == "wide":
+        q = q * 100
+    elif case == "same_query":
+        q = np.broadcast_to(q[:1], q.shape).copy()
+    else:
+        k = np.broadcast_to(k[:1], k.shape).copy() * 30
+        q = np.broadcast_to(k[:1], q.shape).copy()
+    for causal in (False, True):
+        o, lse = F(q, k, v, [0, 64], 0.25, causal)
+        assert np.isfinite(o).all() and np.isfinite(lse).all()
+        assert np.abs(o).max() <= np.abs(v).max() + 1e-12  # convex combination of V rows
+
+
+# ---------------------------------------------------------------- structure
+
+def test_gqa_equals_repeated_heads():
+    q, k, v, do = rnd(30, 8, 2, 8, 9)
+    rep = lambda x: np.repeat(x, 4, axis=1)  # consecutive grouping: kv = h // 4
+    for causal in (False, True):
+        o1, l1 = F(q, k, v, [0, 30], 0.3, causal)
+        o2, l2 = F(q, rep(k), rep(v), [0, 30], 0.3, causal)
+        np.testing.assert_allclose(o1, o2, rtol=1e-14)
+        np.testing.assert_allclose(l1, l2, rtol=1e-14)
+        dq1, dk1, dv1 = BWD(q, k, v, do, [0, 30], 0.3, causal)
+        dq2, dk2, dv2 = BWD(q, rep(k), rep(v), do, [0, 30], 0.3, causal)
+        np.testing.assert_allclose(dq1, dq2, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(dk1, dk2.reshape(30, 2, 4, 8).sum(2), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(dv1, dv2.reshape(30, 2, 4, 8).sum(2), rtol=1e-12, atol=1e-13)
+
+
+def test_varlen_equals_independent_sequences():
+    lengths = [5, 1, 17, 9]
+    cu = oracle.cu_from_lengths(lengths)
+    q, k, v, do = rnd(int(cu[-1]), 4, 2, 8, 10)
+    for causal in (False, True):
+        o, lse = F(q, k, v, cu, 0.3, causal)
+        dq, dk, dv = BWD(q, k, v, do, cu, 0.3, causal)
+        for s in range(len(lengths)):
+            a, b = cu[s], cu[s + 1]
+            os_, ls_ = F(q[a:b], k[a:b], v[a:b], [0, b - a], 0.3, causal)
+            np.testing.assert_allclose(o[a:b], os_, rtol=1e-14)
+            np.testing.assert_allclose(lse[:, a:b], ls_, rtol=1e-14)
+            g = BWD(q[a:b], k[a:b], v[a:b], do[a:b], [0, b - a], 0.3, causal)
+            for x, y in zip((dq, dk, dv), g):
+                np.testing.assert_allclose(x[a:b], y, rtol=1e-13, atol=1e-14)
+
+
+def test_empty_sequence_and_single_token():
+    cu = oracle.cu_from_lengths([0, 1, 0, 3])
+    q, k, v, do = rnd(4, 2, 1, 4, 11)
+    o, lse = F(q, k, v, cu, 0.5, True)
+    np.testing.assert_allclose(o[0], np.repeat(v[0], 2, axis=0), rtol=1e-14)  # one key: O = v
+    np.testing.assert_allclose(lse[:, 0], 0.5 * (q[0] @ k[0, 0]), rtol=1e-14)
+
+
+def test_rows_function_matches_full():
+    lengths = [37, 130, 64]
+    cu = oracle.cu_from_lengths(lengths)
+    q, k, v, _ = rnd(int(cu[-1]), 4, 2, 16, 12)
+    o, lse = F(q, k, v, cu, 0.25, True)
+    toks = np.array([0, 36, 37, 100, 166, 170, 230])
+    heads = np.array([0, 3, 1, 2, 3, 0, 1])
+    o_r, l_r = oracle.attention_forward_rows(q, k, v, cu, 0.25, True, toks, heads)
+    np.testing.assert_allclose(o_r, o[toks, heads], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(l_r, lse[heads, toks], rtol=1e-14)
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(q, k, v, do, cu, scale, causal):
+    o, _ = F(q, k, v, cu, scale, causal)
+    return float((o * do).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("heads", [(2, 2), (4, 2), (3, 1)])
+def test_backward_matches_finite_differences(causal, heads):
+    """Central differences (h = 1e-6, fp64) of L = sum(dO * O)."""
+    Hq, Hkv = heads
+    cu = oracle.cu_from_lengths([5, 3])
+    q, k, v, do = rnd(8, Hq, Hkv, 3, 13)
+    scale = 0.8
+    grads = BWD(q, k, v, do, cu, scale, causal)
+    h = 1e-6
+    for which, g in zip(range(3), grads):
+        args = [q, k, v]
+        fd = np.zeros_like(args[which])
+        it = np.nditer(args[which], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            fd[idx] = (_loss(*plus, do, cu, scale, causal) - _loss(*minus, do, cu, scale, causal)) / (2 * h)
+        err = np.linalg.norm(fd - g) / np.linalg.norm(g)
+        assert err <= 1e-6, (which, err)
+
+
+def test_backward_sum_identities():
+    """rowsum(dP*P) = rowsum(dO*O); sum_j dS_ij = 0 so sum_j dK_j = 0 per
+    (sequence, kv head)."""
+    lengths = [50, 13]
+    cu = oracle.cu_from_lengths(lengths)
+    q, k, v, do = rnd(63, 4, 2, 8, 14)
+    for causal in (False, True):
+        o, _ = F(q, k, v, cu, 0.3, causal)
+        dq, dk, dv, rs = BWD(q, k, v, do, cu, 0.3, causal, return_rowsum=True)
+        np.testing.assert_allclose(rs, np.einsum("thd,thd->ht", do, o), rtol=1e-11, atol=1e-12)
+        for s in range(2):
+            a, b = cu[s], cu[s + 1]
+            assert np.abs(dk[a:b].sum(axis=0)).max() < 1e-11 * max(1.0, np.abs(dk).max())
+
+
+def test_backward_single_key_gradients_vanish():
+    """One visible key: P = 1 exactly, so dS = 0 and dQ = dK = 0, dV = dO."""
+    q, k, v, do = rnd(1, 2, 1, 4, 15)
+    dq, dk, dv = BWD(q, k, v, do, [0, 1], 0.5, True)
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+    np.testing.assert_allclose(dv[0, 0], do[0].sum(axis=0), rtol=1e-15)
+
+
+# ---------------------------------------------------------------- tile counts
+
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 255, 256, 300, 511, 513, 1000, 1706, 4096])
+def test_tile_counts_closed_form_matches_brute_force(L):
+    for causal in (False, True):
+        assert oracle.tile_counts([L], causal)[0] == oracle.tile_counts_closed_form(L, causal)
+
+
+def test_causal_skips_about_half_of_the_tiles():
+    """"Attention 算子优化…" section 四: about half of the tiles are skipped."""
+    full = oracle.tile_counts([4096], False)[0]
+    causal = oracle.tile_counts([4096], True)[0]
+    assert full == 32 * 32
+    assert causal == 32 * 33 // 2
+    assert 0.5 <= causal / full < 0.52
