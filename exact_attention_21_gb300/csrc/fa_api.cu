@@ -1,0 +1,264 @@
+// C ABI of the attention library: argument validation, TMA descriptor setup,
+// work-grid sizing and kernel launch.  Declarations and the contract of each
+// entry point are in include/fa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_common.cuh"
+
+namespace fa {
+int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+               cudaStream_t stream);
+int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+}  // namespace fa
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+// Device status word: bits from kStatusTimeout / kStatusBadOffsets.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  int checked = 0;       // 0 = not yet, 1 = supported, -1 = unsupported
+  unsigned* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Checks the current device (compute capability 10.3) and finds its status
+// word; done once per device.
+int device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(FA_ERR_LAUNCH, "cudaGetDevice failed");
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceState& st = g_dev[dev];
+  if (st.checked == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+      st.checked = -1;
+    } else {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess)
+        return fail(FA_ERR_LAUNCH, "cudaGetSymbolAddress(status) failed");
+      st.status = static_cast<unsigned*>(addr);
+      st.checked = 1;
+    }
+  }
+  if (st.checked < 0) return fail(FA_ERR_UNSUPPORTED_DEVICE, "device %d is not compute capability 10.3", dev);
+  *out = &st;
+  return FA_OK;
+}
+
+// [T, H, d] bf16 viewed as a 3-D tensor (d, H, T); box = 64 columns x 1 head
+// x 128 tokens with the 128-byte swizzle, which is the K-major SW128 operand
+// layout the MMAs read.  Rows past T read as zeros.
+int make_map(CUtensorMap* map, const void* base, long long T, int H, int d, const char* what) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(fa::kTile)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+  return FA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Shape {
+  int B, Hq, Hkv, N, d;
+  long long T;
+  int n_tiles;  // ceil(N / 128)
+};
+
+int check_shape(int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal, const int* cu,
+                Shape* s) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return fail(FA_ERR_INVALID_ARG, "B, Hq, Hkv, N must be >= 1");
+  if (Hq % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(FA_ERR_INVALID_ARG, "d must be 64 or 128 (got %d)", d);
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (T < 1 || T > (1ll << 31) - 1) return fail(FA_ERR_INVALID_ARG, "T must be in [1, 2^31)");
+  if (cu == nullptr && T != static_cast<long long>(B) * N)
+    return fail(FA_ERR_INVALID_ARG, "batched mode needs T == B * N");
+  if (cu != nullptr && !aligned(cu, 4)) return fail(FA_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+  if (B > 65535) return fail(FA_ERR_INVALID_ARG, "B must be <= 65535");
+  if (static_cast<long long>(Hq) * T * d > (1ll << 40)) return fail(FA_ERR_INVALID_ARG, "problem too large");
+  *s = Shape{B, Hq, Hkv, N, d, T, (N + fa::kTile - 1) / fa::kTile};
+  if (s->n_tiles > 65535) return fail(FA_ERR_INVALID_ARG, "N too large");
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_last_error_string(void) { return g_err; }
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+           long long T, float scale, int causal, const int* cu_seqlens, void* stream) {
+  g_err[0] = '\0';
+  Shape s;
+  int rc = check_shape(B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, &s);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(FA_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  DeviceState* dev = nullptr;
+  if ((rc = device_state(&dev))) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_map(&tq, q, T, Hq, d, "q")) || (rc = make_map(&tk, k, T, Hkv, d, "k")) ||
+      (rc = make_map(&tv, v, T, Hkv, d, "v")))
+    return rc;
+  fa::FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu = cu_seqlens;
+  p.status = dev->status;
+  p.T = T;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.group = Hq / Hkv;
+  p.causal = causal;
+  p.n_qtiles = s.n_tiles;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  int e = fa::launch_fwd(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString((cudaError_t)e));
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int Hq, long long T, int d) {
+  if (Hq < 1 || T < 1 || d < 1) return 0;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  return up(static_cast<size_t>(Hq) * T * 4) + up(static_cast<size_t>(T) * Hq * d * 4);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
+           const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  Shape s;
+  int rc = check_shape(B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, &s);
+  if (rc) return rc;
+  if (d != 64) return fail(FA_ERR_UNSUPPORTED, "backward supports d = 64 in this build");
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return fail(FA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return fail(FA_ERR_INVALID_ARG, "bf16 tensors must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = fa_bwd_workspace_size(Hq, T, d);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  DeviceState* dev = nullptr;
+  if ((rc = device_state(&dev))) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = make_map(&tq, q, T, Hq, d, "q")) || (rc = make_map(&tk, k, T, Hkv, d, "k")) ||
+      (rc = make_map(&tv, v, T, Hkv, d, "v")) || (rc = make_map(&tdo, dout, T, Hq, d, "dout")))
+    return rc;
+  fa::BwdParams p{};
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.rowdot = static_cast<float*>(workspace);
+  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                      (static_cast<size_t>(Hq) * T * 4 + 255) / 256 * 256);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.cu = cu_seqlens;
+  p.status = dev->status;
+  p.T = T;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.group = Hq / Hkv;
+  p.causal = causal;
+  p.n_kvtiles = s.n_tiles;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  int e = fa::launch_bwd(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  if (e == -1) return fail(FA_ERR_UNSUPPORTED, "backward kernel unavailable for d = %d", d);
+  if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString((cudaError_t)e));
+  return FA_OK;
+}
+
+int fa_tile_counts(int B, const int* lengths, int causal, long long* out) {
+  g_err[0] = '\0';
+  if (B < 0 || (B > 0 && (!lengths || !out))) return fail(FA_ERR_INVALID_ARG, "bad arguments");
+  for (int s = 0; s < B; ++s) {
+    const int L = lengths[s];
+    if (L < 0) return fail(FA_ERR_INVALID_ARG, "negative length");
+    const int nq = (L + fa::kTile - 1) / fa::kTile;
+    long long n = 0;
+    for (int i = 0; i < nq; ++i) n += fa::kv_tiles_for(i, L, causal != 0);
+    out[s] = n;
+  }
+  return FA_OK;
+}
+
+int fa_stream_status(void* stream) {
+  g_err[0] = '\0';
+  DeviceState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "stream failed: %s", cudaGetErrorString(e));
+  unsigned word = 0;
+  if (cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return fail(FA_ERR_LAUNCH, "reading the status word failed");
+  if (word == 0) return FA_OK;
+  const unsigned zero = 0;
+  cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (word & fa::kStatusTimeout) return fail(FA_ERR_TIMEOUT, "a device-side wait timed out");
+  return fail(FA_ERR_INVALID_ARG, "packed sequence offsets out of range");
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Definitions shared by the attention kernels and the host launcher.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fa {
+
+// Query and key tiles are 128 x 128: 128 is the M of one tcgen05 MMA and the
+// number of TMEM lanes, so each query row owns one TMEM lane.
+constexpr int kTile = 128;
+
+// Bits of the device status word.
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBadOffsets = 2u;
+
+// Key tiles visible from query tile i of a sequence of length L: all of them
+// without a mask, else tiles 0..i (tiles right of the diagonal hold only
+// masked scores and are skipped).
+__host__ __device__ __forceinline__ int kv_tiles_for(int i, int L, bool causal) {
+  const int n = (L + kTile - 1) / kTile;
+  return causal ? (i + 1 < n ? i + 1 : n) : n;
+}
+
+// First query tile that sees key tile j.
+__host__ __device__ __forceinline__ int first_q_tile_for(int j, bool causal) {
+  return causal ? j : 0;
+}
+
+// Start token and length of sequence s; false (and a status bit) when packed
+// offsets are out of range.
+__device__ __forceinline__ bool sequence_bounds(const int* cu, int s, int N, long long T,
+                                                long long& start, int& len, unsigned* status) {
+  if (cu == nullptr) {
+    start = static_cast<long long>(s) * N;
+    len = N;
+    return true;
+  }
+  const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
+  if (a < 0 || b < a || b > T || b - a > N) {
+    atomicOr(status, kStatusBadOffsets);
+    return false;
+  }
+  start = a;
+  len = b - a;
+  return true;
+}
+
+struct FwdParams {
+  void* o;            // bf16 [T, Hq, d]
+  float* lse;         // f32 [Hq, T]
+  const int* cu;      // device int32 [B + 1] or null
+  unsigned* status;   // device status word
+  long long T;
+  int B, Hq, Hkv, N, group, causal, n_qtiles;
+  float scale_log2;   // scale * log2(e)
+};
+
+struct BwdParams {
+  const void* o;      // bf16 [T, Hq, d]
+  const void* dout;   // bf16 [T, Hq, d]
+  const float* lse;   // f32 [Hq, T]
+  float* rowdot;      // f32 [Hq, T]: D = rowsum(dO * O)
+  float* dq_acc;      // f32 [T, Hq, d]
+  void* dq;           // bf16 [T, Hq, d]
+  void* dk;           // bf16 [T, Hkv, d]
+  void* dv;           // bf16 [T, Hkv, d]
+  const int* cu;
+  unsigned* status;
+  long long T;
+  int B, Hq, Hkv, N, group, causal, n_kvtiles;
+  float scale, scale_log2;
+};
+
+}  // namespace fa

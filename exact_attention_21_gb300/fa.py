@@ -1,0 +1,153 @@
+"""ctypes binding of libfa.so: the same entry points as include/fa.h.
+
+Argument marshalling only: tensors are passed as device pointers with the
+current torch CUDA stream, and a non-zero status becomes an ``FAError``.
+Every step of the computation runs in the library's CUDA kernels; there is no
+other implementation behind these functions, and loading fails loudly when
+the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED_DEVICE = 2
+FA_ERR_LAUNCH = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_UNSUPPORTED = 5
+
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_tile_counts", "fa_stream_status",
+           "fa_last_error_string")
+
+
+class FAError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"fa error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib():
+    """Loads libfa.so once; raises if it is missing (build it first)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run exact_attention_21_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp]
+        L.fa_fwd.restype = i32
+        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp,
+                             ctypes.c_size_t, vp]
+        L.fa_bwd.restype = i32
+        L.fa_bwd_workspace_size.argtypes = [i32, i64, i32]
+        L.fa_bwd_workspace_size.restype = ctypes.c_size_t
+        L.fa_tile_counts.argtypes = [i32, ctypes.POINTER(ctypes.c_int), i32, ctypes.POINTER(ctypes.c_longlong)]
+        L.fa_tile_counts.restype = i32
+        L.fa_stream_status.argtypes = [vp]
+        L.fa_stream_status.restype = i32
+        L.fa_last_error_string.argtypes = []
+        L.fa_last_error_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(rc):
+    if rc != FA_OK:
+        raise FAError(rc, lib().fa_last_error_string().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens=None, stream=None):
+    """Forward pass into caller-allocated ``o`` [T,Hq,d] bf16 and ``lse`` [Hq,T] f32."""
+    _check(lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, T, float(scale),
+                        int(causal), _ptr(cu_seqlens), _stream(stream)))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace,
+           stream=None):
+    """Backward pass into caller-allocated ``dq``, ``dk``, ``dv`` (bf16)."""
+    _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, Hq, Hkv, N, d, T, float(scale), int(causal), _ptr(cu_seqlens), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_bwd_workspace_size(Hq, T, d):
+    return int(lib().fa_bwd_workspace_size(Hq, T, d))
+
+
+def fa_tile_counts(lengths, causal):
+    n = len(lengths)
+    arr = (ctypes.c_int * max(n, 1))(*[int(x) for x in lengths])
+    out = (ctypes.c_longlong * max(n, 1))()
+    _check(lib().fa_tile_counts(n, arr, int(causal), out))
+    return [int(out[i]) for i in range(n)]
+
+
+def fa_stream_status(stream=None):
+    """Synchronises the stream and raises on a latched device-side error."""
+    _check(lib().fa_stream_status(_stream(stream)))
+
+
+# ---------------------------------------------------------------- conveniences
+
+def attention_forward(q, k, v, causal, scale=None, cu_seqlens=None, max_seqlen=None, stream=None):
+    """Allocates o and lse with torch and calls :func:`fa_fwd`.
+
+    q [T,Hq,d], k/v [T,Hkv,d] bf16 CUDA tensors; batched mode takes
+    ``q.shape[0] == B * N`` with ``max_seqlen = N`` (default: one sequence).
+    """
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if cu_seqlens is None:
+        N = max_seqlen or T
+        B = T // N
+    else:
+        B = cu_seqlens.numel() - 1
+        N = max_seqlen
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, T, dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, causal, scale=None, cu_seqlens=None, max_seqlen=None,
+                       workspace=None, stream=None):
+    """Allocates dq, dk, dv (and the workspace if not given) and calls :func:`fa_bwd`."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if cu_seqlens is None:
+        N = max_seqlen or T
+        B = T // N
+    else:
+        B = cu_seqlens.numel() - 1
+        N = max_seqlen
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_size(Hq, T, d), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace, stream)
+    return dq, dk, dv

@@ -1,0 +1,141 @@
+/*
+ * fa.h — C ABI of the exact-attention library (libfa.so, sm_103a / GB300).
+ *
+ * The library computes exact scaled-dot-product attention
+ *     O = softmax(scale * Q K^T) V
+ * tile by tile with the online-softmax recurrence, so that the N x N score and
+ * probability matrices never reach device memory, and its gradient by
+ * recomputing each tile from the saved per-row LogSumExp.  Sources:
+ *   - "FlashAttention：从 Safe Softmax 到分块计算": section 1 (formula and
+ *     shapes), section 3.2 (merge rule of the running max m, sum l and
+ *     unnormalised output), section 5.2 (causal mask s_ij = -inf for j > i),
+ *     section 7 (tiled forward), section 8 (per-row LogSumExp kept for the
+ *     backward pass).
+ *   - "企业官网建设流程全解析" (FlashAttention data-flow notes), section 2.1
+ *     (forward loop, P = exp(S - m_new)), section 2.3 (backward:
+ *     dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dP * P))).
+ *   - "Attention 算子优化…", section 四 (causal tile skipping, recompute in
+ *     the backward pass), section 五 (GQA: consecutive groups of query heads
+ *     share one K/V head), section 二 (packed variable-length sequences).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory and keeps no pointer after a call returns.
+ *   - Element types: q, k, v, o, dO, dq, dk, dv are bfloat16 (passed as void*);
+ *     lse and workspaces are float32.
+ *   - Layout is token-major: q, o, dO, dq are [T, Hq, d] and k, v, dk, dv are
+ *     [T, Hkv, d], contiguous, head dimension innermost.  lse is [Hq, T].
+ *   - Batched mode (cu_seqlens == NULL): B sequences of N tokens, T = B * N.
+ *     Packed mode (cu_seqlens != NULL): cu_seqlens is a DEVICE int32 array of
+ *     B + 1 non-decreasing offsets with cu_seqlens[0] = 0 and
+ *     cu_seqlens[B] = T; sequence s is tokens cu_seqlens[s] .. cu_seqlens[s+1]-1
+ *     and no sequence may be longer than N.  Offsets outside [0, T] are
+ *     detected on the device: the affected sequence is skipped and the next
+ *     fa_stream_status() reports FA_ERR_INVALID_ARG.
+ *   - Query head h reads K/V head h / (Hq / Hkv).
+ *   - Causal masking uses positions relative to each sequence's start; key j
+ *     is visible from query i when j <= i.
+ *   - scale multiplies the raw scores; it must be positive and finite.
+ *   - lse is the natural-log LogSumExp of the scaled, masked scores of each
+ *     query row.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream).  Outputs are fully overwritten.  Calls on distinct buffers are
+ *     independent; calls that share an output buffer must be ordered by the
+ *     caller.
+ *
+ * Errors: every function returns 0 (FA_OK) or an FA_ERR_* code and never
+ * prints or aborts.  Argument errors are found on the host before any launch.
+ * fa_last_error_string() describes the most recent failure of the calling
+ * thread.  Device-side conditions (a bounded wait that ran out, bad packed
+ * offsets) are latched in a device word that fa_stream_status() reads.
+ */
+#ifndef EXACT_ATTENTION_FA_H
+#define EXACT_ATTENTION_FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,        /* null or misaligned pointer, bad size or shape */
+  FA_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
+  FA_ERR_LAUNCH = 3,             /* a CUDA runtime call or kernel launch failed */
+  FA_ERR_TIMEOUT = 4,            /* a device-side bounded wait gave up */
+  FA_ERR_UNSUPPORTED = 5         /* valid request this build does not implement */
+};
+
+/*
+ * Forward pass.  Tiled exact attention with the online-softmax recurrence
+ * ("FlashAttention：从 Safe Softmax 到分块计算", sections 3.2 and 7), causal
+ * tile skipping ("Attention 算子优化…", section 四), GQA and packed sequences.
+ *
+ *   q   [T, Hq, d]  bf16, 16-byte aligned          (in)
+ *   k   [T, Hkv, d] bf16, 16-byte aligned          (in)
+ *   v   [T, Hkv, d] bf16, 16-byte aligned          (in)
+ *   o   [T, Hq, d]  bf16, 16-byte aligned          (out)
+ *   lse [Hq, T]     f32, 4-byte aligned            (out)
+ *   B, Hq, Hkv, N, d: batch (or sequence count), query heads, K/V heads,
+ *       sequence length (or longest packed sequence), head dimension.
+ *       Requires B, Hq, Hkv, N >= 1, Hq % Hkv == 0, d in {64, 128}.
+ *   T   total tokens: B * N in batched mode, cu_seqlens[B] in packed mode.
+ *   scale  score multiplier (1/sqrt(d) for standard attention), > 0.
+ *   causal 0 or 1.
+ *   cu_seqlens  NULL (batched) or device int32 [B + 1] (packed).
+ *   stream      cudaStream_t.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
+           const int* cu_seqlens, void* stream);
+
+/*
+ * Backward pass.  Recomputes S and P tile by tile from the saved LSE and
+ * applies dV = P^T dO, dP = dO V^T, dS = P * (dP - D) with
+ * D = rowsum(dO * O) (equal to rowsum(dP * P)), dQ = scale dS K,
+ * dK = scale dS^T Q ("企业官网建设流程全解析", section 2.3; "Attention 算子优化…",
+ * section 四 on recomputation).  dK and dV of a K/V head are summed over the
+ * query heads that share it.
+ *
+ *   q, k, v, o, lse  as produced for / by fa_fwd with the same shape arguments (in)
+ *   dout [T, Hq, d]  bf16 upstream gradient dO                     (in)
+ *   dq [T, Hq, d], dk [T, Hkv, d], dv [T, Hkv, d]  bf16            (out)
+ *   workspace        device scratch of at least
+ *                    fa_bwd_workspace_size(Hq, T, d) bytes, 256-byte aligned;
+ *                    its contents on entry are ignored.
+ *   Other arguments as for fa_fwd.  This build supports d = 64; d = 128
+ *   returns FA_ERR_UNSUPPORTED.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv,
+           int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
+           const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_bwd needs: the row dots D (f32 [Hq, T]) and the f32 dQ
+ * accumulator ([T, Hq, d]), each rounded up to 256 bytes.  Returns 0 for
+ * non-positive arguments. */
+size_t fa_bwd_workspace_size(int Hq, long long T, int d);
+
+/*
+ * Host-side count of the (query tile, key tile) pairs the forward kernel
+ * processes per query head, for each sequence, with the kernel's 128 x 128
+ * tiles: under the causal mask tiles entirely above the diagonal are skipped
+ * ("Attention 算子优化…", section 四).  lengths: host int32 [B]; out: host
+ * int64 [B].  Uses the same tile-range function as the kernels.
+ */
+int fa_tile_counts(int B, const int* lengths, int causal, long long* out);
+
+/* Synchronises `stream`, then reports and clears the device status word:
+ * FA_ERR_TIMEOUT if a bounded wait gave up, FA_ERR_INVALID_ARG if packed
+ * offsets were out of range, FA_ERR_LAUNCH if the stream itself failed. */
+int fa_stream_status(void* stream);
+
+/* Text of the calling thread's most recent error (empty string if none). */
+const char* fa_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_FA_H */
