@@ -1,0 +1,364 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the exact-attention library on GB300.
+
+One step is one pass of the whole hot path over one batch of seeded synthetic
+input: the forward kernel, and for the forward+backward workload the backward
+call (row-dot preprocess, backward kernel, dQ postprocess).  The default
+workload is B=2, H=16, N=4096, d=64, causal, forward + backward.
+
+Prints ONE JSON line (rank 0).  ``value`` is algorithmic TFLOP/s of the whole
+job (4 L^2 d per (sequence, head) forward, halved under the causal mask,
+backward 2.5x that) with inputs resident in HBM; L2 is flushed before every
+timed step.  ``e2e`` repeats the measurement through the same C ABI with the
+inputs copied from pinned host memory and the gradients (or O) copied back
+inside the timed region.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "fwdbwd_b2_h16_n4096_d64_causal"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bitmask
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+    0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+    0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu),
+                 "--query-gpu=timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        for t, line in self.rows:
+            if self.t_on is None or not (self.t_on - 0.06 <= t <= self.t_off + 0.06):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                bits = int(parts[4], 16)
+            except (ValueError, IndexError):
+                continue
+            for b, name in THROTTLE_BITS.items():
+                if bits & b:
+                    reasons.add(name)
+        reasons.discard("gpu_idle")
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def bench_ours(args, world, rank, local):
+    import torch
+
+    import exact_attention_21_gb300.fa as fa
+    from exact_attention_21_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    fa.lib()
+    stream = torch.cuda.current_stream()
+
+    host = make_inputs(w, seed=rank)  # weak scaling: each rank its own batch
+    d, T, Hq, Hkv = w.d, w.T, w.Hq, w.Hkv
+    cu = host["cu_seqlens"].to(dev) if w.varlen else None
+    B, N = (len(w.seq_lengths), w.N) if w.varlen else (w.B, w.N)
+    q, k, v = (host[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, T, dtype=torch.float32, device=dev)
+    if w.backward:
+        do = host["do"].to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(fa.fa_bwd_workspace_size(Hq, T, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    launches_per_step = 1 + (3 if w.backward else 0)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, T, w.scale, w.causal, cu, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if w.backward:
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, w.scale, w.causal, cu, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    fa.fa_stream_status(stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_on()
+    for i in range(args.steps):
+        flush.fill_(float(i))  # evicts L2 (256 MiB > 129 MB) outside the timed events
+        step(events[i])
+    torch.cuda.synchronize()
+    sampler.mark_off()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    fa.fa_stream_status(stream)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in events]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in events]
+    step_ms = [a + b for a, b in zip(fwd_ms, bwd_ms)]
+    total_ms = sum(step_ms)
+
+    # ---- end to end: host (pinned) inputs in, result out, through the same C ABI
+    pin = {n: host[n].pin_memory() for n in host if n != "cu_seqlens"}
+    outs = ("dq", "dk", "dv") if w.backward else ("o",)
+    res_host = {n: torch.empty((T, Hq if n in ("dq", "o") else Hkv, d), dtype=torch.bfloat16).pin_memory()
+                for n in outs}
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in res_host.values())
+    e2e_steps = max(3, args.steps // 4)
+
+    def e2e_step():
+        for n, t in pin.items():
+            {"q": q, "k": k, "v": v, "do": do if w.backward else None}[n].copy_(t, non_blocking=True)
+        step()
+        src = {"dq": dq, "dk": dk, "dv": dv} if w.backward else {"o": o}
+        for n, t in res_host.items():
+            t.copy_(src[n], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        flush.fill_(0.0)
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    fa.fa_stream_status(stream)
+
+    if pg:
+        t = torch.tensor([total_ms, e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+
+    flops_step = w.fwd_flops() + (w.bwd_flops() if w.backward else 0.0)
+    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+    e2e_value = flops_step * world / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms) if w.backward else 0.0
+    if w.backward and bwd_avg > fwd_avg:
+        kern, kflops, kms = "fa_bwd (row-dot, backward kernel, dQ convert)", w.bwd_flops(), bwd_avg
+    else:
+        kern, kflops, kms = "fa_fwd_kernel", w.fwd_flops(), fwd_avg
+    achieved = kflops / (kms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"])
+    line = {
+        "metric": "attention fwd+bwd TFLOPS (bf16, 1xGB300) and % of dense BF16 tensor peak"
+        if w.backward else "attention fwd TFLOPS (bf16, 1xGB300) and % of dense BF16 tensor peak",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": d,
+                   "causal": w.causal, "seq_lengths": w.seq_lengths if w.varlen else None,
+                   "global_batch": w.B * world, "seq_len": w.N,
+                   "fwd_gflop_per_step": round(w.fwd_flops() / 1e9, 3),
+                   "bwd_gflop_per_step": round(w.bwd_flops() / 1e9, 3) if w.backward else 0.0,
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "fwd_ms": round(fwd_avg, 4),
+        "bwd_ms": round(bwd_avg, 4),
+        "pct_of_bf16_peak": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": kern, "achieved": round(achieved, 2), "peak": peak,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)", "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if args.traffic_file and os.path.exists(args.traffic_file):
+        with open(args.traffic_file) as f:
+            tr = json.load(f)
+        if tr.get("workload") == w.name and tr.get("kernel") == kern:
+            line["roofline"]["traffic"] = tr.get("bytes_per_launch")
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    if pg:
+        pg.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def oracle_sample(w, n_heads, seed=0):
+    """Runs the fp64 oracle on the first n_heads (sequence, query head) pairs of
+    workload w; returns (seconds, algorithmic flops of that sample)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from exact_attention_21_gb300.inputs import make_qkv
+
+    L = w.seq_lengths[0]
+    t = make_qkv(L, n_heads, n_heads, w.d, seed=seed, with_do=w.backward)
+    f64 = {n: t[n].to(torch.float64).numpy() for n in t}
+    cu = np.array([0, L])
+    t0 = time.perf_counter()
+    oracle.attention_forward(f64["q"], f64["k"], f64["v"], cu, w.scale, w.causal)
+    if w.backward:
+        oracle.attention_backward(f64["q"], f64["k"], f64["v"], f64["do"], cu, w.scale, w.causal)
+    sec = time.perf_counter() - t0
+    per_head = 4.0 * L * L * w.d / (2 if w.causal else 1)
+    flops = per_head * n_heads * (3.5 if w.backward else 1.0)
+    return sec, flops
+
+
+def cpu_baseline(w, budget_s=15.0):
+    sec1, fl1 = oracle_sample(w, 1)
+    n = max(1, min(w.Hq, int(budget_s / max(sec1, 1e-3))))
+    sec, fl = oracle_sample(w, n) if n > 1 else (sec1, fl1)
+    return {"value": round(fl / sec / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {w.Hq * len(w.seq_lengths)} (sequence, head) pairs of {w.name}, L={w.seq_lengths[0]}, "
+                      f"numpy fp64 (BLAS threads = all host cores)",
+            "seconds": round(sec, 3)}
+
+
+def bench_reference(args, world, rank):
+    from exact_attention_21_gb300.inputs import WORKLOADS
+
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        oracle_sample(w, 1)
+    secs, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        s, f = oracle_sample(w, 1)
+        secs += s
+        flops += f
+    value = flops / secs / 1e12
+    sample = f"1 (sequence, head) pair of {w.name} per step, numpy fp64 (BLAS threads = all host cores)"
+    return {
+        "impl": "reference",
+        "metric": "attention fwd+bwd TFLOPS (bf16, 1xGB300) and % of dense BF16 tensor peak"
+        if w.backward else "attention fwd TFLOPS (bf16, 1xGB300) and % of dense BF16 tensor peak",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                   "causal": w.causal, "parallelism": "cpu oracle, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "traffic.json"))
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = bench_reference(args, world, rank)
+    else:
+        line = bench_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,9 +1,443 @@
-// Backward kernels (placeholder until the tcgen05 backward lands).
+// Backward kernels: recompute-based attention gradient.
+//
+// What it computes ("企业官网建设流程全解析", section 2.3; "Attention 算子优化…",
+// section 四 on recomputation; "FlashAttention：从 Safe Softmax 到分块计算",
+// section 8 on the saved LSE): with D_q = rowsum(dO_q * O_q) (equal to
+// rowsum(dP * P) for that query row), for every visible (key tile j, query
+// tile i) pair of a (sequence, K/V head):
+//     S^T  = K_j Q_i^T                 P^T = exp2(S^T * c - LSE * log2 e)
+//     dP^T = V_j dO_i^T                dS^T = P^T * (dP^T - D)
+//     dV_j += P^T dO_i                 dK_j += dS^T Q_i
+//     dQ_i += dS K_j   (f32 reduce-add into a global accumulator)
+// and finally dK *= scale, dQ = scale * dQ_acc.  P is recomputed already
+// normalised from the LSE, so no running max is needed.
+//
+// Three launches: fa_bwd_rowdot_kernel (D and zeroing of the dQ accumulator),
+// fa_bwd_kernel (the five tcgen05 products per tile pair), fa_bwd_dq_kernel
+// (dQ accumulator -> bf16).
+//
+// fa_bwd_kernel: one CTA per (key tile j, K/V head, sequence); it walks the
+// query heads of the group and their query tiles, so dK and dV of the group
+// accumulate in TMEM with no atomics.  Warp roles:
+//   warp 0       producer: K_j, V_j once (TMA); per step Q_i, dO_i (TMA) and
+//                the LSE / D values of the tile (plain loads) into a ring.
+//   warp 1       TMEM allocator and MMA issuer (one thread).
+//   warps 2..5   score warpgroup: thread = key row (TMEM lane); P^T and dS^T
+//                to TMEM (bf16) and dS^T to shared memory; dK/dV epilogue.
+//   warps 6..9   dQ warpgroup: thread = query row; dQ tile from TMEM to the
+//                global f32 accumulator.
+// TMEM (d = 64): S^T [0,128) with P^T aliased on [0,64); dP^T [128,256) with
+// dS^T aliased on [128,192); dV [256,320); dK [320,384); dQ [384,448).
+#include <cuda_bf16.h>
+
 #include "fa_common.cuh"
 
 namespace fa {
-int launch_bwd(int, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-               const BwdParams&, cudaStream_t) {
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kChunkBytes = kTile * 128;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = 3;
+  static constexpr int kStatBytes = 2 * kTile * 4;  // lse2[128], rowdot[128]
+  static constexpr int kStageBytes = (2 * kTileBytes + kStatBytes + 1023) / 1024 * 1024;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffDS = kOffV + kTileBytes;       // dS^T, MN-major, 2 chunks of 64 queries
+  static constexpr int kDSBytes = 2 * kChunkBytes;
+  static constexpr int kOffRing = kOffDS + kDSBytes;
+  static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
+  // kv_full, qdo_full[], qdo_empty[], sdp_full, ps_ready, dq_full, dq_free, epi, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 7;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 256 + 2 * D;
+  static_assert(kColDQ + D <= 512, "TMEM budget");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const BwdParams p) {
+  using Lay = BwdLayout<D>;
+  constexpr int NS = Lay::kStages;
+
+  const int g = blockIdx.x;  // K/V head
+  const int kt = blockIdx.y;
+  const int s = blockIdx.z;
+  long long seq0;
+  int L;
+  if (!sequence_bounds(p.cu, s, p.N, p.T, seq0, L, p.status)) return;
+  const int k0 = kt * kTile;
+  if (k0 >= L) return;
+  const bool causal = p.causal != 0;
+  const int nqt = (L + kTile - 1) / kTile;
+  const int i0 = first_q_tile_for(kt, causal);
+  const int per_head = nqt - i0;
+  const int nsteps = p.group * per_head;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + Lay::kOffK;
+  uint8_t* sV = smem + Lay::kOffV;
+  uint8_t* sDS = smem + Lay::kOffDS;
+  uint8_t* ring = smem + Lay::kOffRing;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
+  uint64_t* kv_full = bars;
+  uint64_t* qdo_full = kv_full + 1;
+  uint64_t* qdo_empty = qdo_full + NS;
+  uint64_t* sdp_full = qdo_empty + NS;
+  uint64_t* ps_ready = sdp_full + 1;
+  uint64_t* dq_full = ps_ready + 1;
+  uint64_t* dq_free = dq_full + 1;
+  uint64_t* epi = dq_free + 1;
+  uint64_t* drain = epi + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
+
+  auto stage_q = [&](int st) { return ring + st * Lay::kStageBytes; };
+  auto stage_do = [&](int st) { return ring + st * Lay::kStageBytes + Lay::kTileBytes; };
+  auto stage_stats = [&](int st) { return reinterpret_cast<float*>(ring + st * Lay::kStageBytes + 2 * Lay::kTileBytes); };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < NS; ++i) { mbar_init(qdo_full + i, 32); mbar_init(qdo_empty + i, 1); }
+    mbar_init(sdp_full, 1);
+    mbar_init(ps_ready, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(epi, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Lay::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto give_up = [&]() {
+    atomicOr(p.status, kStatusTimeout);
+    *abort_flag = 1;
+  };
+  // step n -> (query head, query tile)
+  auto step_head = [&](int n) { return g * p.group + n / per_head; };
+  auto step_qtile = [&](int n) { return i0 + n % per_head; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * Lay::kTileBytes);
+      for (int c = 0; c < Lay::kChunks; ++c) {
+        tma_load_3d(sK + c * Lay::kChunkBytes, &tm_k, kv_full, c * 64, g, static_cast<int>(seq0 + k0));
+        tma_load_3d(sV + c * Lay::kChunkBytes, &tm_v, kv_full, c * 64, g, static_cast<int>(seq0 + k0));
+      }
+    }
+    int uses[NS] = {};
+    bool ok = true;
+    for (int n = 0; n < nsteps; ++n) {
+      const int st = n % NS;
+      if (n >= NS && !(ok = mbar_wait(qdo_empty + st, ((n / NS) - 1) & 1, abort_flag))) break;
+      const int h = step_head(n), q0 = step_qtile(n) * kTile;
+      float* stats = stage_stats(st);
+      const long long lrow = static_cast<long long>(h) * p.T + seq0 + q0;
+#pragma unroll
+      for (int t = 0; t < kTile / 32; ++t) {
+        const int idx = lane + 32 * t;
+        const bool valid = q0 + idx < L;
+        stats[idx] = valid ? __ldg(p.lse + lrow + idx) * kLog2e : INFINITY;
+        stats[kTile + idx] = valid ? __ldg(p.rowdot + lrow + idx) : 0.f;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(qdo_full + st, 2 * Lay::kTileBytes);
+        const int row = static_cast<int>(seq0 + q0);
+        for (int c = 0; c < Lay::kChunks; ++c) {
+          tma_load_3d(stage_q(st) + c * Lay::kChunkBytes, &tm_q, qdo_full + st, c * 64, h, row);
+          tma_load_3d(stage_do(st) + c * Lay::kChunkBytes, &tm_do, qdo_full + st, c * 64, h, row);
+        }
+      } else {
+        mbar_arrive(qdo_full + st);
+      }
+      ++uses[st];
+    }
+    if (!ok && lane == 0) give_up();
+    if (lane == 0) {
+      int never = 0;
+      mbar_wait(kv_full, 0, &never);
+      for (int i = 0; i < NS; ++i)
+        if (uses[i]) mbar_wait(qdo_full + i, (uses[i] - 1) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_sdp = idesc_bf16_f32(kTile, kTile, false, false);  // K-major x K-major
+      constexpr uint32_t id_dvk = idesc_bf16_f32(kTile, D, false, true);       // TMEM A x MN-major B
+      constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, true, true);         // MN-major A x MN-major B
+      const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV), sDSa = smem_u32(sDS);
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      tc_fence_after();
+      for (int n = 0; n < nsteps && ok; ++n) {
+        const int st = n % NS;
+        if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t sQa = smem_u32(stage_q(st)), sDOa = smem_u32(stage_do(st));
+        // S^T = K Q^T and dP^T = V dO^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32;
+          umma_ss(tmem + Lay::kColS, sdesc_sw128(sKa + off, 16, 1024), sdesc_sw128(sQa + off, 16, 1024), id_sdp,
+                  kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32;
+          umma_ss(tmem + Lay::kColDP, sdesc_sw128(sVa + off, 16, 1024), sdesc_sw128(sDOa + off, 16, 1024), id_sdp,
+                  kk > 0);
+        }
+        umma_commit(sdp_full);
+        if (!(ok = mbar_wait(ps_ready, n & 1, abort_flag))) break;
+        tc_fence_after();
+        // dV += P^T dO ; dK += dS^T Q   (A from TMEM, B MN-major: K = query rows)
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          umma_ts(tmem + Lay::kColDV, tmem + Lay::kColS + kk * 8,
+                  sdesc_sw128(sDOa + kk * 2048, Lay::kChunkBytes, 1024), id_dvk, (n > 0 || kk > 0));
+        }
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          umma_ts(tmem + Lay::kColDK, tmem + Lay::kColDP + kk * 8,
+                  sdesc_sw128(sQa + kk * 2048, Lay::kChunkBytes, 1024), id_dvk, (n > 0 || kk > 0));
+        }
+        umma_commit(qdo_empty + st);
+        // dQ = dS K   (A = dS^T stored key-major in smem: MN-major A; B = K, MN-major)
+        if (n > 0 && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          umma_ss(tmem + Lay::kColDQ, sdesc_sw128(sDSa + kk * 2048, Lay::kChunkBytes, 1024),
+                  sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
+        }
+        umma_commit(dq_full);
+      }
+      if (ok) umma_commit(epi);
+      if (!ok) give_up();
+      umma_commit(drain);
+      int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ score warpgroup
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // key row within the tile
+    const int kpos = k0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int n = 0; n < nsteps; ++n) {
+      const int st = n % NS;
+      if (!(ok = mbar_wait(sdp_full, n & 1, abort_flag))) break;
+      if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
+      tc_fence_after();
+      const float* lse2 = stage_stats(st);
+      const float* rowdot = lse2 + kTile;
+      const int q0 = step_qtile(n) * kTile;
+      // keys past the sequence end, and keys after the query under the mask, get P = 0
+      const bool key_ok = kpos < L;
+      const bool diag = causal && (q0 == k0);
+#pragma unroll
+      for (int cc = 0; cc < kTile / 32; ++cc) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld_x32(tmem_addr(tmem, lane_base, Lay::kColS + cc * 32), sv);
+        tmem_ld_x32(tmem_addr(tmem, lane_base, Lay::kColDP + cc * 32), dpv);
+        uint32_t pk[16], dsk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int qi = cc * 32 + 2 * t + e;
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[2 * t + e]), c, -lse2[qi]));
+            if (!key_ok || (diag && r > qi)) pv = 0.f;
+            pp[e] = pv;
+            dd[e] = pv * (__uint_as_float(dpv[2 * t + e]) - rowdot[qi]);
+          }
+          pk[t] = pack_bf16x2(pp[0], pp[1]);
+          dsk[t] = pack_bf16x2(dd[0], dd[1]);
+        }
+        // P^T and dS^T overwrite score columns this thread has already read.
+        tmem_st_x16(tmem_addr(tmem, lane_base, Lay::kColS + cc * 16), pk);
+        tmem_st_x16(tmem_addr(tmem, lane_base, Lay::kColDP + cc * 16), dsk);
+        // dS^T row r into the MN-major (query-contiguous) 128B-swizzled tile.
+        uint8_t* chunk = sDS + (cc / 2) * Lay::kChunkBytes + r * 128;
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const int u = (cc % 2) * 4 + u4;  // 16-byte unit within the 128-byte row
+          *reinterpret_cast<uint4*>(chunk + ((u ^ (r & 7)) << 4)) =
+              make_uint4(dsk[4 * u4], dsk[4 * u4 + 1], dsk[4 * u4 + 2], dsk[4 * u4 + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ps_ready);
+    }
+    if (ok) ok = mbar_wait(epi, 0, abort_flag);
+    if (!ok) {
+      give_up();
+    } else {
+      tc_fence_after();
+      const bool row_ok = kpos < L;
+      const long long tok = seq0 + kpos;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? Lay::kColDV : Lay::kColDK;
+        const float mul = which == 0 ? 1.f : p.scale;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) + (tok * p.Hkv + g) * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem_addr(tmem, lane_base, col + cc * 32), v);
+          uint32_t pk[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            pk[t] = pack_bf16x2(__uint_as_float(v[2 * t]) * mul, __uint_as_float(v[2 * t + 1]) * mul);
+          if (row_ok) {
+            uint4* o4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) o4[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ warpgroup
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // query row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
+    bool ok = true;
+    for (int n = 0; n < nsteps; ++n) {
+      if (!(ok = mbar_wait(dq_full, n & 1, abort_flag))) break;
+      tc_fence_after();
+      float acc[D];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem_addr(tmem, lane_base, Lay::kColDQ + cc * 32), v);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[cc * 32 + t] = __uint_as_float(v[t]);
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+      const int h = step_head(n), qpos = step_qtile(n) * kTile + r;
+      if (qpos < L) {
+        float* dst = p.dq_acc + ((seq0 + qpos) * p.Hq + h) * D;
+#pragma unroll
+        for (int t = 0; t < D / 4; ++t) red_add_v4(dst + 4 * t, acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
+      }
+    }
+    if (!ok) give_up();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+}
+
+// D[h, t] = sum_d dO[t, h, d] * O[t, h, d] (f32) and dQ_acc = 0.  Eight
+// threads per (token, head) row, 16 bytes each per pass.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const BwdParams p) {
+  constexpr int kPerRow = 8;
+  const long long rows = p.T * p.Hq;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / kPerRow;
+  const int sub = threadIdx.x % kPerRow;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + row * D);
+    const uint4* d4 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + row * D);
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D);
+#pragma unroll
+    for (int i = sub; i < D / 8; i += kPerRow) {
+      const uint4 a = __ldg(o4 + i), b = __ldg(d4 + i);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa2 = __bfloat1622float2(a2[e]), fb2 = __bfloat1622float2(b2[e]);
+        acc = fmaf(fa2.x, fb2.x, acc);
+        acc = fmaf(fa2.y, fb2.y, acc);
+      }
+      z[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+#pragma unroll
+  for (int off = kPerRow / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) {
+    const long long t = row / p.Hq;
+    const int h = static_cast<int>(row % p.Hq);
+    p.rowdot[static_cast<long long>(h) * p.T + t] = acc;
+  }
+}
+
+// dQ = bf16(scale * dQ_acc), eight elements per thread.
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p, long long n8) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc) + 2 * i;
+  const float4 a = src[0], b = src[1];
+  const float s = p.scale;
+  uint4 out = make_uint4(pack_bf16x2(a.x * s, a.y * s), pack_bf16x2(a.z * s, a.w * s), pack_bf16x2(b.x * s, b.y * s),
+                         pack_bf16x2(b.z * s, b.w * s));
+  reinterpret_cast<uint4*>(p.dq)[i] = out;
+}
+
+template <int D>
+int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                 const BwdParams& p, cudaStream_t stream) {
+  using Lay = BwdLayout<D>;
+  const long long rows = p.T * p.Hq;
+  const long long pre_blocks = (rows * 8 + 255) / 256;
+  fa_bwd_rowdot_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.Hkv, p.n_kvtiles, p.B);
+  fa_bwd_kernel<D><<<grid, 320, Lay::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long n8 = rows * D / 8;
+  fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
+  return cudaGetLastError();
+}
+
+int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+               const BwdParams& p, cudaStream_t stream) {
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, p, stream);
   return -1;
 }
+
 }  // namespace fa
