@@ -133,6 +133,10 @@ int check_shape(int B, int Hq, int Hkv, int N, int d, long long T, float scale, 
 
 }  // namespace
 
+namespace fa {
+int record_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace fa
+
 extern "C" {
 
 const char* fa_last_error_string(void) { return g_err; }

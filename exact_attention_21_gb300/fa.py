@@ -23,8 +23,8 @@ FA_ERR_LAUNCH = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_UNSUPPORTED = 5
 
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_tile_counts", "fa_stream_status",
-           "fa_last_error_string")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_tile_counts",
+           "fa_stream_status", "fa_last_error_string")
 
 
 class FAError(RuntimeError):
@@ -49,6 +49,9 @@ def lib():
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp,
                              ctypes.c_size_t, vp]
         L.fa_bwd.restype = i32
+        L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32,
+                                     vp, vp]
+        L.fa_bwd_noalloc.restype = i32
         L.fa_bwd_workspace_size.argtypes = [i32, i64, i32]
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
         L.fa_tile_counts.argtypes = [i32, ctypes.POINTER(ctypes.c_int), i32, ctypes.POINTER(ctypes.c_longlong)]
@@ -88,6 +91,20 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal
     _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                         B, Hq, Hkv, N, d, T, float(scale), int(causal), _ptr(cu_seqlens), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens=None,
+                   stream=None):
+    """Backward pass without a workspace argument, for callers that cannot
+    allocate device memory: the library's built-in scratch array is used
+    instead (at most FA_BWD_NOALLOC_SCRATCH_BYTES; calls share it, so calls
+    that overlap on the GPU must be ordered by the caller)."""
+    _check(lib().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                _ptr(dv), B, Hq, Hkv, N, d, T, float(scale), int(causal), _ptr(cu_seqlens),
+                                _stream(stream)))
+
+
+FA_BWD_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 def fa_bwd_workspace_size(Hq, T, d):

@@ -126,6 +126,39 @@ size_t fa_bwd_workspace_size(int Hq, long long T, int d);
  */
 int fa_tile_counts(int B, const int* lengths, int causal, long long* out);
 
+/*
+ * Backward pass for callers that cannot allocate device memory.  No passage of
+ * the source pages has a counterpart: this is a library convenience.
+ *
+ * fa_bwd needs a caller-allocated workspace.  Some callers cannot provide one
+ * at the point where they need gradients — for example code running under a
+ * runtime whose memory pool forbids cudaMalloc outside its own allocator, or a
+ * plugin inside a host program that owns all device memory.  fa_bwd_noalloc
+ * takes the same arguments as fa_bwd minus the workspace and uses instead a
+ * scratch array of FA_BWD_NOALLOC_SCRATCH_BYTES compiled into the library.
+ * It allocates nothing and calls no allocating routine.
+ *
+ *   - Size limit: fa_bwd_workspace_size(Hq, T, d) must not exceed
+ *     FA_BWD_NOALLOC_SCRATCH_BYTES; larger problems get FA_ERR_INVALID_ARG
+ *     (and a message from fa_last_error_string) and must use fa_bwd.
+ *   - The array stays resident on every GPU that loads the library until the
+ *     process exits.
+ *   - The first call on each device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps what the last call left in
+ *     it; each call re-initialises what must start at zero.  Calls whose
+ *     kernels overlap on the GPU (different streams, no ordering) race on the
+ *     array and give wrong gradients: order them.
+ *   - Other arguments, layouts and errors as for fa_bwd.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64ull * 1024ull * 1024ull)
+
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
+                   const int* cu_seqlens, void* stream);
+
 /* Synchronises `stream`, then reports and clears the device status word:
  * FA_ERR_TIMEOUT if a bounded wait gave up, FA_ERR_INVALID_ARG if packed
  * offsets were out of range, FA_ERR_LAUNCH if the stream itself failed. */
