@@ -17,7 +17,7 @@ namespace fa {
 int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                cudaStream_t stream);
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
 }  // namespace fa
 
 namespace {
@@ -99,6 +99,23 @@ int make_map(CUtensorMap* map, const void* base, long long T, int H, int d, cons
   cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(fa::kTile)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+  return FA_OK;
+}
+
+// f32 [T, H, d] accumulator viewed as (d, H, T); box = 32 columns (128 bytes)
+// x 1 head x 128 tokens with the 128-byte swizzle, the layout the backward
+// kernel stages dQ tiles in before its bulk reduce-add.
+int make_map_f32(CUtensorMap* map, void* base, long long T, int H, int d, const char* what) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(H) * d * 4};
+  cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(fa::kTile)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", what, (int)r);
@@ -202,17 +219,18 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     return fail(FA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
   DeviceState* dev = nullptr;
   if ((rc = device_state(&dev))) return rc;
-  CUtensorMap tq, tk, tv, tdo;
+  void* dq_acc = static_cast<char*>(workspace) + (static_cast<size_t>(Hq) * T * 4 + 255) / 256 * 256;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if ((rc = make_map(&tq, q, T, Hq, d, "q")) || (rc = make_map(&tk, k, T, Hkv, d, "k")) ||
-      (rc = make_map(&tv, v, T, Hkv, d, "v")) || (rc = make_map(&tdo, dout, T, Hq, d, "dout")))
+      (rc = make_map(&tv, v, T, Hkv, d, "v")) || (rc = make_map(&tdo, dout, T, Hq, d, "dout")) ||
+      (rc = make_map_f32(&tdq, dq_acc, T, Hq, d, "dq accumulator")))
     return rc;
   fa::BwdParams p{};
   p.o = o;
   p.dout = dout;
   p.lse = lse;
   p.rowdot = static_cast<float*>(workspace);
-  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                      (static_cast<size_t>(Hq) * T * 4 + 255) / 256 * 256);
+  p.dq_acc = static_cast<float*>(dq_acc);
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -228,7 +246,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   p.n_kvtiles = s.n_tiles;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  int e = fa::launch_bwd(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  int e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
   if (e == -1) return fail(FA_ERR_UNSUPPORTED, "backward kernel unavailable for d = %d", d);
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;

@@ -8,7 +8,7 @@
 //     S^T  = K_j Q_i^T                 P^T = exp2(S^T * c - LSE * log2 e)
 //     dP^T = V_j dO_i^T                dS^T = P^T * (dP^T - D)
 //     dV_j += P^T dO_i                 dK_j += dS^T Q_i
-//     dQ_i += dS K_j   (f32 reduce-add into a global accumulator)
+//     dQ_i += dS K_j   (f32 bulk reduce-add into a global accumulator)
 // and finally dK *= scale, dQ = scale * dQ_acc.  P is recomputed already
 // normalised from the LSE, so no running max is needed.
 //
@@ -17,17 +17,23 @@
 // (dQ accumulator -> bf16).
 //
 // fa_bwd_kernel: one CTA per (key tile j, K/V head, sequence); it walks the
-// query heads of the group and their query tiles, so dK and dV of the group
-// accumulate in TMEM with no atomics.  Warp roles:
+// query heads of the group and their query tiles ("steps"), so dK and dV of
+// the group accumulate in TMEM with no atomics.  Warp roles:
 //   warp 0       producer: K_j, V_j once (TMA); per step Q_i, dO_i (TMA) and
-//                the LSE / D values of the tile (plain loads) into a ring.
+//                the LSE / D values of the tile (plain loads) into a 2-stage ring.
 //   warp 1       TMEM allocator and MMA issuer (one thread).
-//   warps 2..5   score warpgroup: thread = key row (TMEM lane); P^T and dS^T
-//                to TMEM (bf16) and dS^T to shared memory; dK/dV epilogue.
-//   warps 6..9   dQ warpgroup: thread = query row; dQ tile from TMEM to the
-//                global f32 accumulator.
-// TMEM (d = 64): S^T [0,128) with P^T aliased on [0,64); dP^T [128,256) with
-// dS^T aliased on [128,192); dV [256,320); dK [320,384); dQ [384,448).
+//   warps 2..5   score warpgroup: thread = key row (TMEM lane); P^T to TMEM
+//                (bf16) and dS^T to shared memory; dK/dV epilogue.
+//   warps 6..9   dQ warpgroup: dQ tile TMEM -> swizzled shared memory -> one
+//                TMA bulk reduce-add (f32) per step.
+// MMA issue order per step n:  [wait P^T_n, dS^T_n]  S^T_{n+1}, dP^T_{n+1},
+// dV += P^T_n dO_n, dK += dS^T_n Q_n, dQ_n = dS_n K — so the score warpgroup
+// works on step n+1 while the tensor core finishes the products of step n.
+// TMEM (d = 64, 512 columns): two step regions of 128 columns (S^T f32; P^T
+// bf16 over its first 64 columns once S^T is consumed; dQ f32 in its last 64),
+// dP^T [256, 384), dV [384, 448), dK [448, 512).  dS^T lives in shared memory
+// only (double-buffered); the same swizzled tile is the K-major A operand of
+// dK (rows = keys) and the MN-major A operand of dQ (rows = queries).
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
@@ -39,37 +45,50 @@ struct BwdLayout {
   static constexpr int kChunkBytes = kTile * 128;
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 2;
   static constexpr int kStatBytes = 2 * kTile * 4;  // lse2[128], rowdot[128]
   static constexpr int kStageBytes = (2 * kTileBytes + kStatBytes + 1023) / 1024 * 1024;
+  static constexpr int kDSBytes = 2 * kChunkBytes;  // 128 keys x 128 queries bf16
+  static constexpr int kDQBytes = kTile * D * 4;    // 128 queries x D f32 staging tile
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffDS = kOffV + kTileBytes;       // dS^T, MN-major, 2 chunks of 64 queries
-  static constexpr int kDSBytes = 2 * kChunkBytes;
-  static constexpr int kOffRing = kOffDS + kDSBytes;
+  static constexpr int kOffDS = kOffV + kTileBytes;  // two buffers
+  static constexpr int kOffDQ = kOffDS + 2 * kDSBytes;
+  static constexpr int kOffRing = kOffDQ + kDQBytes;
   static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
-  // kv_full, qdo_full[], qdo_empty[], sdp_full, ps_ready, dq_full, dq_free, epi, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 7;
+  // kv_full, qdo_full[], qdo_empty[], sdp_full, ps_ready, dq_full, dq_free, dq_staged,
+  // dq_stage_free, epi, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 256 + 2 * D;
-  static_assert(kColDQ + D <= 512, "TMEM budget");
+  static constexpr uint32_t kColStep = 0;      // + 128 * (n & 1)
+  static constexpr uint32_t kColDQ = 64;       // within a step region
+  static constexpr uint32_t kColDP = 256, kColDV = 384, kColDK = 384 + D;
+  static_assert(D == 64, "TMEM plan is for d = 64");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+// f32 tile in shared memory added into global memory by the TMA unit.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
 }
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const BwdParams p) {
+              const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using Lay = BwdLayout<D>;
   constexpr int NS = Lay::kStages;
 
@@ -92,6 +111,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint8_t* sK = smem + Lay::kOffK;
   uint8_t* sV = smem + Lay::kOffV;
   uint8_t* sDS = smem + Lay::kOffDS;
+  uint8_t* sDQ = smem + Lay::kOffDQ;
   uint8_t* ring = smem + Lay::kOffRing;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
   uint64_t* kv_full = bars;
@@ -101,7 +121,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* ps_ready = sdp_full + 1;
   uint64_t* dq_full = ps_ready + 1;
   uint64_t* dq_free = dq_full + 1;
-  uint64_t* epi = dq_free + 1;
+  uint64_t* dq_staged = dq_free + 1;
+  uint64_t* dq_stage_free = dq_staged + 1;
+  uint64_t* epi = dq_stage_free + 1;
   uint64_t* drain = epi + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
@@ -118,6 +140,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(ps_ready, 128);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
+    mbar_init(dq_staged, 128);
+    mbar_init(dq_stage_free, 1);
     mbar_init(epi, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -138,6 +162,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   // step n -> (query head, query tile)
   auto step_head = [&](int n) { return g * p.group + n / per_head; };
   auto step_qtile = [&](int n) { return i0 + n % per_head; };
+  auto region = [&](int n) { return tmem + Lay::kColStep + static_cast<uint32_t>(n & 1) * 128; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -146,6 +171,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_dq);
       mbar_arrive_expect_tx(kv_full, 2 * Lay::kTileBytes);
       for (int c = 0; c < Lay::kChunks; ++c) {
         tma_load_3d(sK + c * Lay::kChunkBytes, &tm_k, kv_full, c * 64, g, static_cast<int>(seq0 + k0));
@@ -190,22 +216,17 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_sdp = idesc_bf16_f32(kTile, kTile, false, false);  // K-major x K-major
-      constexpr uint32_t id_dvk = idesc_bf16_f32(kTile, D, false, true);       // TMEM A x MN-major B
+      constexpr uint32_t id_dv = idesc_bf16_f32(kTile, D, false, true);        // TMEM A x MN-major B
+      constexpr uint32_t id_dk = idesc_bf16_f32(kTile, D, false, true);        // K-major A x MN-major B
       constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, true, true);         // MN-major A x MN-major B
       const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV), sDSa = smem_u32(sDS);
-      bool ok = mbar_wait(kv_full, 0, abort_flag);
-      tc_fence_after();
-      for (int n = 0; n < nsteps && ok; ++n) {
+      auto issue_sdp = [&](int n) {
         const int st = n % NS;
-        if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
-        tc_fence_after();
         const uint32_t sQa = smem_u32(stage_q(st)), sDOa = smem_u32(stage_do(st));
-        // S^T = K Q^T and dP^T = V dO^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32;
-          umma_ss(tmem + Lay::kColS, sdesc_sw128(sKa + off, 16, 1024), sdesc_sw128(sQa + off, 16, 1024), id_sdp,
-                  kk > 0);
+          umma_ss(region(n), sdesc_sw128(sKa + off, 16, 1024), sdesc_sw128(sQa + off, 16, 1024), id_sdp, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -214,28 +235,45 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                   kk > 0);
         }
         umma_commit(sdp_full);
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag) && mbar_wait(qdo_full, 0, abort_flag);
+      tc_fence_after();
+      if (ok) issue_sdp(0);
+      for (int n = 0; n < nsteps && ok; ++n) {
+        const int st = n % NS;
         if (!(ok = mbar_wait(ps_ready, n & 1, abort_flag))) break;
         tc_fence_after();
-        // dV += P^T dO ; dK += dS^T Q   (A from TMEM, B MN-major: K = query rows)
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          umma_ts(tmem + Lay::kColDV, tmem + Lay::kColS + kk * 8,
-                  sdesc_sw128(sDOa + kk * 2048, Lay::kChunkBytes, 1024), id_dvk, (n > 0 || kk > 0));
+        bool freed_prev = (n == 0);
+        if (n + 1 < nsteps) {
+          if (!(ok = mbar_wait(qdo_full + (n + 1) % NS, ((n + 1) / NS) & 1, abort_flag))) break;
+          // the region of step n+1 holds dQ_{n-1} until the dQ warpgroup has read it
+          if (!freed_prev) {
+            if (!(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
+            freed_prev = true;
+          }
+          tc_fence_after();
+          issue_sdp(n + 1);
         }
+        const uint32_t sQa = smem_u32(stage_q(st)), sDOa = smem_u32(stage_do(st));
+        const uint32_t dsb = sDSa + (n & 1) * Lay::kDSBytes;
+        // dV += P^T dO  (A: P^T in TMEM; B: dO rows = queries = K, MN-major)
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          umma_ts(tmem + Lay::kColDK, tmem + Lay::kColDP + kk * 8,
-                  sdesc_sw128(sQa + kk * 2048, Lay::kChunkBytes, 1024), id_dvk, (n > 0 || kk > 0));
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ts(tmem + Lay::kColDV, region(n) + kk * 8, sdesc_sw128(sDOa + kk * 2048, Lay::kChunkBytes, 1024),
+                  id_dv, (n > 0 || kk > 0));
+        // dK += dS^T Q  (A: dS^T tile, rows = keys, K-major; B: Q rows = K, MN-major)
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ss(tmem + Lay::kColDK, sdesc_sw128(dsb + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
+                  sdesc_sw128(sQa + kk * 2048, Lay::kChunkBytes, 1024), id_dk, (n > 0 || kk > 0));
         umma_commit(qdo_empty + st);
-        // dQ = dS K   (A = dS^T stored key-major in smem: MN-major A; B = K, MN-major)
-        if (n > 0 && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
+        if (!freed_prev && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
         tc_fence_after();
+        // dQ_n = dS K  (A: the same dS^T tile read query-major, MN-major; B: K rows = K, MN-major)
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          umma_ss(tmem + Lay::kColDQ, sdesc_sw128(sDSa + kk * 2048, Lay::kChunkBytes, 1024),
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
                   sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
-        }
         umma_commit(dq_full);
       }
       if (ok) umma_commit(epi);
@@ -251,46 +289,53 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int kpos = k0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
     const float c = p.scale_log2;
+    const bool key_ok = kpos < L;
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
       const int st = n % NS;
       if (!(ok = mbar_wait(sdp_full, n & 1, abort_flag))) break;
       if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
       tc_fence_after();
-      const float* lse2 = stage_stats(st);
-      const float* rowdot = lse2 + kTile;
+      const float4* lse4 = reinterpret_cast<const float4*>(stage_stats(st));
+      const float4* dot4 = lse4 + kTile / 4;
       const int q0 = step_qtile(n) * kTile;
-      // keys past the sequence end, and keys after the query under the mask, get P = 0
-      const bool key_ok = kpos < L;
-      const bool diag = causal && (q0 == k0);
+      // Keys past the sequence end and keys after the query (diagonal tile,
+      // causal) get P = 0; queries past the end carry LSE = +inf, so P = 0.
+      const bool masked = !key_ok || (causal && q0 == k0);
+      const int key_lim = key_ok ? r : -1;  // visible iff query index >= key_lim (diagonal tile)
+      uint8_t* ds_row = sDS + (n & 1) * Lay::kDSBytes + r * 128;
+      const uint32_t reg = region(n);
 #pragma unroll
       for (int cc = 0; cc < kTile / 32; ++cc) {
         uint32_t sv[32], dpv[32];
-        tmem_ld_x32(tmem_addr(tmem, lane_base, Lay::kColS + cc * 32), sv);
+        tmem_ld_x32(tmem_addr(reg, lane_base, cc * 32), sv);
         tmem_ld_x32(tmem_addr(tmem, lane_base, Lay::kColDP + cc * 32), dpv);
         uint32_t pk[16], dsk[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          float pp[2], dd[2];
+        for (int t4 = 0; t4 < 8; ++t4) {
+          const float4 l4 = lse4[cc * 8 + t4], d4 = dot4[cc * 8 + t4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pp[4], dd[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int qi = cc * 32 + 2 * t + e;
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[2 * t + e]), c, -lse2[qi]));
-            if (!key_ok || (diag && r > qi)) pv = 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int qi = cc * 32 + 4 * t4 + e;
+            float pv = ex2_approx(fmaf(__uint_as_float(sv[4 * t4 + e]), c, -lv[e]));
+            if (masked && qi < (key_ok ? key_lim : kTile + 1)) pv = 0.f;
             pp[e] = pv;
-            dd[e] = pv * (__uint_as_float(dpv[2 * t + e]) - rowdot[qi]);
+            dd[e] = pv * (__uint_as_float(dpv[4 * t4 + e]) - dv4[e]);
           }
-          pk[t] = pack_bf16x2(pp[0], pp[1]);
-          dsk[t] = pack_bf16x2(dd[0], dd[1]);
+          pk[2 * t4] = pack_bf16x2(pp[0], pp[1]);
+          pk[2 * t4 + 1] = pack_bf16x2(pp[2], pp[3]);
+          dsk[2 * t4] = pack_bf16x2(dd[0], dd[1]);
+          dsk[2 * t4 + 1] = pack_bf16x2(dd[2], dd[3]);
         }
-        // P^T and dS^T overwrite score columns this thread has already read.
-        tmem_st_x16(tmem_addr(tmem, lane_base, Lay::kColS + cc * 16), pk);
-        tmem_st_x16(tmem_addr(tmem, lane_base, Lay::kColDP + cc * 16), dsk);
-        // dS^T row r into the MN-major (query-contiguous) 128B-swizzled tile.
-        uint8_t* chunk = sDS + (cc / 2) * Lay::kChunkBytes + r * 128;
+        // P^T overwrites S^T columns this thread has already read.
+        tmem_st_x16(tmem_addr(reg, lane_base, cc * 16), pk);
+        // dS^T row r into the 128B-swizzled tile (query-contiguous rows).
+        uint8_t* chunk = ds_row + (cc / 2) * Lay::kChunkBytes;
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
-          const int u = (cc % 2) * 4 + u4;  // 16-byte unit within the 128-byte row
+          const int u = (cc % 2) * 4 + u4;
           *reinterpret_cast<uint4*>(chunk + ((u ^ (r & 7)) << 4)) =
               make_uint4(dsk[4 * u4], dsk[4 * u4 + 1], dsk[4 * u4 + 2], dsk[4 * u4 + 3]);
         }
@@ -333,27 +378,40 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
+    const bool issuer = (warp == 6 && lane == 0);
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
       if (!(ok = mbar_wait(dq_full, n & 1, abort_flag))) break;
+      // the previous reduce has finished reading the staging tile
+      if (n > 0 && !(ok = mbar_wait(dq_stage_free, (n - 1) & 1, abort_flag))) break;
       tc_fence_after();
-      float acc[D];
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t v[32];
-        tmem_ld_x32(tmem_addr(tmem, lane_base, Lay::kColDQ + cc * 32), v);
+        tmem_ld_x32(tmem_addr(region(n), lane_base, Lay::kColDQ + cc * 32), v);
+        // f32 box of 32 columns x 128 rows, 128-byte swizzle
+        uint8_t* row = sDQ + cc * (kTile * 128) + r * 128;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) acc[cc * 32 + t] = __uint_as_float(v[t]);
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4)) = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
       }
       tc_fence_before();
       mbar_arrive(dq_free);
-      const int h = step_head(n), qpos = step_qtile(n) * kTile + r;
-      if (qpos < L) {
-        float* dst = p.dq_acc + ((seq0 + qpos) * p.Hq + h) * D;
-#pragma unroll
-        for (int t = 0; t < D / 4; ++t) red_add_v4(dst + 4 * t, acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(dq_staged);
+      if (issuer) {
+        if (!(ok = mbar_wait(dq_staged, n & 1, abort_flag))) break;
+        // Rows past the sequence end hold exact zeros (P = 0 there), so the
+        // whole tile can be added; rows past T are clipped by the TMA unit.
+        const int h = step_head(n), q0 = step_qtile(n) * kTile;
+        for (int cc = 0; cc < D / 32; ++cc)
+          tma_reduce_add_3d(&tm_dq, sDQ + cc * (kTile * 128), cc * 32, h, static_cast<int>(seq0 + q0));
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(dq_stage_free);
       }
     }
+    if (issuer) bulk_wait_group0();
     if (!ok) give_up();
   }
 
@@ -416,7 +474,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p, long 
 
 template <int D>
 int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                 const BwdParams& p, cudaStream_t stream) {
+                 const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
   using Lay = BwdLayout<D>;
   const long long rows = p.T * p.Hq;
   const long long pre_blocks = (rows * 8 + 255) / 256;
@@ -426,7 +484,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Hkv, p.n_kvtiles, p.B);
-  fa_bwd_kernel<D><<<grid, 320, Lay::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  fa_bwd_kernel<D><<<grid, 320, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long n8 = rows * D / 8;
@@ -435,8 +493,8 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 }
 
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-               const BwdParams& p, cudaStream_t stream) {
-  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, p, stream);
+               const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, p, stream);
   return -1;
 }
 
