@@ -20,17 +20,21 @@
 // query heads of the group and their query tiles ("steps"), so dK and dV of
 // the group accumulate in TMEM with no atomics.  Warp roles:
 //   warp 0       producer: K_j, V_j once (TMA); per step Q_i, dO_i (TMA) and
-//                the LSE / D values of the tile (plain loads) into a 2-stage ring.
+//                the LSE / D values of the tile (plain loads) into a 3-stage ring.
 //   warp 1       TMEM allocator and MMA issuer (one thread).
-//   warps 2..5   score warpgroup: thread = key row (TMEM lane); P^T to TMEM
-//                (bf16) and dS^T to shared memory; dK/dV epilogue.
-//   warps 6..9   dQ warpgroup: dQ tile TMEM -> swizzled shared memory -> one
-//                TMA bulk reduce-add (f32) per step.
+//   warps 2..9   two score warpgroups: thread = key row (TMEM lane); the
+//                first takes query columns 0..63, the second 64..127; P^T to
+//                TMEM (bf16) and dS^T to shared memory; dV / dK epilogue.
+//   warps 10..13 dQ warpgroup: dQ tile TMEM -> swizzled shared memory -> TMA
+//                bulk reduce-add (f32), in two 32-column halves per step.
 // MMA issue order per step n:  [wait P^T_n, dS^T_n]  S^T_{n+1}, dP^T_{n+1},
 // dV += P^T_n dO_n, dK += dS^T_n Q_n, dQ_n = dS_n K — so the score warpgroup
 // works on step n+1 while the tensor core finishes the products of step n.
 // TMEM (d = 64, 512 columns): two step regions of 128 columns (S^T f32; P^T
-// bf16 over its first 64 columns once S^T is consumed; dQ f32 in its last 64),
+// bf16 for queries 0..63 over columns 0..31 and for queries 64..127 over
+// columns 64..95, each written by the warpgroup that read those S^T columns;
+// dQ f32 over columns 64..127, written by an MMA issued after the dV product
+// that reads P^T),
 // dP^T [256, 384), dV [384, 448), dK [448, 512).  dS^T lives in shared memory
 // only (double-buffered); the same swizzled tile is the K-major A operand of
 // dK (rows = keys) and the MN-major A operand of dQ (rows = queries).
@@ -45,11 +49,11 @@ struct BwdLayout {
   static constexpr int kChunkBytes = kTile * 128;
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = 2;
+  static constexpr int kStages = 3;
   static constexpr int kStatBytes = 2 * kTile * 4;  // lse2[128], rowdot[128]
   static constexpr int kStageBytes = (2 * kTileBytes + kStatBytes + 1023) / 1024 * 1024;
   static constexpr int kDSBytes = 2 * kChunkBytes;  // 128 keys x 128 queries bf16
-  static constexpr int kDQBytes = kTile * D * 4;    // 128 queries x D f32 staging tile
+  static constexpr int kDQBytes = kTile * 32 * 4;   // 128 queries x 32 f32 staging half-tile
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffDS = kOffV + kTileBytes;  // two buffers
@@ -85,7 +89,7 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
@@ -137,7 +141,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(kv_full, 1);
     for (int i = 0; i < NS; ++i) { mbar_init(qdo_full + i, 32); mbar_init(qdo_empty + i, 1); }
     mbar_init(sdp_full, 1);
-    mbar_init(ps_ready, 128);
+    mbar_init(ps_ready, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
     mbar_init(dq_staged, 128);
@@ -184,25 +188,32 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const int st = n % NS;
       if (n >= NS && !(ok = mbar_wait(qdo_empty + st, ((n / NS) - 1) & 1, abort_flag))) break;
       const int h = step_head(n), q0 = step_qtile(n) * kTile;
-      float* stats = stage_stats(st);
-      const long long lrow = static_cast<long long>(h) * p.T + seq0 + q0;
-#pragma unroll
-      for (int t = 0; t < kTile / 32; ++t) {
-        const int idx = lane + 32 * t;
-        const bool valid = q0 + idx < L;
-        stats[idx] = valid ? __ldg(p.lse + lrow + idx) * kLog2e : INFINITY;
-        stats[kTile + idx] = valid ? __ldg(p.rowdot + lrow + idx) : 0.f;
-      }
       if (lane == 0) {
-        mbar_arrive_expect_tx(qdo_full + st, 2 * Lay::kTileBytes);
+        // tiles first, so their latency overlaps the plain loads below
+        mbar_expect_tx(qdo_full + st, 2 * Lay::kTileBytes);
         const int row = static_cast<int>(seq0 + q0);
         for (int c = 0; c < Lay::kChunks; ++c) {
           tma_load_3d(stage_q(st) + c * Lay::kChunkBytes, &tm_q, qdo_full + st, c * 64, h, row);
           tma_load_3d(stage_do(st) + c * Lay::kChunkBytes, &tm_do, qdo_full + st, c * 64, h, row);
         }
-      } else {
-        mbar_arrive(qdo_full + st);
       }
+      float* stats = stage_stats(st);
+      const long long lrow = static_cast<long long>(h) * p.T + seq0 + q0;
+      float lv[kTile / 32], dv[kTile / 32];
+#pragma unroll
+      for (int t = 0; t < kTile / 32; ++t) {
+        const int idx = lane + 32 * t;
+        const bool valid = q0 + idx < L;
+        lv[t] = valid ? __ldg(p.lse + lrow + idx) : INFINITY;
+        dv[t] = valid ? __ldg(p.rowdot + lrow + idx) : 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < kTile / 32; ++t) {
+        // stored negated: -LSE * log2 e and -D (queries past the end: P = 0)
+        stats[lane + 32 * t] = -lv[t] * kLog2e;
+        stats[kTile + lane + 32 * t] = -dv[t];
+      }
+      mbar_arrive(qdo_full + st);
       ++uses[st];
     }
     if (!ok && lane == 0) give_up();
@@ -259,8 +270,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // dV += P^T dO  (A: P^T in TMEM; B: dO rows = queries = K, MN-major)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tmem + Lay::kColDV, region(n) + kk * 8, sdesc_sw128(sDOa + kk * 2048, Lay::kChunkBytes, 1024),
-                  id_dv, (n > 0 || kk > 0));
+          umma_ts(tmem + Lay::kColDV, region(n) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                  sdesc_sw128(sDOa + kk * 2048, Lay::kChunkBytes, 1024), id_dv, (n > 0 || kk > 0));
         // dK += dS^T Q  (A: dS^T tile, rows = keys, K-major; B: Q rows = K, MN-major)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
@@ -282,13 +293,15 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int never = 0;
       mbar_wait(drain, 0, &never);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ score warpgroup
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ score warpgroups
+    const int half = (warp - 2) / 4;  // query columns [64 * half, 64 * half + 64)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // key row within the tile
     const int kpos = k0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
     const float c = p.scale_log2;
+    const float2 c2 = make_float2(c, c);
     const bool key_ok = kpos < L;
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
@@ -296,47 +309,43 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (!(ok = mbar_wait(sdp_full, n & 1, abort_flag))) break;
       if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
       tc_fence_after();
-      const float4* lse4 = reinterpret_cast<const float4*>(stage_stats(st));
-      const float4* dot4 = lse4 + kTile / 4;
+      const float2* nlse2 = reinterpret_cast<const float2*>(stage_stats(st)) + half * 32;
+      const float2* ndot2 = nlse2 + kTile / 2;
       const int q0 = step_qtile(n) * kTile;
       // Keys past the sequence end and keys after the query (diagonal tile,
-      // causal) get P = 0; queries past the end carry LSE = +inf, so P = 0.
-      const bool masked = !key_ok || (causal && q0 == k0);
-      const int key_lim = key_ok ? r : -1;  // visible iff query index >= key_lim (diagonal tile)
-      uint8_t* ds_row = sDS + (n & 1) * Lay::kDSBytes + r * 128;
+      // causal) get P = 0: query columns below zero_below are zeroed.
+      // Queries past the end carry -LSE = -inf, so their P is 0 already.
+      const int zero_below = !key_ok ? kTile : ((causal && q0 == k0) ? r : 0);
+      uint8_t* ds_row = sDS + (n & 1) * Lay::kDSBytes + half * Lay::kChunkBytes + r * 128;
       const uint32_t reg = region(n);
 #pragma unroll
-      for (int cc = 0; cc < kTile / 32; ++cc) {
+      for (int cl = 0; cl < 2; ++cl) {
+        const int col0 = half * 64 + cl * 32;  // first query column of this chunk
         uint32_t sv[32], dpv[32];
-        tmem_ld_x32(tmem_addr(reg, lane_base, cc * 32), sv);
-        tmem_ld_x32(tmem_addr(tmem, lane_base, Lay::kColDP + cc * 32), dpv);
+        tmem_ld_x32_pair(tmem_addr(reg, lane_base, col0), sv, tmem_addr(tmem, lane_base, Lay::kColDP + col0), dpv);
         uint32_t pk[16], dsk[16];
+        const bool mask_chunk = zero_below > col0;
 #pragma unroll
-        for (int t4 = 0; t4 < 8; ++t4) {
-          const float4 l4 = lse4[cc * 8 + t4], d4 = dot4[cc * 8 + t4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pp[4], dd[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int qi = cc * 32 + 4 * t4 + e;
-            float pv = ex2_approx(fmaf(__uint_as_float(sv[4 * t4 + e]), c, -lv[e]));
-            if (masked && qi < (key_ok ? key_lim : kTile + 1)) pv = 0.f;
-            pp[e] = pv;
-            dd[e] = pv * (__uint_as_float(dpv[4 * t4 + e]) - dv4[e]);
+        for (int t = 0; t < 16; ++t) {
+          const float2 nl = nlse2[cl * 16 + t], nd = ndot2[cl * 16 + t];
+          const float2 x = fma2(make_float2(__uint_as_float(sv[2 * t]), __uint_as_float(sv[2 * t + 1])), c2, nl);
+          float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (mask_chunk) {
+            if (col0 + 2 * t < zero_below) pv.x = 0.f;
+            if (col0 + 2 * t + 1 < zero_below) pv.y = 0.f;
           }
-          pk[2 * t4] = pack_bf16x2(pp[0], pp[1]);
-          pk[2 * t4 + 1] = pack_bf16x2(pp[2], pp[3]);
-          dsk[2 * t4] = pack_bf16x2(dd[0], dd[1]);
-          dsk[2 * t4 + 1] = pack_bf16x2(dd[2], dd[3]);
+          const float2 dd =
+              mul2(pv, add2(make_float2(__uint_as_float(dpv[2 * t]), __uint_as_float(dpv[2 * t + 1])), nd));
+          pk[t] = pack_bf16x2(pv.x, pv.y);
+          dsk[t] = pack_bf16x2(dd.x, dd.y);
         }
         // P^T overwrites S^T columns this thread has already read.
-        tmem_st_x16(tmem_addr(reg, lane_base, cc * 16), pk);
+        tmem_st_x16(tmem_addr(reg, lane_base, half * 64 + cl * 16), pk);
         // dS^T row r into the 128B-swizzled tile (query-contiguous rows).
-        uint8_t* chunk = ds_row + (cc / 2) * Lay::kChunkBytes;
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
-          const int u = (cc % 2) * 4 + u4;
-          *reinterpret_cast<uint4*>(chunk + ((u ^ (r & 7)) << 4)) =
+          const int u = cl * 4 + u4;
+          *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
               make_uint4(dsk[4 * u4], dsk[4 * u4 + 1], dsk[4 * u4 + 2], dsk[4 * u4 + 3]);
         }
       }
@@ -350,26 +359,24 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       give_up();
     } else {
       tc_fence_after();
+      // first warpgroup stores dV, second stores dK (scaled)
       const bool row_ok = kpos < L;
       const long long tok = seq0 + kpos;
+      const uint32_t col = half == 0 ? Lay::kColDV : Lay::kColDK;
+      const float mul = half == 0 ? 1.f : p.scale;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? p.dv : p.dk) + (tok * p.Hkv + g) * D;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? Lay::kColDV : Lay::kColDK;
-        const float mul = which == 0 ? 1.f : p.scale;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) + (tok * p.Hkv + g) * D;
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem_addr(tmem, lane_base, col + cc * 32), v);
+        uint32_t pk[16];
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld_x32(tmem_addr(tmem, lane_base, col + cc * 32), v);
-          uint32_t pk[16];
+        for (int t = 0; t < 16; ++t)
+          pk[t] = pack_bf16x2(__uint_as_float(v[2 * t]) * mul, __uint_as_float(v[2 * t + 1]) * mul);
+        if (row_ok) {
+          uint4* o4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
-          for (int t = 0; t < 16; ++t)
-            pk[t] = pack_bf16x2(__uint_as_float(v[2 * t]) * mul, __uint_as_float(v[2 * t + 1]) * mul);
-          if (row_ok) {
-            uint4* o4 = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) o4[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
-          }
+          for (int t = 0; t < 4; ++t) o4[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
         }
       }
     }
@@ -378,37 +385,39 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
-    const bool issuer = (warp == 6 && lane == 0);
+    const bool issuer = (warp == 10 && lane == 0);
     bool ok = true;
-    for (int n = 0; n < nsteps; ++n) {
+    for (int n = 0; n < nsteps && ok; ++n) {
       if (!(ok = mbar_wait(dq_full, n & 1, abort_flag))) break;
-      // the previous reduce has finished reading the staging tile
-      if (n > 0 && !(ok = mbar_wait(dq_stage_free, (n - 1) & 1, abort_flag))) break;
       tc_fence_after();
+      uint32_t v[D];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem_addr(region(n), lane_base, Lay::kColDQ + cc * 32), v);
-        // f32 box of 32 columns x 128 rows, 128-byte swizzle
-        uint8_t* row = sDQ + cc * (kTile * 128) + r * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4)) = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-      }
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld_x32(tmem_addr(region(n), lane_base, Lay::kColDQ + cc * 32), v + 32 * cc);
       tc_fence_before();
       mbar_arrive(dq_free);
-      fence_proxy_async_smem();
-      mbar_arrive(dq_staged);
-      if (issuer) {
-        if (!(ok = mbar_wait(dq_staged, n & 1, abort_flag))) break;
-        // Rows past the sequence end hold exact zeros (P = 0 there), so the
-        // whole tile can be added; rows past T are clipped by the TMA unit.
-        const int h = step_head(n), q0 = step_qtile(n) * kTile;
-        for (int cc = 0; cc < D / 32; ++cc)
-          tma_reduce_add_3d(&tm_dq, sDQ + cc * (kTile * 128), cc * 32, h, static_cast<int>(seq0 + q0));
-        bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(dq_stage_free);
+      const int h = step_head(n), q0 = step_qtile(n) * kTile;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        const int use = n * (D / 32) + cc;  // staging-tile use counter
+        // the previous reduce has finished reading the staging tile
+        if (use > 0 && !(ok = mbar_wait(dq_stage_free, (use - 1) & 1, abort_flag))) break;
+        // f32 box of 32 columns x 128 rows, 128-byte swizzle
+        uint8_t* row = sDQ + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4)) =
+              make_uint4(v[32 * cc + 4 * u], v[32 * cc + 4 * u + 1], v[32 * cc + 4 * u + 2], v[32 * cc + 4 * u + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(dq_staged);
+        if (issuer) {
+          if (!(ok = mbar_wait(dq_staged, use & 1, abort_flag))) break;
+          // Rows past the sequence end hold exact zeros (P = 0 there), so the
+          // whole tile can be added; rows past T are clipped by the TMA unit.
+          tma_reduce_add_3d(&tm_dq, sDQ, cc * 32, h, static_cast<int>(seq0 + q0));
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(dq_stage_free);
+        }
       }
     }
     if (issuer) bulk_wait_group0();
@@ -484,7 +493,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Hkv, p.n_kvtiles, p.B);
-  fa_bwd_kernel<D><<<grid, 320, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+  fa_bwd_kernel<D><<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long n8 = rows * D / 8;
