@@ -47,7 +47,18 @@ def test_fwd_packed_ragged(cuda_device, d, causal):
 
 
 def test_fwd_wide_scores_stay_finite(cuda_device):
-    check_case(600, 2, 2, 64, True, seed=3, q_mult=8.0)
+    """Queries scaled by 8: the softmax is nearly one-hot, so O is close to a
+    single V row and |O| reaches 4-5.  Rounding O to bf16 (8 significant
+    bits) then costs up to 2^-9 |O| on its own, above the 1e-2 absolute bound
+    the N(0,1) workloads use, so this case allows 1e-2 + 2^-8 |O_ref| per
+    element (one more half-ulp of headroom for the accumulation)."""
+    t = make_qkv(600, 2, 2, 64, seed=3, q_mult=8.0)
+    o, lse = run_fwd(t["q"], t["k"], t["v"], True)
+    o_ref, lse_ref = oracle.attention_forward(f64(t["q"]), f64(t["k"]), f64(t["v"]), [0, 600], 0.125, True)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert (np.abs(o - o_ref) <= 1e-2 + 2.0 ** -8 * np.abs(o_ref)).all()
+    assert np.abs(o - o_ref).mean() <= 1e-3
+    assert np.abs(lse - lse_ref).max() <= 1e-3
 
 
 def test_fwd_workload_small(cuda_device):
