@@ -27,9 +27,11 @@
 //                TMEM (bf16) and dS^T to shared memory; dV / dK epilogue.
 //   warps 10..13 dQ warpgroup: dQ tile TMEM -> swizzled shared memory -> TMA
 //                bulk reduce-add (f32), in two 32-column halves per step.
-// MMA issue order per step n:  [wait P^T_n, dS^T_n]  S^T_{n+1}, dP^T_{n+1},
-// dV += P^T_n dO_n, dK += dS^T_n Q_n, dQ_n = dS_n K — so the score warpgroup
-// works on step n+1 while the tensor core finishes the products of step n.
+// MMA issue order: once the score warpgroups finish step n, dV += P^T_n dO_n,
+// dK += dS^T_n Q_n, dQ_n = dS_n K; then, as soon as the score warpgroups of
+// step n+1 have read their dP^T and the dQ of step n has been read out,
+// S^T_{n+2} and dP^T_{n+2}.  The scores of the next step are thus computed
+// while the score warpgroups still work on the current one.
 // TMEM (d = 64, 512 columns): two step regions of 128 columns (S^T f32; P^T
 // bf16 for queries 0..63 over columns 0..31 and for queries 64..127 over
 // columns 64..95, each written by the warpgroup that read those S^T columns;
@@ -60,9 +62,9 @@ struct BwdLayout {
   static constexpr int kOffDQ = kOffDS + 2 * kDSBytes;
   static constexpr int kOffRing = kOffDQ + kDQBytes;
   static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
-  // kv_full, qdo_full[], qdo_empty[], sdp_full, ps_ready, dq_full, dq_free, dq_staged,
-  // dq_stage_free, epi, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 9;
+  // kv_full, qdo_full[], qdo_empty[], sdp_full, ps_ready, dp_free, dq_full, dq_free,
+  // dq_staged, dq_stage_free, epi, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 10;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -123,7 +125,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* qdo_empty = qdo_full + NS;
   uint64_t* sdp_full = qdo_empty + NS;
   uint64_t* ps_ready = sdp_full + 1;
-  uint64_t* dq_full = ps_ready + 1;
+  uint64_t* dp_free = ps_ready + 1;
+  uint64_t* dq_full = dp_free + 1;
   uint64_t* dq_free = dq_full + 1;
   uint64_t* dq_staged = dq_free + 1;
   uint64_t* dq_stage_free = dq_staged + 1;
@@ -142,6 +145,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int i = 0; i < NS; ++i) { mbar_init(qdo_full + i, 32); mbar_init(qdo_empty + i, 1); }
     mbar_init(sdp_full, 1);
     mbar_init(ps_ready, 256);
+    mbar_init(dp_free, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
     mbar_init(dq_staged, 128);
@@ -247,24 +251,26 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         umma_commit(sdp_full);
       };
-      bool ok = mbar_wait(kv_full, 0, abort_flag) && mbar_wait(qdo_full, 0, abort_flag);
+      // S^T_m and dP^T_m need: the Q/dO stage of step m, the dP^T region
+      // released by the score warpgroups of step m-1 (they arrive on dp_free
+      // once their last dP^T load is done), and the step region of m-2,
+      // whose dQ the dQ warpgroup must have read.
+      auto issue_next = [&](int m) -> bool {
+        if (!mbar_wait(qdo_full + m % NS, (m / NS) & 1, abort_flag)) return false;
+        if (m >= 1 && !mbar_wait(dp_free, (m - 1) & 1, abort_flag)) return false;
+        if (m >= 2 && !mbar_wait(dq_free, (m - 2) & 1, abort_flag)) return false;
+        tc_fence_after();
+        issue_sdp(m);
+        return true;
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
       tc_fence_after();
-      if (ok) issue_sdp(0);
+      if (ok) ok = issue_next(0);
+      if (ok && nsteps > 1) ok = issue_next(1);
       for (int n = 0; n < nsteps && ok; ++n) {
         const int st = n % NS;
         if (!(ok = mbar_wait(ps_ready, n & 1, abort_flag))) break;
         tc_fence_after();
-        bool freed_prev = (n == 0);
-        if (n + 1 < nsteps) {
-          if (!(ok = mbar_wait(qdo_full + (n + 1) % NS, ((n + 1) / NS) & 1, abort_flag))) break;
-          // the region of step n+1 holds dQ_{n-1} until the dQ warpgroup has read it
-          if (!freed_prev) {
-            if (!(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
-            freed_prev = true;
-          }
-          tc_fence_after();
-          issue_sdp(n + 1);
-        }
         const uint32_t sQa = smem_u32(stage_q(st)), sDOa = smem_u32(stage_do(st));
         const uint32_t dsb = sDSa + (n & 1) * Lay::kDSBytes;
         // dV += P^T dO  (A: P^T in TMEM; B: dO rows = queries = K, MN-major)
@@ -278,14 +284,14 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           umma_ss(tmem + Lay::kColDK, sdesc_sw128(dsb + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
                   sdesc_sw128(sQa + kk * 2048, Lay::kChunkBytes, 1024), id_dk, (n > 0 || kk > 0));
         umma_commit(qdo_empty + st);
-        if (!freed_prev && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        // dQ_n = dS K  (A: the same dS^T tile read query-major, MN-major; B: K rows = K, MN-major)
+        // dQ_n = dS K into the step region of n, whose dQ_{n-2} was read before
+        // S^T_n was issued  (A: the dS^T tile read query-major, MN-major; B: K, MN-major)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
                   sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
         umma_commit(dq_full);
+        if (n + 2 < nsteps && !(ok = issue_next(n + 2))) break;
       }
       if (ok) umma_commit(epi);
       if (!ok) give_up();
@@ -323,6 +329,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int col0 = half * 64 + cl * 32;  // first query column of this chunk
         uint32_t sv[32], dpv[32];
         tmem_ld_x32_pair(tmem_addr(reg, lane_base, col0), sv, tmem_addr(tmem, lane_base, Lay::kColDP + col0), dpv);
+        if (cl == 1) {
+          // dP^T fully read: the next step's dP^T may overwrite it
+          tc_fence_before();
+          mbar_arrive(dp_free);
+        }
         uint32_t pk[16], dsk[16];
         const bool mask_chunk = zero_below > col0;
 #pragma unroll

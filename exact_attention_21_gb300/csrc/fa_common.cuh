@@ -54,6 +54,7 @@ struct FwdParams {
   unsigned* status;   // device status word
   long long T;
   int B, Hq, Hkv, N, group, causal, n_qtiles;
+  int group_pairs;    // (sequence, head) pairs per scheduling group
   float scale_log2;   // scale * log2(e)
 };
 

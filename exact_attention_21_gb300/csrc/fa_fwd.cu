@@ -17,21 +17,38 @@
 // The merge rule holds for any common reference, so the result is the same
 // exact attention; this only skips O rescales that would multiply by nearly 1.
 //
-// One CTA owns two consecutive 128-row query tiles of one (query head,
-// sequence).  Warp roles:
-//   warp 0      TMA producer: both Q tiles once, then K_j and V_j through rings.
-//   warp 1      TMEM allocator and MMA issuer (one thread).
-//   warps 2..5  softmax of query tile 0; warps 6..9 softmax of query tile 1.
-//               Thread t of a warpgroup owns query row 32 * (warp % 4) + lane,
-//               i.e. that TMEM lane, so row max and row sum stay in-thread;
-//               each warpgroup also rescales its O and writes its output.
-// MMA order: S0_0, S1_0, then per key tile j: PV0_j, S0_{j+1}, PV1_j, S1_{j+1}.
-// While one warpgroup turns S_t into P_t, the tensor core works on the other
-// tile, so the exponentials overlap the matrix products.
+// The kernel is persistent: one CTA per SM walks work units (128-row query
+// tile, query head, sequence) in heavy-first order, keeping its TMEM,
+// barriers and K/V ring across units so each unit's loads overlap the previous
+// unit's tail.  On
+// GB300 the tcgen05 MMAs of one issuing thread run one after another (about
+// 130 cycles per 128-row instruction, whatever N), so the products are split
+// over two issuers and the score tile is triple-buffered: S of the next key
+// tiles is computed while the softmax works on the current one and P V of the
+// previous one runs.  Warp roles:
+//   warp 0       TMA producer for Q (per unit) and K_j;
+//   warp 3       TMA producer for V_j.  Separate threads, so a K load never
+//                waits behind a V ring slot that P V has not released yet.
+//   warp 1       TMEM allocator and S issuer: S_j = Q K_j^T into buffer j % 3.
+//   warp 2       P V issuer: O += P_j V_j (P_j read from TMEM).
+//   warps 4..7   softmax, key columns 0..63 of each score tile;
+//   warps 8..11  softmax, key columns 64..127.
+//                Thread t of each softmax warpgroup owns query row
+//                32 * (warp % 4) + lane (that TMEM lane).  The two
+//                warpgroups exchange their partial row maxima through shared
+//                memory once per key tile, so both use the same reference;
+//                each keeps its own partial row sum, rescales its half of O
+//                and writes its half of the output.
 //
-// TMEM (512 columns): S0 [0, 128), S1 [128, 256) (each with its bf16 P over
-// its first 64 columns once read), O0 [256, 256 + d), O1 [256 + d, 256 + 2d).
+// TMEM (512 columns): S buffers [0, 128), [128, 256), [256, 384) (bf16 P over
+// the first 64 columns of a buffer once read: keys 0..63 in columns 0..31,
+// keys 64..127 in columns 32..63), O [384, 384 + d).
 #include <cuda_bf16.h>
+
+#include <array>
+#include <map>
+#include <mutex>
+#include <vector>
 
 #include "fa_common.cuh"
 
@@ -42,18 +59,25 @@ struct FwdLayout {
   static constexpr int kChunkBytes = kTile * 128;          // 128 rows x 64 bf16 (one SW128 box)
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;  // one 128 x D bf16 tile
-  static constexpr int kStagesK = D == 128 ? 2 : 4;
-  static constexpr int kStagesV = D == 128 ? 2 : 3;
-  static constexpr int kOffQ = 0;  // two query tiles
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  // d = 128: one Q buffer (the next unit's Q loads under the current unit's
+  // tail) so that K gets three stages; d = 64 has room for two.
+  static constexpr int kQBufs = D == 128 ? 1 : 2;
+  static constexpr int kStagesK = D == 128 ? 3 : 4;
+  static constexpr int kStagesV = D == 128 ? 2 : 4;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBufs * kTileBytes;
   static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
-  // q_full, k_full[], k_empty[], v_full[], v_empty[], s_full[2], p_full[2], o_final[2], drain
-  static constexpr int kNumBars = 1 + 2 * kStagesK + 2 * kStagesV + 2 + 2 + 2 + 1;
+  static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // row-max exchange [2 parity][2 halves][128]
+  static constexpr int kOffL = kOffX + 2 * 2 * kTile * 4;      // final row-sum exchange [2 parity][2 halves][128]
+  static constexpr int kOffBar = kOffL + 2 * 2 * kTile * 4;
+  static constexpr int kSBufs = 3;
+  // q_full[2], q_empty[2], k_full[], k_empty[], v_full[], v_empty[], s_full[3], s_free[3],
+  // p_full[3], pv_done[2], xchg, o_final, o_free, drain
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 3 * kSBufs + 2 + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColO = 256;
+  static constexpr uint32_t kColS = 0, kColO = 384;
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -61,53 +85,84 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // P values stay below 2^8 between rescales
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Lay = FwdLayout<D>;
   constexpr int NK = Lay::kStagesK, NV = Lay::kStagesV;
 
-  const int h = blockIdx.x;
-  const int pair = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // longest rows first
-  const int s = blockIdx.z;
-  long long seq0;
-  int L;
-  if (!sequence_bounds(p.cu, s, p.N, p.T, seq0, L, p.status)) return;
-  const int q0 = pair * 2 * kTile;
-  if (q0 >= L) return;  // uniform across the CTA
   const bool causal = p.causal != 0;
-  // key tiles seen by each query tile (0 when the tile starts past the end)
-  const int nkv0 = kv_tiles_for(2 * pair, L, causal);
-  const int nkv1 = q0 + kTile < L ? kv_tiles_for(2 * pair + 1, L, causal) : 0;
-  const int nkv = nkv0 > nkv1 ? nkv0 : nkv1;
-  const int kvh = h / p.group;
+  // Work units: (sequence, query head) pairs are taken in groups of kGroup
+  // (chosen by the host)
+  // (consecutive heads, so query heads sharing a K/V head stay together); within
+  // a group the query tiles go heavy-first (last tile down), so the K/V being
+  // read at any time is one group's and stays in L2.  CTA i takes the units i,
+  // 2G-1-i, 2G+i, ... of that order (G = gridDim.x), which balances the causal
+  // work to within a few per cent.  Units past the end of their sequence are
+  // skipped by every role alike.
+  const int kGroup = p.group_pairs;
+  const int n_pairs = p.Hq * p.B;
+  const int n_units = n_pairs * p.n_qtiles;
+  const int G = static_cast<int>(gridDim.x);
+  auto unit_of = [&](int k) { return k * G + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x)); };
+  struct Unit {
+    long long seq0;
+    int L, h, qt, q0, nkv, kvh;
+  };
+  auto unit_at = [&](int u, Unit& w) -> bool {
+    const int gi = u / (kGroup * p.n_qtiles);  // only the last group can be short
+    const int gp = min(kGroup, n_pairs - gi * kGroup);
+    const int r = u - gi * kGroup * p.n_qtiles;
+    const int pair = gi * kGroup + r % gp;
+    w.qt = p.n_qtiles - 1 - r / gp;
+    w.h = pair % p.Hq;
+    const int sq = pair / p.Hq;
+    if (!sequence_bounds(p.cu, sq, p.N, p.T, w.seq0, w.L, p.status)) return false;
+    w.q0 = w.qt * kTile;
+    if (w.q0 >= w.L) return false;
+    w.nkv = kv_tiles_for(w.qt, w.L, causal);
+    w.kvh = w.h / p.group;
+    return true;
+  };
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Lay::kOffQ;
   uint8_t* sK = smem + Lay::kOffK;
   uint8_t* sV = smem + Lay::kOffV;
+  float* xmax = reinterpret_cast<float*>(smem + Lay::kOffX);
+  float* xsum = reinterpret_cast<float*>(smem + Lay::kOffL);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
   uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* k_full = q_empty + 2;
   uint64_t* k_empty = k_full + NK;
   uint64_t* v_full = k_empty + NK;
   uint64_t* v_empty = v_full + NV;
+  constexpr int NB = Lay::kSBufs;
   uint64_t* s_full = v_empty + NV;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_final = p_full + 2;
-  uint64_t* drain = o_final + 2;
+  uint64_t* s_free = s_full + NB;
+  uint64_t* p_full = s_free + NB;
+  uint64_t* pv_done = p_full + NB;  // two, alternating by key-tile parity
+  uint64_t* xchg = pv_done + 2;
+  uint64_t* o_final = xchg + 1;
+  uint64_t* o_free = o_final + 1;
+  uint64_t* drain = o_free + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(q_full + i, 1); mbar_init(q_empty + i, 1); }
     for (int i = 0; i < NK; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
     for (int i = 0; i < NV; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 128); mbar_init(o_final + i, 1); }
-    mbar_init(drain, 1);
+    for (int i = 0; i < NB; ++i) { mbar_init(s_full + i, 1); mbar_init(s_free + i, 1); mbar_init(p_full + i, 256); }
+    for (int i = 0; i < 2; ++i) mbar_init(pv_done + i, 1);
+    mbar_init(xchg, 256);
+    mbar_init(o_final, 1);
+    mbar_init(o_free, 256);
+    mbar_init(drain, 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -125,197 +180,262 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     *abort_flag = 1;
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(q_full, 2 * Lay::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_load_3d(sQ + t * Lay::kTileBytes + c * Lay::kChunkBytes, &tm_q, q_full, c * 64, h,
-                      static_cast<int>(seq0 + q0 + t * kTile));
-      int k_uses[NK] = {}, v_uses[NV] = {};
+      const bool is_k = warp == 0;  // warp 0: Q and K; warp 3: V
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+      } else {
+        tma_prefetch_desc(&tm_v);
+      }
+      int k_uses[NK] = {}, v_uses[NV] = {}, q_uses[2] = {};
+      int jg = 0, uc = 0;  // key tiles and units so far
       bool ok = true;
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int row_k = static_cast<int>(seq0 + j * kTile);
-        const int ks = j % NK, vs = j % NV;
-        if (j >= NK && !(ok = mbar_wait(k_empty + ks, ((j / NK) - 1) & 1, abort_flag))) break;
-        mbar_arrive_expect_tx(k_full + ks, Lay::kTileBytes);
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_load_3d(sK + ks * Lay::kTileBytes + c * Lay::kChunkBytes, &tm_k, k_full + ks, c * 64, kvh, row_k);
-        ++k_uses[ks];
-        if (j >= NV && !(ok = mbar_wait(v_empty + vs, ((j / NV) - 1) & 1, abort_flag))) break;
-        mbar_arrive_expect_tx(v_full + vs, Lay::kTileBytes);
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_load_3d(sV + vs * Lay::kTileBytes + c * Lay::kChunkBytes, &tm_v, v_full + vs, c * 64, kvh, row_k);
-        ++v_uses[vs];
+      for (int k = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++k)) {
+        Unit w;
+        if (!unit_at(u, w)) continue;
+        if (is_k) {
+          const int qb = uc % Lay::kQBufs, qn = uc / Lay::kQBufs;
+          if (qn >= 1 && !(ok = mbar_wait(q_empty + qb, (qn - 1) & 1, abort_flag))) break;
+          mbar_arrive_expect_tx(q_full + qb, Lay::kTileBytes);
+          for (int c = 0; c < Lay::kChunks; ++c)
+            tma_load_3d(sQ + qb * Lay::kTileBytes + c * Lay::kChunkBytes, &tm_q, q_full + qb, c * 64, w.h,
+                        static_cast<int>(w.seq0 + w.q0));
+          ++q_uses[qb];
+        }
+        ++uc;
+        for (int j = 0; j < w.nkv; ++j, ++jg) {
+          const int row_k = static_cast<int>(w.seq0 + j * kTile);
+          if (is_k) {
+            const int ks = jg % NK;
+            if (jg >= NK && !(ok = mbar_wait(k_empty + ks, ((jg / NK) - 1) & 1, abort_flag))) break;
+            mbar_arrive_expect_tx(k_full + ks, Lay::kTileBytes);
+            for (int c = 0; c < Lay::kChunks; ++c)
+              tma_load_3d(sK + ks * Lay::kTileBytes + c * Lay::kChunkBytes, &tm_k, k_full + ks, c * 64, w.kvh,
+                          row_k);
+            ++k_uses[ks];
+          } else {
+            const int vs = jg % NV;
+            if (jg >= NV && !(ok = mbar_wait(v_empty + vs, ((jg / NV) - 1) & 1, abort_flag))) break;
+            mbar_arrive_expect_tx(v_full + vs, Lay::kTileBytes);
+            for (int c = 0; c < Lay::kChunks; ++c)
+              tma_load_3d(sV + vs * Lay::kTileBytes + c * Lay::kChunkBytes, &tm_v, v_full + vs, c * 64, w.kvh,
+                          row_k);
+            ++v_uses[vs];
+          }
+        }
       }
       if (!ok) give_up();
       // Every copy this thread issued has landed before the CTA may exit.
       int never = 0;
-      mbar_wait(q_full, 0, &never);
+      for (int i = 0; i < Lay::kQBufs; ++i)
+        if (q_uses[i]) mbar_wait(q_full + i, (q_uses[i] - 1) & 1, &never);
       for (int i = 0; i < NK; ++i)
         if (k_uses[i]) mbar_wait(k_full + i, (k_uses[i] - 1) & 1, &never);
       for (int i = 0; i < NV; ++i)
         if (v_uses[i]) mbar_wait(v_full + i, (v_uses[i] - 1) & 1, &never);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, false, true);
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
-      const int nkv_t[2] = {nkv0, nkv1};
-      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T into S region t
-        const uint32_t kbase = sKa + (j % NK) * Lay::kTileBytes, qbase = sQa + t * Lay::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32;
-          umma_ss(tmem + Lay::kColS + t * kTile, sdesc_sw128(qbase + off, 16, 1024),
-                  sdesc_sw128(kbase + off, 16, 1024), idesc_s, kk > 0);
-        }
-        umma_commit(s_full + t);
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag) && mbar_wait(k_full, 0, abort_flag);
-      tc_fence_after();
-      if (ok) {
-        for (int t = 0; t < 2; ++t)
-          if (nkv_t[t] > 0) issue_s(t, 0);
-        umma_commit(k_empty);
-      }
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int vs = j % NV;
-        bool v_ready = false, k_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nkv_t[t]) continue;
-          if (!(ok = mbar_wait(p_full + t, j & 1, abort_flag))) break;
-          if (!v_ready && !(ok = v_ready = mbar_wait(v_full + vs, (j / NV) & 1, abort_flag))) break;
+      // Descriptors are built once; a K step only moves the start address.
+      const uint64_t q_desc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(smem_u32(sK), 16, 1024);
+      int g = 0, uc = 0;  // score tiles and units so far
+      bool ok = true;
+      for (int k = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++k)) {
+        Unit w;
+        if (!unit_at(u, w)) continue;
+        const int qb = uc % Lay::kQBufs;
+        if (!(ok = mbar_wait(q_full + qb, (uc / Lay::kQBufs) & 1, abort_flag))) break;
+        ++uc;
+        const uint64_t qd = q_desc + static_cast<uint64_t>((qb * Lay::kTileBytes) >> 4);
+        for (int j = 0; j < w.nkv; ++j, ++g) {
+          const int b = g % NB, ks = g % NK;
+          if (!(ok = mbar_wait(k_full + ks, (g / NK) & 1, abort_flag))) break;
+          // buffer b still holds the P of score tile g-NB until P V has read it
+          if (g >= NB && !(ok = mbar_wait(s_free + b, ((g / NB) - 1) & 1, abort_flag))) break;
           tc_fence_after();
-          const uint32_t a_tm = tmem + Lay::kColS + t * kTile;  // P_t, bf16 pairs
-          const uint32_t vbase = sVa + vs * Lay::kTileBytes;
+          const uint64_t kd = k_desc + static_cast<uint64_t>((ks * Lay::kTileBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts(tmem + Lay::kColO + t * D, a_tm + kk * 8, sdesc_sw128(vbase + kk * 2048, Lay::kChunkBytes, 1024),
-                    idesc_o, (j > 0 || kk > 0));
-          if (j + 1 < nkv_t[t]) {
-            // S_t of the next key tile overwrites P_t after the product above has read it
-            if (!k_ready && !(ok = k_ready = mbar_wait(k_full + (j + 1) % NK, ((j + 1) / NK) & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_s(t, j + 1);
-          } else {
-            umma_commit(o_final + t);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(((kk / 4) * Lay::kChunkBytes + (kk % 4) * 32) >> 4);
+            umma_ss(tmem + Lay::kColS + b * kTile, qd + off, kd + off, idesc_s, kk > 0);
           }
+          umma_commit(s_full + b);
+          umma_commit(k_empty + ks);
         }
-        if (!ok) break;
-        umma_commit(v_empty + vs);
-        if (k_ready) umma_commit(k_empty + (j + 1) % NK);
+        if (ok) umma_commit(q_empty + qb);
       }
       if (!ok) give_up();
-      // Drain: every MMA issued above completes before TMEM is released.
       umma_commit(drain);
       int never = 0;
       mbar_wait(drain, 0, &never);
     }
-  } else {
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, false, true);
+      const uint64_t v_desc = sdesc_sw128(smem_u32(sV), Lay::kChunkBytes, 1024);
+      int g = 0, uc = 0;  // score tiles and units so far
+      bool ok = true;
+      for (int k = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++k)) {
+        Unit w;
+        if (!unit_at(u, w)) continue;
+        // O of the previous unit must have been read out before P V restarts it
+        if (uc >= 1 && !(ok = mbar_wait(o_free, (uc - 1) & 1, abort_flag))) break;
+        ++uc;
+        for (int j = 0; j < w.nkv; ++j, ++g) {
+          const int b = g % NB, vs = g % NV;
+          if (!(ok = mbar_wait(p_full + b, (g / NB) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(v_full + vs, (g / NV) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint64_t vd = v_desc + static_cast<uint64_t>((vs * Lay::kTileBytes) >> 4);
+          const uint32_t a_tm = tmem + Lay::kColS + b * kTile;  // P, bf16 pairs
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ts(tmem + Lay::kColO, a_tm + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_o,
+                    (j > 0 || kk > 0));
+          umma_commit(s_free + b);
+          umma_commit(v_empty + vs);
+          umma_commit(pv_done + (g & 1));
+        }
+        if (ok) umma_commit(o_final);
+      }
+      if (!ok) give_up();
+      umma_commit(drain);
+      int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) / 4;  // query tile of this warpgroup
+    const int half = (warp - 4) / 4;  // key columns [64 * half, 64 * half + 64)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int qt = 2 * pair + t;
-    const int qpos = qt * kTile + r;
-    const int my_nkv = t == 0 ? nkv0 : nkv1;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
-    const uint32_t tS = tmem + Lay::kColS + t * kTile, tO = tmem + Lay::kColO + t * D;
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
-    float m = -INFINITY, l = 0.f;  // reference max (log2 units) and row sum against it
+    int g = 0, uc = 0, xp = 0;  // score tiles, units and exchange phases so far
     bool ok = true;
-    for (int j = 0; j < my_nkv; ++j) {
-      if (!(ok = mbar_wait(s_full + t, j & 1, abort_flag))) break;
+    for (int k = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++k)) {
+      Unit w;
+      if (!unit_at(u, w)) continue;
+      const int qpos = w.q0 + r;
+      float m = -INFINITY, l = 0.f;  // reference max (log2 units) and this half's row sum against it
+      for (int j = 0; j < w.nkv; ++j, ++g) {
+        const int b = g % NB;
+        const uint32_t tS = tmem + Lay::kColS + b * kTile;
+        if (!(ok = mbar_wait(s_full + b, (g / NB) & 1, abort_flag))) break;
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld_x64(tmem_addr(tS, lane_base, half * 64), sr);
+        float* x = reinterpret_cast<float*>(sr);
+        const int k0 = j * kTile + half * 64;
+        if ((causal && j == w.qt) || (k0 + 64 > w.L)) {
+          const int lim = causal ? min(qpos + 1, w.L) : w.L;  // visible keys: [0, lim)
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (k0 + i >= lim) x[i] = -INFINITY;
+        }
+        float mx[4] = {fmaxf(x[0], x[1]), fmaxf(x[2], x[3]), fmaxf(x[4], x[5]), fmaxf(x[6], x[7])};
+#pragma unroll
+        for (int i = 8; i < 64; i += 8) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) mx[t] = max3(mx[t], x[i + 2 * t], x[i + 2 * t + 1]);
+        }
+        // exchange the partial row max with the other half (double-buffered by phase)
+        float* xm = xmax + ((xp & 1) * 2) * kTile;
+        xm[half * kTile + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        mbar_arrive(xchg);
+        if (!(ok = mbar_wait(xchg, xp & 1, abort_flag))) break;
+        ++xp;
+        const float mt = fmaxf(xm[r], xm[kTile + r]) * c;
+        // move the reference only when the row max grows past the slack
+        const bool bump = mt > m + kRescaleSlack;
+        const float m_new = bump ? mt : m;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = bump ? ex2_approx(m - m_use) : 1.f;
+        const float2 nm = make_float2(-m_use, -m_use);
+        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float2 e = fma2(make_float2(x[cc * 32 + 2 * t], x[cc * 32 + 2 * t + 1]), c2, nm);
+            const float2 pv = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+            sum2[t & 3] = add2(sum2[t & 3], pv);
+            pk[t] = pack_bf16x2(pv.x, pv.y);
+          }
+          // P for keys [64 half + 32 cc, +32) goes to columns [32 half + 16 cc, +16);
+          // every thread of both halves read its scores before the exchange above.
+          tmem_st_x16(tmem_addr(tS, lane_base, half * 32 + cc * 16), pk);
+        }
+        const float2 s01 = add2(sum2[0], sum2[1]), s23 = add2(sum2[2], sum2[3]);
+        l = l * alpha + ((s01.x + s01.y) + (s23.x + s23.y));
+        m = m_new;
+        if (j > 0 && __any_sync(0xffffffffu, bump)) {
+          // O may only be rescaled once P V of the previous key tile has landed
+          // (P V of tile g-NB is done, so the barrier of tile g-1's parity is at
+          // most one phase behind: its parity identifies the phase)
+          if (!(ok = mbar_wait(pv_done + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t ov[32];
+            const uint32_t ta = tmem_addr(tmem + Lay::kColO, lane_base, half * (D / 2) + cc * 32);
+            tmem_ld_x32(ta, ov);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
+            tmem_st_x32(ta, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + b);
+      }
+      if (!ok) break;
+      // ---- epilogue of this unit
+      if (!(ok = mbar_wait(o_final, uc & 1, abort_flag))) break;
+      ++uc;
+      // combine the two halves' row sums
+      xsum[(xp & 1) * kTile * 2 + half * kTile + r] = l;
+      mbar_arrive(xchg);
+      if (!(ok = mbar_wait(xchg, xp & 1, abort_flag))) break;
+      const float lt = xsum[(xp & 1) * kTile * 2 + r] + xsum[(xp & 1) * kTile * 2 + kTile + r];
+      ++xp;
       tc_fence_after();
-      uint32_t sr[kTile];
-      tmem_ld_x128(tmem_addr(tS, lane_base, 0), sr);
-      float* x = reinterpret_cast<float*>(sr);
-      const int k0 = j * kTile;
-      const bool need_mask = (causal && j == qt) || (k0 + kTile > L);
-      if (need_mask) {
-        const int lim = causal ? min(qpos + 1, L) : L;  // visible keys: [0, lim)
+      uint32_t ov[D / 2];
 #pragma unroll
-        for (int i = 0; i < kTile; ++i)
-          if (k0 + i >= lim) x[i] = -INFINITY;
-      }
-      float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]);
-#pragma unroll
-      for (int i = 4; i < kTile; i += 4) {
-        mx0 = max3(mx0, x[i], x[i + 1]);
-        mx1 = max3(mx1, x[i + 2], x[i + 3]);
-      }
-      const float mt = fmaxf(mx0, mx1) * c;
-      // move the reference only when the row max grows past the slack
-      const bool bump = mt > m + kRescaleSlack;
-      const float m_new = bump ? mt : m;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = bump ? ex2_approx(m - m_use) : 1.f;
-      const float2 nm = make_float2(-m_use, -m_use);
-      float2 sum2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float2 e = fma2(make_float2(x[cc * 32 + 2 * u], x[cc * 32 + 2 * u + 1]), c2, nm);
-          const float2 pv = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-          sum2 = add2(sum2, pv);
-          pk[u] = pack_bf16x2(pv.x, pv.y);
-        }
-        tmem_st_x16(tmem_addr(tS, lane_base, cc * 16), pk);
-      }
-      l = l * alpha + (sum2.x + sum2.y);
-      m = m_new;
-      // O was last written by P V of the previous key tile, which completed
-      // before S of this tile (same issuing thread, committed after it).
-      if (j > 0 && __any_sync(0xffffffffu, bump)) {
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t ov[32];
-          const uint32_t ta = tmem_addr(tO, lane_base, cc * 32);
-          tmem_ld_x32(ta, ov);
-#pragma unroll
-          for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * alpha);
-          tmem_st_x32(ta, ov);
-        }
-      }
-      tmem_st_wait();
+      for (int cc = 0; cc < D / 64; ++cc)
+        tmem_ld_x32(tmem_addr(tmem + Lay::kColO, lane_base, half * (D / 2) + cc * 32), ov + 32 * cc);
+      // O is in registers: the next unit's P V may start overwriting it
       tc_fence_before();
-      mbar_arrive(p_full + t);
-    }
-    if (ok && my_nkv > 0) ok = mbar_wait(o_final + t, 0, abort_flag);
-    if (!ok) {
-      give_up();
-    } else if (my_nkv > 0) {
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool row_ok = qpos < L;
-      const long long tok = seq0 + qpos;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + h) * D;
+      mbar_arrive(o_free);
+      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+      const bool row_ok = qpos < w.L;
+      const long long tok = w.seq0 + qpos;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + w.h) * D + half * (D / 2);
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t ov[32];
-        tmem_ld_x32(tmem_addr(tO, lane_base, cc * 32), ov);
+      for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t pk[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          pk[u] = pack_bf16x2(__uint_as_float(ov[2 * u]) * inv_l, __uint_as_float(ov[2 * u + 1]) * inv_l);
+        for (int t = 0; t < 16; ++t)
+          pk[t] = pack_bf16x2(__uint_as_float(ov[32 * cc + 2 * t]) * inv_l, __uint_as_float(ov[32 * cc + 2 * t + 1]) * inv_l);
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          for (int t = 0; t < 4; ++t) dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
         }
       }
-      if (row_ok) p.lse[static_cast<long long>(h) * p.T + tok] = l > 0.f ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
+      if (row_ok && half == 0)
+        p.lse[static_cast<long long>(w.h) * p.T + tok] = lt > 0.f ? (m + lg2_approx(lt)) * kLn2 : -INFINITY;
     }
+    if (!ok) give_up();
   }
 
   tc_fence_before();
@@ -326,6 +446,65 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   }
 }
 
+// Scheduling group size (in (sequence, head) pairs) for the persistent grid.
+// Batched inputs: simulate the kernel's snake assignment of the grouped,
+// heavy-first unit order for a few group sizes and keep the one with the
+// smallest busiest-CTA load (ties: the smaller group, for L2 locality), among
+// groups whose K/V fits in 48 MB.  Packed inputs (lengths on the device): 16.
+static int simulate_group_pairs(const FwdParams& p, int G, int d);
+
+static int choose_group_pairs(const FwdParams& p, int G, int d) {
+  const int n_pairs = p.Hq * p.B;
+  if (p.cu != nullptr || G > 1024 || static_cast<long long>(n_pairs) * p.n_qtiles > (1 << 22))
+    return n_pairs < 16 ? n_pairs : 16;
+  // one simulation per shape, cached
+  static std::mutex mu;
+  static std::map<std::array<int, 8>, int> cache;
+  const std::array<int, 8> key = {p.Hq, p.B, p.N, p.n_qtiles, p.causal, p.group, G, d};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const int gs = simulate_group_pairs(p, G, d);
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = gs;
+  return gs;
+}
+
+static int simulate_group_pairs(const FwdParams& p, int G, int d) {
+  const int n_pairs = p.Hq * p.B;
+  const int nq = p.n_qtiles;
+  const int L = p.N;
+  const long long kv_bytes_per_pair = 2ll * L * d * 2 / p.group;  // K and V, shared by the query group
+  const int cands[] = {8, 16, 24, 32, 48, 64, 96, 128, 1 << 30};
+  int best = n_pairs;
+  double best_load = 1e300;
+  std::vector<double> load(G);
+  for (int gs0 : cands) {
+    const int gs = gs0 < n_pairs ? gs0 : n_pairs;
+    if (gs * kv_bytes_per_pair > (48ll << 20) && gs != cands[0]) continue;
+    for (int i = 0; i < G; ++i) load[i] = 0.0;
+    const int n_units = n_pairs * nq;
+    for (int u = 0; u < n_units; ++u) {
+      const int gi = u / (gs * nq), gp = (gs < n_pairs - gi * gs) ? gs : n_pairs - gi * gs;
+      const int r = u - gi * gs * nq;
+      const int qt = nq - 1 - r / gp;
+      const int k = u / G, i = u % G;
+      const int cta = (k & 1) ? G - 1 - i : i;
+      load[cta] += (p.causal ? (qt + 1 < nq ? qt + 1 : nq) : nq) + 0.3;  // + per-unit overhead
+    }
+    double mx = 0.0;
+    for (int i = 0; i < G; ++i) mx = load[i] > mx ? load[i] : mx;
+    if (mx < best_load * 0.995) {
+      best_load = mx;
+      best = gs;
+    }
+    if (gs == n_pairs) break;
+  }
+  return best;
+}
+
 // Host-side launch for one head dimension; returns a cudaError_t value.
 template <int D>
 int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
@@ -333,10 +512,14 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   using Lay = FwdLayout<D>;
   cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long units = static_cast<long long>(p.Hq) * p.n_qtiles * p.B;
+  const int grid = static_cast<int>(units < sms ? units : sms);  // one CTA per SM, persistent
   FwdParams q = p;
-  q.n_qtiles = (p.n_qtiles + 1) / 2;  // the grid walks pairs of query tiles
-  dim3 grid(q.Hq, q.n_qtiles, q.B);
-  fa_fwd_kernel<D><<<grid, 320, Lay::kBytes, stream>>>(tq, tk, tv, q);
+  q.group_pairs = choose_group_pairs(p, grid, D);
+  fa_fwd_kernel<D><<<grid, 384, Lay::kBytes, stream>>>(tq, tk, tv, q);
   return cudaGetLastError();
 }
 
