@@ -32,7 +32,7 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
-// Device status word: bits from kStatusTimeout / kStatusBadOffsets.
+// Device status word: bits from kStatusTimeout / kStatusBadOffsets / kStatusSmemAlign.
 __device__ unsigned int g_status_word;
 
 constexpr int kMaxDevices = 64;
@@ -206,7 +206,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   Shape s;
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, &s);
   if (rc) return rc;
-  if (d != 64) return fail(FA_ERR_UNSUPPORTED, "backward supports d = 64 in this build");
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
     return fail(FA_ERR_INVALID_ARG, "null pointer");
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
@@ -280,6 +279,8 @@ int fa_stream_status(void* stream) {
   const unsigned zero = 0;
   cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
   if (word & fa::kStatusTimeout) return fail(FA_ERR_TIMEOUT, "a device-side wait timed out");
+  if (word & fa::kStatusSmemAlign)
+    return fail(FA_ERR_LAUNCH, "dynamic shared memory of a kernel was not 1024-byte aligned; the kernel did nothing");
   return fail(FA_ERR_INVALID_ARG, "packed sequence offsets out of range");
 }
 

@@ -13,8 +13,9 @@
 // normalised from the LSE, so no running max is needed.
 //
 // Three launches: fa_bwd_rowdot_kernel (D and zeroing of the dQ accumulator),
-// fa_bwd_kernel (the five tcgen05 products per tile pair), fa_bwd_dq_kernel
-// (dQ accumulator -> bf16).
+// the gradient kernel (the five tcgen05 products per tile pair: fa_bwd_kernel
+// below for d = 64, fa_bwd128_kernel in fa_bwd128.cu for d = 128),
+// fa_bwd_dq_kernel (dQ accumulator -> bf16).
 //
 // fa_bwd_kernel: one CTA per (key tile j, K/V head, sequence); it walks the
 // query heads of the group and their query tiles ("steps"), so dK and dV of
@@ -74,21 +75,6 @@ struct BwdLayout {
   static_assert(D == 64, "TMEM plan is for d = 64");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
-
-constexpr float kLog2e = 1.4426950408889634f;
-
-// f32 tile in shared memory added into global memory by the TMA unit.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(448, 1)
@@ -492,20 +478,27 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p, long 
   reinterpret_cast<uint4*>(p.dq)[i] = out;
 }
 
+int launch_bwd128_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
+
 template <int D>
 int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                  const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
-  using Lay = BwdLayout<D>;
   const long long rows = p.T * p.Hq;
   const long long pre_blocks = (rows * 8 + 255) / 256;
   fa_bwd_rowdot_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
-  if (e != cudaSuccess) return e;
-  dim3 grid(p.Hkv, p.n_kvtiles, p.B);
-  fa_bwd_kernel<D><<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
-  e = cudaGetLastError();
+  if constexpr (D == 64) {
+    using Lay = BwdLayout<D>;
+    e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.Hkv, p.n_kvtiles, p.B);
+    fa_bwd_kernel<D><<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+    e = cudaGetLastError();
+  } else {
+    e = static_cast<cudaError_t>(launch_bwd128_main(tq, tk, tv, tdo, tdq, p, stream));
+  }
   if (e != cudaSuccess) return e;
   const long long n8 = rows * D / 8;
   fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
@@ -515,6 +508,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
   if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, p, stream);
+  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, p, stream);
   return -1;
 }
 

@@ -11,9 +11,12 @@ namespace fa {
 // number of TMEM lanes, so each query row owns one TMEM lane.
 constexpr int kTile = 128;
 
+constexpr float kLog2e = 1.4426950408889634f;
+
 // Bits of the device status word.
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusBadOffsets = 2u;
+constexpr unsigned kStatusSmemAlign = 4u;  // dynamic shared memory not 1 KB aligned
 
 // Key tiles visible from query tile i of a sequence of length L: all of them
 // without a mask, else tiles 0..i (tiles right of the diagonal hold only

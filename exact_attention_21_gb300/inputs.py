@@ -73,6 +73,8 @@ WORKLOADS = {
         VARLEN_LENGTHS),
     "fwdbwd_b2_h16_n4096_d64_causal": Workload(
         "fwdbwd_b2_h16_n4096_d64_causal", 2, 16, 16, 4096, 64, True, (), True),
+    "fwdbwd_b2_h32_n4096_d128_causal": Workload(
+        "fwdbwd_b2_h32_n4096_d128_causal", 2, 32, 32, 4096, 128, True, (), True),
 }
 
 

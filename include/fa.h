@@ -104,8 +104,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   workspace        device scratch of at least
  *                    fa_bwd_workspace_size(Hq, T, d) bytes, 256-byte aligned;
  *                    its contents on entry are ignored.
- *   Other arguments as for fa_fwd.  This build supports d = 64; d = 128
- *   returns FA_ERR_UNSUPPORTED.
+ *   Other arguments as for fa_fwd (d in {64, 128}).
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
            const float* lse, void* dq, void* dk, void* dv,

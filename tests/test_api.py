@@ -73,9 +73,9 @@ def test_bwd_rejects_bad_arguments_on_host(fa):
     L = fa.lib()
     vp = ctypes.c_void_p
     args = [vp(fake(i + 1)) for i in range(9)]
-    # d = 128 backward is not built
-    rc = L.fa_bwd(*args, 1, 2, 2, 128, 128, 128, 0.1, 1, None, vp(fake(20)), 1 << 30, None)
-    assert rc == fa.FA_ERR_UNSUPPORTED
+    # head dimension other than 64 or 128
+    rc = L.fa_bwd(*args, 1, 2, 2, 128, 96, 128, 0.1, 1, None, vp(fake(20)), 1 << 30, None)
+    assert rc == fa.FA_ERR_INVALID_ARG
     # workspace too small
     rc = L.fa_bwd(*args, 1, 2, 2, 128, 64, 128, 0.1, 1, None, vp(fake(20)), 16, None)
     assert rc == fa.FA_ERR_INVALID_ARG

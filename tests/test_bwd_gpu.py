@@ -51,27 +51,31 @@ def check(t, causal, lengths=None, N=None):
     return errs
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 3, 127, 128, 129, 300, 512])
-def test_bwd_single_sequence(cuda_device, causal, N):
-    check(make_qkv(N, 2, 2, 64, seed=10, with_do=True), causal)
+def test_bwd_single_sequence(cuda_device, causal, N, d):
+    check(make_qkv(N, 2, 2, d, seed=10, with_do=True), causal)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_batched_gqa(cuda_device, causal):
-    check(make_qkv(3 * 384, 8, 2, 64, seed=11, with_do=True), causal, N=384)
+def test_bwd_batched_gqa(cuda_device, causal, d):
+    check(make_qkv(3 * 384, 8, 2, d, seed=11, with_do=True), causal, N=384)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_packed_ragged(cuda_device, causal):
+def test_bwd_packed_ragged(cuda_device, causal, d):
     lengths = [5, 1, 300, 128, 129, 0, 640, 77]
-    check(make_qkv(sum(lengths), 4, 1, 64, seed=12, with_do=True), causal, lengths=lengths)
+    check(make_qkv(sum(lengths), 4, 1, d, seed=12, with_do=True), causal, lengths=lengths)
 
 
-def test_bwd_workload_b2_h16_n4096_d64_causal(cuda_device):
-    """Full-size fwd+bwd workload: whole-output properties, plus complete
+@pytest.mark.parametrize("name", ["fwdbwd_b2_h16_n4096_d64_causal", "fwdbwd_b2_h32_n4096_d128_causal"])
+def test_bwd_workload(cuda_device, name):
+    """Full-size fwd+bwd workloads: whole-output properties, plus complete
     oracle gradients for sampled (sequence, head) slices."""
-    w = WORKLOADS["fwdbwd_b2_h16_n4096_d64_causal"]
+    w = WORKLOADS[name]
     t = make_inputs(w)
     dq, dk, dv = run_fwd_bwd(t, w.causal, N=w.N)
     for x in (dq, dk, dv):
@@ -81,11 +85,11 @@ def test_bwd_workload_b2_h16_n4096_d64_causal(cuda_device):
         sl = slice(b * w.N, (b + 1) * w.N)
         col = np.abs(dk[sl].sum(axis=0)).max()
         assert col <= 2e-2 * np.abs(dk[sl]).sum(axis=0).max() + 1e-3, col
-    for b, h in [(0, 0), (1, 7), (0, 15)]:
+    for b, h in [(0, 0), (1, 7), (0, w.Hq - 1)]:
         sl = slice(b * w.N, (b + 1) * w.N)
         sub = {n: t[n][sl, h:h + 1] for n in ("q", "k", "v", "do")}
         ref = oracle.attention_backward(f64(sub["q"]), f64(sub["k"]), f64(sub["v"]), f64(sub["do"]),
                                         [0, w.N], w.scale, w.causal)
-        for name, x, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        for gname, x, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
             e = rel_fro(x[sl, h:h + 1], r)
-            assert e <= BWD_REL_FRO, (b, h, name, e)
+            assert e <= BWD_REL_FRO, (b, h, gname, e)
