@@ -5,6 +5,7 @@ and reference legs may import this package.  See ``oracle/attention.py``.
 """
 from .attention import (  # noqa: F401
     attention_backward,
+    attention_decode,
     attention_forward,
     attention_forward_rows,
     cu_from_lengths,

@@ -26,6 +26,14 @@ tiled method is built to avoid:
 * "Attention 算子优化…", section 五 (GQA: consecutive groups of query heads
   share one K/V head) and section 二 (packed variable-length sequences, no
   padding).
+* decoding (``attention_decode``): "Attention 算子优化…", section 五 (each
+  newly generated token's query attends to the K/V of every earlier token,
+  held in the K/V cache: a matrix-vector product per head) and
+  "FlashAttention：从 Safe Softmax 到分块计算", section 10 (a decode step with
+  one or a few queries calls for a split-K/V strategy such as Flash-Decoding).
+  The oracle evaluates the definition directly, with no split; the split
+  path's merge is the section 3 rule, which is exact, so the result is the
+  same number.
 
 Readings of points the pages leave open (each one is also listed in the design
 notes):
@@ -36,6 +44,8 @@ notes):
   key j is visible from query i when j <= i.
 * A row with no visible key (only possible for an empty sequence here) gives
   O = 0 and LSE = -inf.
+* In a decoding step the new query is the newest token of its sequence and its
+  own K/V row is already in the cache, so it sees every cached key: no mask.
 * Layout: tokens-major ``[T, H, d]`` for q/k/v/o and their gradients, ``[Hq, T]``
   for the LSE; sequence s covers tokens ``cu_seqlens[s] .. cu_seqlens[s+1]-1``.
 
@@ -53,6 +63,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
+    "attention_decode",
     "attention_forward",
     "attention_forward_rows",
     "attention_backward",
@@ -169,6 +180,40 @@ def attention_forward_rows(q, k, v, cu_seqlens, scale, causal, tokens, heads):
         P, lse_row = _safe_softmax(S)
         o[n] = (P @ vv)[0]
         lse[n] = lse_row[0]
+    return o, lse
+
+
+def attention_decode(q, k, v, cu_seqlens_k, scale):
+    """One decoding step: O and LSE for one new query per sequence (fp64).
+
+    q: [B, Hq, d], the query of sequence b's newest token; k, v: [T, Hkv, d],
+    the packed K/V cache, sequence b owning rows cu_seqlens_k[b] ..
+    cu_seqlens_k[b+1]-1.  Every cached key is visible.  Returns o [B, Hq, d]
+    and lse [Hq, B]; a sequence with an empty cache gives O = 0, LSE = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Hq, d = q.shape
+    T, Hkv, dk = k.shape
+    cu = np.asarray(cu_seqlens_k, dtype=np.int64)
+    if v.shape != k.shape or dk != d or Hq % Hkv != 0:
+        raise ValueError("q [B,Hq,d], k and v [T,Hkv,d] with Hq a multiple of Hkv expected")
+    if len(cu) != B + 1 or cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens_k must rise from 0 to T over B + 1 entries")
+    group = Hq // Hkv
+    o = np.zeros((B, Hq, d), dtype=np.float64)
+    lse = np.full((Hq, B), -np.inf, dtype=np.float64)
+    for b in range(B):
+        a, e = int(cu[b]), int(cu[b + 1])
+        if e == a:
+            continue
+        for h in range(Hq):
+            kv = h // group
+            S = _scores(q[b, h, :][None, :], k[a:e, kv, :], scale, False, [0], e - a)
+            P, lse_row = _safe_softmax(S)
+            o[b, h, :] = (P @ v[a:e, kv, :])[0]
+            lse[h, b] = lse_row[0]
     return o, lse
 
 

@@ -355,3 +355,67 @@ def test_causal_skips_about_half_of_the_tiles():
     assert full == 32 * 32
     assert causal == 32 * 33 // 2
     assert 0.5 <= causal / full < 0.52
+
+
+# ---------------------------------------------------------------- decode
+
+DEC = oracle.attention_decode
+
+
+def test_decode_value_example():
+    """The section 3.3 example of "FlashAttention：从 Safe Softmax 到分块计算"
+    as one decoding step: a query q = [1] against cached keys [1], [2], [3]
+    (d = 1, scale = 1) with values 10, 20, 30."""
+    g = load("online_softmax_value_example.txt")
+    n = len(g["scores"])
+    q = np.ones((1, 1, 1))
+    k = np.array(g["scores"], float).reshape(n, 1, 1)
+    v = np.array(g["values"], float).reshape(n, 1, 1)
+    o, lse = DEC(q, k, v, [0, n], 1.0)
+    assert o[0, 0, 0] == pytest.approx(g["merged_u"] / g["merged_l"], rel=1e-14)
+    assert lse[0, 0] == pytest.approx(g["m_final"] + math.log(g["merged_l"]), rel=1e-14)
+
+
+def test_decode_equals_last_causal_row():
+    """A decoding step is the last row of causal attention over the sequence
+    whose newest token carries the query."""
+    lengths = [7, 1, 30, 12]
+    cu = oracle.cu_from_lengths(lengths)
+    q, k, v, _ = rnd(int(cu[-1]), 8, 2, 16, 20)
+    o_full, l_full = F(q, k, v, cu, 0.3, True)
+    last = cu[1:] - 1
+    o, lse = DEC(q[last], k, v, cu, 0.3)
+    np.testing.assert_allclose(o, o_full[last], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, l_full[:, last], rtol=1e-14)
+
+
+def test_decode_zero_query_means_and_degenerate_caches():
+    """q = 0: uniform weights, O = mean of the cached V rows, LSE = ln L; an
+    empty cache gives O = 0, LSE = -inf; one cached key gives O = v_0."""
+    lengths = [5, 0, 1, 9]
+    cu = oracle.cu_from_lengths(lengths)
+    _, k, v, _ = rnd(int(cu[-1]), 2, 2, 4, 21)
+    q = np.zeros((4, 2, 4))
+    o, lse = DEC(q, k, v, cu, 0.7)
+    for b, L in enumerate(lengths):
+        a = cu[b]
+        if L == 0:
+            assert (o[b] == 0).all() and np.isneginf(lse[:, b]).all()
+        else:
+            np.testing.assert_allclose(o[b], v[a:a + L].mean(axis=0), rtol=1e-14)
+            np.testing.assert_allclose(lse[:, b], math.log(L), rtol=1e-14)
+    q1 = np.random.default_rng(3).standard_normal((4, 2, 4))
+    o1, l1 = DEC(q1, k, v, cu, 0.7)
+    np.testing.assert_allclose(o1[2], v[cu[2]], rtol=1e-14)
+    np.testing.assert_allclose(l1[:, 2], 0.7 * np.einsum("hd,hd->h", q1[2], k[cu[2]]), rtol=1e-13)
+
+
+def test_decode_gqa_equals_repeated_heads():
+    cu = oracle.cu_from_lengths([11, 6])
+    _, k, v, _ = rnd(17, 8, 2, 8, 22)
+    q = np.random.default_rng(4).standard_normal((2, 8, 8))
+    rep = lambda x: np.repeat(x, 4, axis=1)
+    o1, l1 = DEC(q, k, v, cu, 0.4)
+    o2, l2 = DEC(q, rep(k), rep(v), cu, 0.4)
+    np.testing.assert_allclose(o1, o2, rtol=1e-14)
+    np.testing.assert_allclose(l1, l2, rtol=1e-14)
