@@ -15,6 +15,11 @@ inside the timed region.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this method
 has) on a bounded sample of the same workload.
+
+``--workload decode_...`` measures one decoding step instead (one new query per
+sequence against a resident K/V cache, split-K/V kernel plus combine): the
+metric is algorithmic GB/s (K/V cache, q, o, LSE moved once) and the roofline
+is HBM bandwidth.
 """
 from __future__ import annotations
 
@@ -275,6 +280,173 @@ def bench_ours(args, world, rank, local):
     return line if rank == 0 else None
 
 
+DECODE_METRIC = "attention decode step, K/V cache bytes read per second (bf16, 1xGB300)"
+
+
+def bench_decode(args, world, rank, local):
+    """One decoding step per timed iteration: fa_decode (split kernel +
+    combine) over a K/V cache resident in HBM, larger than L2 for the
+    64-sequence workload; L2 is flushed before every step anyway."""
+    import torch
+
+    import exact_attention_21_gb300.fa as fa
+    from exact_attention_21_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    fa.lib()
+    stream = torch.cuda.current_stream()
+    host = make_inputs(w, seed=rank)
+    d, T, Hq, Hkv, B, N = w.d, w.T, w.Hq, w.Hkv, w.B, w.N
+    cu = host["cu_seqlens"].to(dev) if w.varlen else None
+    q, k, v = (host[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, B, dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_size(B, Hq, d, N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        fa.fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, w.scale, cu, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    fa.fa_stream_status(stream)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_on()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        events[i][0].record(stream)
+        step()
+        events[i][1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_off()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    fa.fa_stream_status(stream)
+    step_ms = [e[0].elapsed_time(e[1]) for e in events]
+    total_ms = sum(step_ms)
+
+    # end to end: the step's query from pinned host memory in, O and the LSE
+    # back; the K/V cache stays resident, as it does between decoding steps
+    q_pin = host["q"].pin_memory()
+    o_host = torch.empty_like(host["q"]).pin_memory()
+    l_host = torch.empty(Hq, B, dtype=torch.float32).pin_memory()
+    h2d = q_pin.numel() * q_pin.element_size()
+    d2h = o_host.numel() * o_host.element_size() + l_host.numel() * 4
+    e2e_steps = max(3, args.steps // 4)
+
+    def e2e_step():
+        q.copy_(q_pin, non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+        l_host.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        flush.fill_(0.0)
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    fa.fa_stream_status(stream)
+    if pg:
+        t = torch.tensor([total_ms, e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+
+    nbytes = w.decode_bytes()
+    value = nbytes * args.steps * world / (total_ms * 1e-3) / 1e9
+    avg_ms = total_ms / args.steps
+    peaks, peak_src = load_peaks()
+    peak = peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])
+    achieved = nbytes / (avg_ms * 1e-3) / 1e9
+    line = {
+        "metric": DECODE_METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(avg_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+                   "seq_lengths": w.seq_lengths if w.varlen else None, "queries_per_sequence": 1,
+                   "kv_cache_bytes": w.kv_cache_bytes(), "bytes_per_step": nbytes,
+                   "gflop_per_step": round(w.decode_flops() / 1e9, 3),
+                   "tokens_per_s": round(B * world / (avg_ms * 1e-3), 1),
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "fa_decode (split kernel + combine)", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None},
+        "e2e": {"value": round(nbytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if args.traffic_file and os.path.exists(args.traffic_file):
+        with open(args.traffic_file) as f:
+            tr = json.load(f)
+        if tr.get("workload") == w.name:
+            line["roofline"]["traffic"] = tr.get("bytes_per_launch")
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(w, budget_s=args.cpu_seconds)
+    if pg:
+        pg.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def oracle_decode_sample(w, n_seq, seed=0):
+    """fp64 oracle on the first n_seq sequences of decoding workload w (every
+    head); returns (seconds, algorithmic bytes of that sample)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from exact_attention_21_gb300.inputs import make_decode_qkv
+
+    lens = w.seq_lengths[:n_seq]
+    T = int(sum(lens))
+    t = make_decode_qkv(n_seq, w.Hq, T, w.Hkv, w.d, seed=seed)
+    f64 = {n: t[n].to(torch.float64).numpy() for n in t}
+    cu = oracle.cu_from_lengths(lens)
+    t0 = time.perf_counter()
+    oracle.attention_decode(f64["q"], f64["k"], f64["v"], cu, w.scale)
+    sec = time.perf_counter() - t0
+    nbytes = 2 * T * w.Hkv * w.d * 2 + 2 * n_seq * w.Hq * w.d * 2 + n_seq * w.Hq * 4
+    return sec, nbytes
+
+
+def cpu_baseline_decode(w, budget_s=15.0):
+    sec1, b1 = oracle_decode_sample(w, 1)
+    n = max(1, min(w.B, int(budget_s / max(sec1, 1e-3))))
+    sec, nb = oracle_decode_sample(w, n) if n > 1 else (sec1, b1)
+    return {"value": round(nb / sec / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {w.B} sequences of {w.name} (every head), numpy fp64 (BLAS threads = all host cores)",
+            "seconds": round(sec, 3)}
+
+
 def oracle_sample(w, n_heads, seed=0):
     """Runs the fp64 oracle on the first n_heads (sequence, query head) pairs of
     workload w; returns (seconds, algorithmic flops of that sample)."""
@@ -314,6 +486,27 @@ def bench_reference(args, world, rank):
     if rank != 0:
         return None
     w = WORKLOADS[args.workload]
+    if w.decode:
+        for _ in range(args.warmup):
+            oracle_decode_sample(w, 1)
+        secs, nbytes = 0.0, 0
+        for _ in range(args.steps):
+            s_, b_ = oracle_decode_sample(w, 1)
+            secs += s_
+            nbytes += b_
+        value = nbytes / secs / 1e9
+        sample = f"1 sequence (every head) of {w.name} per step, numpy fp64 (BLAS threads = all host cores)"
+        return {
+            "impl": "reference", "metric": DECODE_METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16)",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                       "parallelism": "cpu oracle, rank 0 only"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     for _ in range(args.warmup):
         oracle_sample(w, 1)
     secs, flops = 0.0, 0.0
@@ -352,8 +545,13 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
+    from exact_attention_21_gb300.inputs import WORKLOADS
+    if args.workload not in WORKLOADS:
+        ap.error(f"unknown workload {args.workload}; one of {sorted(WORKLOADS)}")
     if args.impl == "reference":
         line = bench_reference(args, world, rank)
+    elif WORKLOADS[args.workload].decode:
+        line = bench_decode(args, world, rank, local)
     else:
         line = bench_ours(args, world, rank, local)
     if line is not None:

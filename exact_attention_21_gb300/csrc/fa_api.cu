@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -18,6 +19,7 @@ int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
                cudaStream_t stream);
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
+int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream);
 }  // namespace fa
 
 namespace {
@@ -39,6 +41,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   int checked = 0;       // 0 = not yet, 1 = supported, -1 = unsupported
   unsigned* status = nullptr;
+  int sms = 0;           // streaming multiprocessors
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -80,6 +83,8 @@ int device_state(DeviceState** out) {
       if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess)
         return fail(FA_ERR_LAUNCH, "cudaGetSymbolAddress(status) failed");
       st.status = static_cast<unsigned*>(addr);
+      cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+      if (st.sms < 1) st.sms = 1;
       st.checked = 1;
     }
   }
@@ -146,6 +151,29 @@ int check_shape(int B, int Hq, int Hkv, int N, int d, long long T, float scale, 
   *s = Shape{B, Hq, Hkv, N, d, T, (N + fa::kTile - 1) / fa::kTile};
   if (s->n_tiles > 65535) return fail(FA_ERR_INVALID_ARG, "N too large");
   return FA_OK;
+}
+
+// 128-key tiles per decode split.  Decode CTAs are resident one per SM, so a
+// grid of (split, K/V head, sequence) CTAs runs in ceil(CTAs / SMs) waves, and
+// each CTA costs its tiles plus about one tile of start-up (barrier set-up and
+// the latency of its first loads).  Picks the split length with the lowest
+// modelled time; packed caches are modelled as sequences of the mean length.
+int decode_split_tiles(int B, int Hkv, int max_tiles, long long T, bool packed, int sms) {
+  const double mean_tiles =
+      packed ? std::max(1.0, static_cast<double>(T) / B / fa::kTile) : static_cast<double>(max_tiles);
+  int best = 1;
+  double best_time = 0.0;
+  for (int st = 1; st <= 2 * max_tiles && st <= (1 << 20); st *= 2) {
+    const long long per_seq = static_cast<long long>(std::ceil(mean_tiles / st));
+    const long long ctas = static_cast<long long>(B) * Hkv * per_seq;
+    const long long waves = (ctas + sms - 1) / sms;
+    const double time = static_cast<double>(waves) * (std::min<double>(st, mean_tiles) + 1.0);
+    if (st == 1 || time < best_time) {
+      best = st;
+      best_time = time;
+    }
+  }
+  return std::min(best, std::max(max_tiles, 1));
 }
 
 }  // namespace
@@ -248,6 +276,57 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   int e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
   if (e == -1) return fail(FA_ERR_UNSUPPORTED, "backward kernel unavailable for d = %d", d);
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString((cudaError_t)e));
+  return FA_OK;
+}
+
+size_t fa_decode_workspace_size(int B, int Hq, int d, int max_seqlen_k) {
+  if (B < 1 || Hq < 1 || d < 1 || max_seqlen_k < 1) return 0;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = static_cast<size_t>(B) * Hq * ((max_seqlen_k + fa::kTile - 1) / fa::kTile);
+  return up(rows * d * 4) + up(rows * 4);
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+              int d, long long T, float scale, const int* cu_seqlens_k, void* workspace, size_t workspace_bytes,
+              void* stream) {
+  g_err[0] = '\0';
+  Shape s;
+  int rc = check_shape(B, Hq, Hkv, N, d, T, scale, 0, cu_seqlens_k, &s);
+  if (rc) return rc;
+  if (Hq / Hkv > 16) return fail(FA_ERR_UNSUPPORTED, "decode supports up to 16 query heads per K/V head");
+  if (!q || !k || !v || !o || !lse || !workspace) return fail(FA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(FA_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = fa_decode_workspace_size(B, Hq, d, N);
+  if (workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  DeviceState* dev = nullptr;
+  if ((rc = device_state(&dev))) return rc;
+  CUtensorMap tk, tv;
+  if ((rc = make_map(&tk, k, T, Hkv, d, "k")) || (rc = make_map(&tv, v, T, Hkv, d, "v"))) return rc;
+  fa::DecodeParams p{};
+  p.q = q;
+  p.o = o;
+  p.lse = lse;
+  p.cu = cu_seqlens_k;
+  p.status = dev->status;
+  p.T = T;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.group = Hq / Hkv;
+  p.split_tiles = decode_split_tiles(B, Hkv, s.n_tiles, T, cu_seqlens_k != nullptr, dev->sms);
+  p.n_splits = (s.n_tiles + p.split_tiles - 1) / p.split_tiles;
+  const size_t rows = static_cast<size_t>(B) * Hq * p.n_splits;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * d * 4 + 255) / 256 * 256);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  int e = fa::launch_decode(d, tk, tv, p, static_cast<cudaStream_t>(stream));
+  if (e == -1) return fail(FA_ERR_UNSUPPORTED, "decode kernel unavailable for d = %d, group %d", d, p.group);
+  if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "decode launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;
 }
 

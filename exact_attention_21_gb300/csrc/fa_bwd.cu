@@ -63,9 +63,9 @@ struct BwdLayout {
   static constexpr int kOffDQ = kOffDS + 2 * kDSBytes;
   static constexpr int kOffRing = kOffDQ + kDQBytes;
   static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
-  // kv_full, qdo_full[], qdo_empty[], sdp_full, ps_ready, dp_free, dq_full, dq_free,
+  // kv_full, qdo_full[], qdo_empty[], sdp_full, ps_ready[2], dp_free, dq_full, dq_free,
   // dq_staged, dq_stage_free, epi, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 10;
+  static constexpr int kNumBars = 1 + 2 * kStages + 11;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -111,7 +111,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* qdo_empty = qdo_full + NS;
   uint64_t* sdp_full = qdo_empty + NS;
   uint64_t* ps_ready = sdp_full + 1;
-  uint64_t* dp_free = ps_ready + 1;
+  uint64_t* dp_free = ps_ready + 2;  // ps_ready[n & 1]: one per step parity
   uint64_t* dq_full = dp_free + 1;
   uint64_t* dq_free = dq_full + 1;
   uint64_t* dq_staged = dq_free + 1;
@@ -131,6 +131,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int i = 0; i < NS; ++i) { mbar_init(qdo_full + i, 32); mbar_init(qdo_empty + i, 1); }
     mbar_init(sdp_full, 1);
     mbar_init(ps_ready, 256);
+    mbar_init(ps_ready + 1, 256);
     mbar_init(dp_free, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
@@ -255,7 +256,10 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (ok && nsteps > 1) ok = issue_next(1);
       for (int n = 0; n < nsteps && ok; ++n) {
         const int st = n % NS;
-        if (!(ok = mbar_wait(ps_ready, n & 1, abort_flag))) break;
+        // Score warpgroups may finish step n + 1 before this thread looks at
+        // step n, so each step parity has its own barrier: step n + 2 cannot
+        // start before S^T_{n+2} is issued below.
+        if (!(ok = mbar_wait(ps_ready + (n & 1), (n >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t sQa = smem_u32(stage_q(st)), sDOa = smem_u32(stage_do(st));
         const uint32_t dsb = sDSa + (n & 1) * Lay::kDSBytes;
@@ -349,7 +353,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(ps_ready);
+      mbar_arrive(ps_ready + (n & 1));
     }
     if (ok) ok = mbar_wait(epi, 0, abort_flag);
     if (!ok) {

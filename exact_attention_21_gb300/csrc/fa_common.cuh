@@ -77,4 +77,19 @@ struct BwdParams {
   float scale, scale_log2;
 };
 
+struct DecodeParams {
+  const void* q;      // bf16 [B, Hq, d]: the new token's query per sequence
+  void* o;            // bf16 [B, Hq, d]
+  float* lse;         // f32 [Hq, B]
+  float* o_part;      // f32 [B, Hq, n_splits, d]: normalised output of each split
+  float* lse_part;    // f32 [B, Hq, n_splits]
+  const int* cu;      // device int32 [B + 1] offsets into the K/V cache, or null
+  unsigned* status;
+  long long T;        // cached tokens in all
+  int B, Hq, Hkv, N, group;
+  int n_splits;       // splits per (sequence, K/V head) in the grid
+  int split_tiles;    // 128-key tiles per split
+  float scale_log2;   // scale * log2(e)
+};
+
 }  // namespace fa

@@ -1,0 +1,719 @@
+// Split-K/V decoding ("Flash-Decoding").
+//
+// What it computes ("Attention 算子优化…", section 五; "FlashAttention：从
+// Safe Softmax 到分块计算", sections 3 and 10): one decoding step, i.e. for
+// every sequence b and query head h the attention of the single new query
+// q[b, h] over all cached keys and values of the sequence,
+//     O = softmax(scale * K q) V,   LSE = ln sum_j exp(scale * <k_j, q>).
+// A decoding step reads the whole K/V cache for a few multiply-adds per byte,
+// so it is bound by HBM bandwidth; the arithmetic runs on the CUDA cores and
+// the design goal is to keep enough K/V bytes in flight.
+//
+// Two launches:
+//  fa_decode_split_kernel: CTA = (split, K/V head, sequence).  A split is a
+//    run of `split_tiles` 128-key tiles of one sequence.  A producer warp
+//    streams the split's K and V tiles through a ring of shared-memory stages
+//    with TMA; 256 consumer threads keep, for every query head of the GQA
+//    group, the running max, running sum and output accumulator of the
+//    online-softmax recurrence (section 3 of the safe-softmax page), and
+//    finally write the split's normalised output O_s and its LSE_s.
+//  fa_decode_combine_kernel: one warp per (sequence, query head) merges the
+//    splits with the same rule: LSE = ln sum_s e^{LSE_s} and
+//    O = sum_s e^{LSE_s - LSE} O_s.
+//
+// Consumer thread mappings (256 threads, tiles of 128 keys):
+//   scores:  thread t takes key t/2 and half t%2 of the head dimension; the
+//            two halves meet with one shuffle.
+//   P V:     thread t takes the head-dimension pair 2(t mod d/2), 2(t mod d/2)+1
+//            over one 1/(512/d) slice of the tile's keys; the slices are
+//            summed once at the end of the split.
+#include <cuda_bf16.h>
+
+#include "fa_common.cuh"
+
+namespace fa {
+
+constexpr int kDecMaxGroup = 16;   // query heads per K/V head handled by one CTA
+constexpr int kDecConsumers = 256;
+
+template <int D>
+struct DecLayout {
+  static constexpr int kChunkBytes = kTile * 128;            // 128 keys x 64 dims bf16, 128B-swizzled
+  static constexpr int kTileBytes = (D / 64) * kChunkBytes;  // one K or V tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kOffQ = kStages * kStageBytes;             // f32 [group][D], pre-scaled query
+  static constexpr int kOffP = kOffQ + kDecMaxGroup * D * 4;      // f32 [group][128] probabilities
+  static constexpr int kOffRed = kOffP + kDecMaxGroup * kTile * 4;  // f32 [8 warps][group]
+  static constexpr int kOffML = kOffRed + 8 * kDecMaxGroup * 4;     // f32 m[group], l[group]
+  static constexpr int kOffBar = kOffML + 2 * kDecMaxGroup * 4;     // full[kStages], empty[kStages]
+  static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
+  static constexpr int kBytes = kOffMisc + 16 + 1024;
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+  static_assert((512 / D) * kDecMaxGroup * D * 4 <= kStageBytes, "slice sums must fit in one stage");
+};
+
+// Barrier among the 256 consumer threads only (the producer warp does not take
+// part); returns whether `v` was true in every consumer thread.
+__device__ __forceinline__ bool consumers_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+template <int D, int G>
+__global__ void __launch_bounds__(288, 1)
+fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const DecodeParams p) {
+  using Lay = DecLayout<D>;
+  constexpr int NS = Lay::kStages;
+  static_assert(G <= kDecMaxGroup, "group too large");
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  long long seq0;
+  int L;
+  if (!sequence_bounds(p.cu, b, p.N, p.T, seq0, L, p.status)) return;
+  const int seq_tiles = (L + kTile - 1) / kTile;
+  const int t0 = split * p.split_tiles;
+  if (t0 >= seq_tiles) return;  // past the end of this sequence's cache: the combine skips it
+  const int nt = min(p.split_tiles, seq_tiles - t0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
+  uint64_t* empty = full + NS;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc);
+  auto stage = [&](int st) { return smem + st * Lay::kStageBytes; };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, kDecConsumers);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  auto give_up = [&]() {
+    atomicOr(p.status, kStatusTimeout);
+    *abort_flag = 1;
+  };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < nt; ++i) {
+        const int st = i % NS;
+        if (i >= NS && !(ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag))) break;
+        mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
+        const int row = static_cast<int>(seq0 + static_cast<long long>(t0 + i) * kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(stage(st) + c * Lay::kChunkBytes, &tm_k, full + st, c * 64, g, row);
+          tma_load_3d(stage(st) + Lay::kTileBytes + c * Lay::kChunkBytes, &tm_v, full + st, c * 64, g, row);
+        }
+        ++issued;
+      }
+      if (!ok) give_up();
+      // no TMA write may still be in flight when the CTA exits
+      int never = 0;
+      for (int i = issued > NS ? issued - NS : 0; i < issued; ++i) mbar_wait(full + i % NS, (i / NS) & 1, &never);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int t = threadIdx.x;
+  const int group = p.group;
+  const int hq0 = g * group;
+  float* sQ = reinterpret_cast<float*>(smem + Lay::kOffQ);
+  float* sP = reinterpret_cast<float*>(smem + Lay::kOffP);
+  float* sRed = reinterpret_cast<float*>(smem + Lay::kOffRed);
+  float* sM = reinterpret_cast<float*>(smem + Lay::kOffML);
+  float* sL = sM + kDecMaxGroup;
+
+  // the group's queries, scaled by c = scale * log2 e (heads past the group: 0)
+  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q) + (static_cast<long long>(b) * p.Hq + hq0) * D;
+  for (int i = t; i < G * D; i += kDecConsumers)
+    sQ[i] = (i / D < group) ? __bfloat162float(qb[i]) * p.scale_log2 : 0.f;
+
+  const int key = t >> 1;  // score mapping
+  const int dh = t & 1;
+  constexpr int kPairs = D / 2;  // P V mapping
+  constexpr int kSubs = kDecConsumers / kPairs;
+  constexpr int kKeysPerSub = kTile / kSubs;
+  const int e0 = 2 * (t % kPairs);
+  const int sub = t / kPairs;
+  const uint32_t v_off = (e0 / 64) * Lay::kChunkBytes + (e0 % 8) * 2;
+  const int v_unit = (e0 % 64) / 8;
+
+  float m[G], lt[G], acc[G][2];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    lt[h] = 0.f;
+    acc[h][0] = acc[h][1] = 0.f;
+  }
+  bool ok = consumers_sync_and(true);  // sQ written
+  for (int i = 0; i < nt; ++i) {
+    const int st = i % NS;
+    // a lane that gave up takes its whole warp along (the shuffles below
+    // need every lane), and the vote after the scores takes the rest
+    ok = __all_sync(0xffffffffu, mbar_wait(full + st, (i / NS) & 1, abort_flag));
+    const uint8_t* sK = stage(st);
+    const uint8_t* sV = sK + Lay::kTileBytes;
+    float s[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) s[h] = 0.f;
+    if (ok) {
+      // ---- scores s_h = c <q_h, k_key> over this thread's half of the row
+#pragma unroll
+      for (int u = 0; u < D / 16; ++u) {
+        const int unit = dh * (D / 16) + u;  // 16-byte unit of the row
+        const uint4 kr =
+            *reinterpret_cast<const uint4*>(sK + (unit / 8) * Lay::kChunkBytes + key * 128 + (((unit % 8) ^ (key & 7)) << 4));
+        const float kf[8] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y),
+                             bf16_lo(kr.z), bf16_hi(kr.z), bf16_lo(kr.w), bf16_hi(kr.w)};
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float4 qa = *reinterpret_cast<const float4*>(sQ + h * D + unit * 8);
+          const float4 qc = *reinterpret_cast<const float4*>(sQ + h * D + unit * 8 + 4);
+          float x = s[h];
+          x = fmaf(kf[0], qa.x, x);
+          x = fmaf(kf[1], qa.y, x);
+          x = fmaf(kf[2], qa.z, x);
+          x = fmaf(kf[3], qa.w, x);
+          x = fmaf(kf[4], qc.x, x);
+          x = fmaf(kf[5], qc.y, x);
+          x = fmaf(kf[6], qc.z, x);
+          x = fmaf(kf[7], qc.w, x);
+          s[h] = x;
+        }
+      }
+      // keys past the end of the cache (tail tile) take no part
+      const bool valid = (t0 + i) * kTile + key < L;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        s[h] += __shfl_xor_sync(0xffffffffu, s[h], 1);
+        if (!valid) s[h] = -INFINITY;
+        float mx = s[h];
+#pragma unroll
+        for (int off = 16; off > 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) sRed[warp * G + h] = mx;
+      }
+    }
+    // every consumer either has its scores or gives up with the others
+    if (!(ok = consumers_sync_and(ok))) break;
+    // ---- online-softmax update; key 0 of every tile is valid, so the new max is finite
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float tm = sRed[h];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) tm = fmaxf(tm, sRed[w * G + h]);
+      const float mn = fmaxf(m[h], tm);
+      const float alpha = ex2_approx(m[h] - mn);  // 0 on the first tile (m = -inf)
+      m[h] = mn;
+      const float pv = ex2_approx(s[h] - mn);     // 0 for masked keys
+      if (dh == 0) {
+        sP[h * kTile + key] = pv;
+        lt[h] = fmaf(lt[h], alpha, pv);
+      }
+      acc[h][0] *= alpha;
+      acc[h][1] *= alpha;
+    }
+    consumers_sync();
+    // ---- O_h += sum_j p_hj v_j over this thread's key slice and dimension pair
+#pragma unroll
+    for (int j4 = 0; j4 < kKeysPerSub; j4 += 4) {
+      const int kb = sub * kKeysPerSub + j4;
+      float pj[G][4];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float4 pp = *reinterpret_cast<const float4*>(sP + h * kTile + kb);
+        pj[h][0] = pp.x;
+        pj[h][1] = pp.y;
+        pj[h][2] = pp.z;
+        pj[h][3] = pp.w;
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int kk = kb + jj;
+        const uint32_t vv = *reinterpret_cast<const uint32_t*>(sV + v_off + kk * 128 + ((v_unit ^ (kk & 7)) << 4));
+        const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          acc[h][0] = fmaf(pj[h][jj], v0, acc[h][0]);
+          acc[h][1] = fmaf(pj[h][jj], v1, acc[h][1]);
+        }
+      }
+    }
+    // this thread is done with the stage (K read above, V read here)
+    mbar_arrive(empty + st);
+  }
+  if (!ok) {
+    if (t == 0) give_up();
+    return;
+  }
+  // -------------------------------------------------------------- split result
+  consumers_sync();  // every thread is past its last read of the stages
+  // l_h: sum of the per-thread partial sums
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float x = lt[h];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    if (lane == 0) sRed[warp * G + h] = x;
+  }
+  // slice sums of O through the first stage (its last TMA fill was consumed)
+  float* sO = reinterpret_cast<float*>(stage(0));
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    sO[(sub * G + h) * D + e0] = acc[h][0];
+    sO[(sub * G + h) * D + e0 + 1] = acc[h][1];
+  }
+  consumers_sync();
+  if (t < G) {
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) l += sRed[w * G + t];
+    sL[t] = l;
+  }
+  if (t == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) sM[h] = m[h];
+  }
+  consumers_sync();
+  const long long row0 = static_cast<long long>(b) * p.Hq + hq0;
+  for (int idx = t; idx < group * D; idx += kDecConsumers) {
+    const int h = idx / D, e = idx % D;
+    float o = 0.f;
+#pragma unroll
+    for (int sl = 0; sl < kSubs; ++sl) o += sO[(sl * G + h) * D + e];
+    p.o_part[((row0 + h) * p.n_splits + split) * D + e] = o / sL[h];
+  }
+  if (t < group) {
+    // natural-log LSE of the split: (m + log2 l) ln 2, m in log2 units
+    p.lse_part[(row0 + t) * p.n_splits + split] = (sM[t] + log2f(sL[t])) * 0.6931471805599453f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// d = 128: the two products on the tensor cores.  With the query heads of the
+// GQA group (padded to 16) as the MMA's N dimension:
+//     S^T = K_tile Q^T       M = 128 keys,  N = 16 heads, K = d   (TMEM, f32)
+//     O^T += V_tile^T P^T    M = d = 128,   N = 16 heads, K = 128 keys
+// so the threads only turn 16 scores per key into probabilities.  Roles:
+//   warp 0     TMA producer of the K / V stages.
+//   warp 1     TMEM allocator and MMA issuer (one thread).
+//   warps 2-5  softmax warpgroup: thread = key row of S^T (TMEM lane) for the
+//              probabilities, and = dimension row of O^T for the rescale and
+//              the split's output.
+// S^T is double-buffered in TMEM, so S^T of tile i+1 runs while the softmax
+// works on tile i; P^T (bf16, K-major: 16 head rows x 128 keys) is
+// double-buffered in shared memory.  The running max of a head only moves
+// when a tile's max exceeds it by more than kDecRescaleSlack (log2 units);
+// any common reference gives the same merge, so this is exact and O^T is
+// rarely rescaled.
+constexpr int kDecHeads = 16;               // MMA N: query heads per CTA, padded
+constexpr float kDecRescaleSlack = 8.f;
+
+struct DecTcLayout {
+  static constexpr int D = 128;
+  static constexpr int kChunkBytes = kTile * 128;   // 128 keys x 64 dims
+  static constexpr int kTileBytes = 2 * kChunkBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = 3;
+  static constexpr int kHChunkBytes = kDecHeads * 128;  // 16 rows x 64 elements
+  static constexpr int kQBytes = 2 * kHChunkBytes;      // Q: 16 heads x 128 dims, K-major
+  static constexpr int kPBytes = 2 * kHChunkBytes;      // P^T: 16 heads x 128 keys, K-major
+  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffP = kOffQ + kQBytes;          // two buffers
+  static constexpr int kOffRed = kOffP + 2 * kPBytes;    // f32 [4 warps][16 heads]
+  static constexpr int kOffBar = kOffRed + 4 * kDecHeads * 4;
+  // full[3], empty[3], q_ready, s_full[2], p_ready[2], pv_done[2], drain
+  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16 + 1024;
+  static constexpr uint32_t kTmemCols = 64;
+  static constexpr uint32_t kColS = 0, kColO = 32;  // S^T buffers at 0 and 16
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void sts_u16(uint8_t* p, uint16_t v) { *reinterpret_cast<uint16_t*>(p) = v; }
+
+// Barrier among the 128 softmax threads (named barrier 1); returns whether
+// `v` held in all of them.
+__device__ __forceinline__ bool softmax_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(192, 1)
+fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const DecodeParams p) {
+  using Lay = DecTcLayout;
+  constexpr int NS = Lay::kStages;
+  constexpr int D = Lay::D;
+  constexpr int H = kDecHeads;
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  long long seq0;
+  int L;
+  if (!sequence_bounds(p.cu, b, p.N, p.T, seq0, L, p.status)) return;
+  const int seq_tiles = (L + kTile - 1) / kTile;
+  const int t0 = split * p.split_tiles;
+  if (t0 >= seq_tiles) return;  // past the end of this sequence's cache: the combine skips it
+  const int nt = min(p.split_tiles, seq_tiles - t0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + Lay::kOffQ;
+  float* sRed = reinterpret_cast<float*>(smem + Lay::kOffRed);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = full + NS;
+  uint64_t* q_ready = empty + NS;
+  uint64_t* s_full = q_ready + 1;
+  uint64_t* p_ready = s_full + 2;
+  uint64_t* pv_done = p_ready + 2;
+  uint64_t* drain = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
+  auto stage = [&](int st) { return smem + st * Lay::kStageBytes; };
+  auto pbuf = [&](int i) { return smem + Lay::kOffP + (i & 1) * Lay::kPBytes; };
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    mbar_init(q_ready, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(p_ready + i, 128);
+      mbar_init(pv_done + i, 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Lay::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto give_up = [&]() {
+    atomicOr(p.status, kStatusTimeout);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < nt; ++i) {
+        const int st = i % NS;
+        if (i >= NS && !(ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag))) break;
+        mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
+        const int row = static_cast<int>(seq0 + static_cast<long long>(t0 + i) * kTile);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(stage(st) + c * Lay::kChunkBytes, &tm_k, full + st, c * 64, g, row);
+          tma_load_3d(stage(st) + Lay::kTileBytes + c * Lay::kChunkBytes, &tm_v, full + st, c * 64, g, row);
+        }
+        ++issued;
+      }
+      if (!ok) give_up();
+      // no TMA write may still be in flight when the CTA exits
+      int never = 0;
+      for (int i = issued > NS ? issued - NS : 0; i < issued; ++i) mbar_wait(full + i % NS, (i / NS) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(kTile, H, false, false);  // K (K-major) x Q (K-major)
+      constexpr uint32_t id_o = idesc_bf16_f32(D, H, true, false);       // V^T (MN-major) x P^T (K-major)
+      const uint32_t sQa = smem_u32(sQ);
+      auto issue_s = [&](int i) -> bool {
+        const int st = i % NS;
+        if (!mbar_wait(full + st, (i / NS) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t sKa = smem_u32(stage(st));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + Lay::kColS + (i & 1) * H,
+                  sdesc_sw128(sKa + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
+                  sdesc_sw128(sQa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_s, kk > 0);
+        umma_commit(s_full + (i & 1));
+        return true;
+      };
+      bool ok = mbar_wait(q_ready, 0, abort_flag);
+      if (ok) ok = issue_s(0);
+      if (ok && nt > 1) ok = issue_s(1);
+      for (int i = 0; i < nt && ok; ++i) {
+        const int st = i % NS;
+        // P^T of tile i written, S^T buffer i & 1 read, O^T rescaled
+        if (!(ok = mbar_wait(p_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t sVa = smem_u32(stage(st) + Lay::kTileBytes), sPa = smem_u32(pbuf(i));
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ss(tmem + Lay::kColO, sdesc_sw128(sVa + kk * 2048, Lay::kChunkBytes, 1024),
+                  sdesc_sw128(sPa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_o, (i > 0 || kk > 0));
+        umma_commit(empty + st);
+        umma_commit(pv_done + (i & 1));
+        if (i + 2 < nt && !(ok = issue_s(i + 2))) break;
+      }
+      if (!ok) give_up();
+      umma_commit(drain);
+      int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroup
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // key row of S^T, dimension row of O^T
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
+    const int group = p.group;
+    const int hq0 = g * group;
+    const float c = p.scale_log2;
+    // Q (16 head rows x 128 dims, K-major, 128-byte swizzle); padded heads are 0
+    {
+      const int h = r / 8, u2 = (r % 8) * 2;  // 8 threads per head row, two 16-byte units each
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                        (static_cast<long long>(b) * p.Hq + hq0 + h) * D);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int u = u2 + j;  // unit of the 256-byte row: chunk u / 8, unit u % 8
+        const uint4 val = h < group ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sQ + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = val;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_ready);
+    }
+    float m[H], lt[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      m[h] = -INFINITY;
+      lt[h] = 0.f;
+    }
+    // A wait that gives up must not leave the other threads at a barrier:
+    // results of waits are made warp-uniform (the shuffles and TMEM accesses
+    // need whole warps) and the loop ends only on a vote of all 128 threads.
+    bool ok = true;
+    for (int i = 0; i < nt; ++i) {
+      bool w = __all_sync(0xffffffffu, mbar_wait(s_full + (i & 1), (i >> 1) & 1, abort_flag));
+      float x[H];
+      if (w) {
+        tc_fence_after();
+        uint32_t sv[H];
+        tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (i & 1) * H, lane_base, 0), sv);
+        const bool valid = (t0 + i) * kTile + r < L;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+          x[h] = valid ? __uint_as_float(sv[h]) * c : -INFINITY;
+          float mx = x[h];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          if (lane == 0) sRed[quad * H + h] = mx;
+        }
+      }
+      if (!(ok = softmax_sync_and(w))) break;
+      bool bump = false;
+      float alpha[H];
+#pragma unroll
+      for (int h = 0; h < H; ++h) {
+        const float tm = fmaxf(fmaxf(sRed[h], sRed[H + h]), fmaxf(sRed[2 * H + h], sRed[3 * H + h]));
+        // the tile's key 0 is valid, so tm is finite
+        const bool up = tm > m[h] + kDecRescaleSlack;  // always on the first tile (m = -inf)
+        const float mn = up ? tm : m[h];
+        alpha[h] = up ? ex2_approx(m[h] - mn) : 1.f;
+        bump |= up;
+        m[h] = mn;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // sRed is rewritten by the next tile
+      // P^T buffer i & 1 was last read by P V of tile i - 2
+      w = i < 2 || __all_sync(0xffffffffu, mbar_wait(pv_done + (i & 1), ((i - 2) >> 1) & 1, abort_flag));
+      if (w) {
+        uint8_t* pb = pbuf(i) + (r / 64) * Lay::kHChunkBytes + (r % 8) * 2;
+        const int pu = (r % 64) / 8;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+          const float pv = ex2_approx(x[h] - m[h]);  // masked keys: 0
+          lt[h] = fmaf(lt[h], alpha[h], pv);
+          const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
+          sts_u16(pb + h * 128 + ((pu ^ (h & 7)) << 4), *reinterpret_cast<const uint16_t*>(&pb16));
+        }
+      }
+      // m is the same in every thread, so bump is uniform
+      if (w && i > 0 && bump) {
+        // O^T may only be touched once P V of tile i - 1 has completed
+        w = __all_sync(0xffffffffu, mbar_wait(pv_done + ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag));
+        if (w) {
+          tc_fence_after();
+          uint32_t ov[H];
+          tmem_ld_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
+#pragma unroll
+          for (int h = 0; h < H; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+          tmem_st_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
+          tmem_st_wait();
+        }
+      }
+      if (w) {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_ready + (i & 1));
+      }
+      // a warp that gave up here stops arriving; the vote of the next tile
+      // (or the final wait below) ends the loop for everyone
+      ok = w;
+    }
+    ok = softmax_sync_and(ok);
+    // ---- the split's output: O^T / l, and its LSE
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      float x = lt[h];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      if (lane == 0) sRed[quad * H + h] = x;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(pv_done + ((nt - 1) & 1), ((nt - 1) >> 1) & 1, abort_flag));
+    if (!ok) {
+      if (lane == 0) give_up();
+    } else {
+      tc_fence_after();
+      uint32_t ov[H];
+      tmem_ld_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
+      const long long row0 = static_cast<long long>(b) * p.Hq + hq0;
+#pragma unroll
+      for (int h = 0; h < H; ++h) {
+        if (h < group) {
+          const float l = sRed[h] + sRed[H + h] + sRed[2 * H + h] + sRed[3 * H + h];
+          p.o_part[((row0 + h) * p.n_splits + split) * D + r] = __uint_as_float(ov[h]) / l;
+          if (r == 0) p.lse_part[(row0 + h) * p.n_splits + split] = (m[h] + log2f(l)) * 0.6931471805599453f;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::kTmemCols);
+  }
+}
+
+// Merges the splits of one (sequence, query head) row per warp.
+template <int D>
+__global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
+  constexpr int E = D / 32;  // dimensions per lane
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const long long row = static_cast<long long>(blockIdx.x) * 4 + warp;  // b * Hq + h
+  if (row >= static_cast<long long>(p.B) * p.Hq) return;
+  const int b = static_cast<int>(row / p.Hq), h = static_cast<int>(row % p.Hq);
+  int L = p.N;
+  if (p.cu != nullptr) {
+    const int a = __ldg(p.cu + b), e = __ldg(p.cu + b + 1);
+    L = (a >= 0 && e >= a && e <= p.T && e - a <= p.N) ? e - a : 0;  // bad offsets: reported by the split kernel
+  }
+  const int tiles = (L + kTile - 1) / kTile;
+  const int ns = (tiles + p.split_tiles - 1) / p.split_tiles;
+  const float* lp = p.lse_part + row * p.n_splits;
+  const float* op = p.o_part + row * p.n_splits * D + lane * E;
+  float mx = -INFINITY;
+  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, lp[s]);
+  float den = 0.f, acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float w = expf(lp[s] - mx);
+    den += w;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, op[static_cast<long long>(s) * D + e], acc[e]);
+  }
+  const float inv = ns > 0 ? 1.f / den : 0.f;
+  uint32_t pk[E / 2];
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e) pk[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o) + row * D + lane * E;
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2*>(o) = make_uint2(pk[0], pk[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(o) = pk[0];
+  }
+  if (lane == 0) p.lse[static_cast<long long>(h) * p.B + b] = ns > 0 ? mx + logf(den) : -INFINITY;
+}
+
+template <int D, int G>
+int launch_decode_dg(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+  using Lay = DecLayout<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_decode_split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_splits, p.Hkv, p.B);
+  fa_decode_split_kernel<D, G><<<grid, 288, Lay::kBytes, stream>>>(tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long rows = static_cast<long long>(p.B) * p.Hq;
+  fa_decode_combine_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+int launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+  // the kernel is instantiated for power-of-two groups; others round up and
+  // leave the extra heads unused
+  if (p.group <= 1) return launch_decode_dg<D, 1>(tk, tv, p, stream);
+  if (p.group <= 2) return launch_decode_dg<D, 2>(tk, tv, p, stream);
+  if (p.group <= 4) return launch_decode_dg<D, 4>(tk, tv, p, stream);
+  if (p.group <= 8) return launch_decode_dg<D, 8>(tk, tv, p, stream);
+  if (p.group <= 16) return launch_decode_dg<D, 16>(tk, tv, p, stream);
+  return -1;
+}
+
+int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+  using Lay = DecTcLayout;
+  if (p.group > kDecHeads) return -1;
+  cudaError_t e = cudaFuncSetAttribute(fa_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_splits, p.Hkv, p.B);
+  fa_decode_tc_kernel<<<grid, 192, Lay::kBytes, stream>>>(tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long rows = static_cast<long long>(p.B) * p.Hq;
+  fa_decode_combine_kernel<128><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+  if (d == 64) return launch_decode_d<64>(tk, tv, p, stream);
+  if (d == 128) return launch_decode_tc(tk, tv, p, stream);
+  return -1;
+}
+
+}  // namespace fa

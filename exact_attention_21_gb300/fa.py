@@ -23,8 +23,8 @@ FA_ERR_LAUNCH = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_UNSUPPORTED = 5
 
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_tile_counts",
-           "fa_stream_status", "fa_last_error_string")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
+           "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
 
 
 class FAError(RuntimeError):
@@ -54,6 +54,10 @@ def lib():
         L.fa_bwd_noalloc.restype = i32
         L.fa_bwd_workspace_size.argtypes = [i32, i64, i32]
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
+        L.fa_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, vp, vp, ctypes.c_size_t, vp]
+        L.fa_decode.restype = i32
+        L.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.fa_decode_workspace_size.restype = ctypes.c_size_t
         L.fa_tile_counts.argtypes = [i32, ctypes.POINTER(ctypes.c_int), i32, ctypes.POINTER(ctypes.c_longlong)]
         L.fa_tile_counts.restype = i32
         L.fa_stream_status.argtypes = [vp]
@@ -111,6 +115,17 @@ def fa_bwd_workspace_size(Hq, T, d):
     return int(lib().fa_bwd_workspace_size(Hq, T, d))
 
 
+def fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace, stream=None):
+    """One decoding step into caller-allocated ``o`` [B,Hq,d] bf16 and ``lse`` [Hq,B] f32."""
+    _check(lib().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, T, float(scale),
+                           _ptr(cu_seqlens_k), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream)))
+
+
+def fa_decode_workspace_size(B, Hq, d, max_seqlen_k):
+    return int(lib().fa_decode_workspace_size(B, Hq, d, max_seqlen_k))
+
+
 def fa_tile_counts(lengths, causal):
     n = len(lengths)
     arr = (ctypes.c_int * max(n, 1))(*[int(x) for x in lengths])
@@ -145,6 +160,28 @@ def attention_forward(q, k, v, causal, scale=None, cu_seqlens=None, max_seqlen=N
     o = torch.empty_like(q)
     lse = torch.empty(Hq, T, dtype=torch.float32, device=q.device)
     fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, stream)
+    return o, lse
+
+
+def attention_decode(q, k, v, scale=None, cu_seqlens_k=None, max_seqlen_k=None, workspace=None, stream=None):
+    """Allocates o, lse (and the workspace if not given) and calls :func:`fa_decode`.
+
+    q [B,Hq,d]: one new query per sequence; k/v [T,Hkv,d]: the K/V cache,
+    batched (``T == B * max_seqlen_k``) or packed by ``cu_seqlens_k``.
+    """
+    B, Hq, d = q.shape
+    T, Hkv, _ = k.shape
+    if scale is None:
+        scale = d ** -0.5
+    if cu_seqlens_k is None:
+        N = max_seqlen_k or T // B
+    else:
+        N = max_seqlen_k
+    if workspace is None:
+        workspace = torch.empty(fa_decode_workspace_size(B, Hq, d, N), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, B, dtype=torch.float32, device=q.device)
+    fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace, stream)
     return o, lse
 
 

@@ -11,6 +11,11 @@ bfloat16 (round to nearest even).  ``scale`` is 1/sqrt(d).  Packed
 variable-length workloads list their sequence lengths literally; they were drawn
 once as ``torch.randint(512, 8193, (8,))`` from a CPU generator seeded 0 and are
 frozen here so that no torch version can change them.
+
+Decoding workloads (``decode=True``) have one new query token per sequence:
+the generator draws q shaped ``[B, Hq, d]`` and then k, v shaped
+``[T, Hkv, d]`` (the K/V cache, T = the summed cache lengths), each rounded to
+bfloat16 as above.
 """
 from __future__ import annotations
 
@@ -19,7 +24,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_qkv"]
+__all__ = ["Workload", "WORKLOADS", "make_decode_qkv", "make_inputs", "make_qkv"]
 
 
 @dataclass(frozen=True)
@@ -33,6 +38,7 @@ class Workload:
     causal: bool
     lengths: tuple = field(default=())  # packed sequences; empty = batched
     backward: bool = False
+    decode: bool = False  # one new query per sequence against a K/V cache of the lengths above
 
     @property
     def seq_lengths(self) -> list:
@@ -49,6 +55,19 @@ class Workload:
     @property
     def varlen(self) -> bool:
         return bool(self.lengths)
+
+    def kv_cache_bytes(self) -> int:
+        """Bytes of the K and V caches a decoding step reads (bf16)."""
+        return 2 * self.T * self.Hkv * self.d * 2
+
+    def decode_bytes(self) -> int:
+        """Algorithmic bytes of one decoding step: the K/V caches read once,
+        q and o (bf16) and the LSE (f32)."""
+        return self.kv_cache_bytes() + 2 * self.B * self.Hq * self.d * 2 + self.B * self.Hq * 4
+
+    def decode_flops(self) -> float:
+        """Algorithmic FLOPs of one decoding step: 4 L d per (sequence, query head)."""
+        return sum(4.0 * L * self.d for L in self.seq_lengths) * self.Hq
 
     def fwd_flops(self) -> float:
         """Algorithmic forward FLOPs: 4 L^2 d per (sequence, query head),
@@ -75,6 +94,15 @@ WORKLOADS = {
         "fwdbwd_b2_h16_n4096_d64_causal", 2, 16, 16, 4096, 64, True, (), True),
     "fwdbwd_b2_h32_n4096_d128_causal": Workload(
         "fwdbwd_b2_h32_n4096_d128_causal", 2, 32, 32, 4096, 128, True, (), True),
+    # 64 sequences with 4096 cached tokens each, 64 query heads sharing 8 K/V
+    # heads (the grouping the GQA section names for Llama-2 70B), d = 128: one
+    # step reads 1.07 GB of K/V cache.
+    "decode_b64_hq64_hkv8_n4096_d128": Workload(
+        "decode_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True),
+    # the packed workload's sequences and heads, one new token each
+    "decode_varlen8_hq32_hkv8_d128": Workload(
+        "decode_varlen8_hq32_hkv8_d128", 8, 32, 8, max(VARLEN_LENGTHS), 128, False, VARLEN_LENGTHS, False,
+        True),
 }
 
 
@@ -104,8 +132,23 @@ def cu_seqlens_of(lengths) -> torch.Tensor:
     return torch.tensor(cu, dtype=torch.int32)
 
 
+def make_decode_qkv(B, Hq, T, Hkv, d, seed=0):
+    """Draw q [B,Hq,d] (one new query per sequence) and the K/V cache k, v
+    [T,Hkv,d] as bf16 CPU tensors."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Hq, d, generator=g)
+    k = torch.randn(T, Hkv, d, generator=g)
+    v = torch.randn(T, Hkv, d, generator=g)
+    return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
+
+
 def make_inputs(w: Workload, seed=0, with_do=None):
-    """Inputs of workload ``w`` on the CPU: q, k, v (, do) bf16 and cu_seqlens int32."""
+    """Inputs of workload ``w`` on the CPU: q, k, v (, do) bf16 and cu_seqlens int32
+    (decoding workloads: q [B,Hq,d], the K/V cache and its offsets)."""
+    if w.decode:
+        t = make_decode_qkv(w.B, w.Hq, w.T, w.Hkv, w.d, seed=seed)
+        t["cu_seqlens"] = cu_seqlens_of(w.seq_lengths)
+        return t
     if with_do is None:
         with_do = w.backward
     t = make_qkv(w.T, w.Hq, w.Hkv, w.d, seed=seed, with_do=with_do)

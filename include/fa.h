@@ -117,6 +117,46 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 size_t fa_bwd_workspace_size(int Hq, long long T, int d);
 
 /*
+ * One decoding step with the K/V cache split into chunks ("Flash-Decoding").
+ * Every sequence b has one new query token whose query q[b] attends to all
+ * of the sequence's cached keys and values; the result for each query head
+ * is O = softmax(scale * K q) V and its LSE ("Attention 算子优化…", section 五:
+ * the new token's query against the cached K/V of all earlier tokens, a
+ * matrix-vector product bound by HBM bandwidth; "FlashAttention：从 Safe
+ * Softmax 到分块计算", section 10: one or a few queries against a long cache
+ * call for a split-K/V strategy).  The cache of each sequence is processed in
+ * splits whose partial (O, LSE) are merged with the online-softmax rule of
+ * section 3 of the same page, which is exact.
+ *
+ *   q   [B, Hq, d]  bf16, 16-byte aligned: the new token's query of each sequence (in)
+ *   k   [T, Hkv, d] bf16, 16-byte aligned: the K cache                      (in)
+ *   v   [T, Hkv, d] bf16, 16-byte aligned: the V cache                      (in)
+ *   o   [B, Hq, d]  bf16, 16-byte aligned                                   (out)
+ *   lse [Hq, B]     f32, 4-byte aligned: natural-log LSE of the scaled scores (out)
+ *   B, Hq, Hkv, d   as for fa_fwd; Hq / Hkv must be at most 16
+ *                   (FA_ERR_UNSUPPORTED otherwise).
+ *   N   longest cache (batched mode: every sequence caches N tokens).
+ *   T   cached tokens in all: B * N in batched mode, cu_seqlens_k[B] in packed mode.
+ *   cu_seqlens_k  NULL (batched) or device int32 [B + 1] offsets of each
+ *                 sequence's cache in k / v (packed); an empty cache gives
+ *                 O = 0 and LSE = -inf.
+ *   workspace     device scratch of at least fa_decode_workspace_size(B, Hq,
+ *                 d, N) bytes, 256-byte aligned (per-split partial results);
+ *                 contents on entry are ignored.
+ *   Other conventions, errors and asynchrony as for fa_fwd.  The query is the
+ *   newest token of its sequence, so no key is masked.
+ */
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int Hq, int Hkv, int N, int d, long long T, float scale,
+              const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_decode needs for B sequences, Hq query heads, head
+ * dimension d and caches of at most max_seqlen_k tokens (an upper bound over
+ * every split length the library picks).  Returns 0 for non-positive
+ * arguments. */
+size_t fa_decode_workspace_size(int B, int Hq, int d, int max_seqlen_k);
+
+/*
  * Host-side count of the (query tile, key tile) pairs the forward kernel
  * processes per query head, for each sequence, with the kernel's 128 x 128
  * tiles: under the causal mask tiles entirely above the diagonal are skipped

@@ -88,3 +88,28 @@ def test_binding_raises_fa_error(fa):
     t = torch.empty(0)
     with pytest.raises(fa.FAError):
         fa._check(call_fwd(fa, d=96))
+
+
+def test_decode_workspace_size(fa):
+    # per (sequence, query head): at most ceil(N / 128) splits of d f32 plus one f32 LSE
+    n = 4 * 8 * 32
+    assert fa.fa_decode_workspace_size(4, 8, 128, 4096) == n * 128 * 4 + n * 4
+    assert fa.fa_decode_workspace_size(1, 1, 64, 1) == 256 + 256
+    assert fa.fa_decode_workspace_size(0, 8, 64, 10) == 0
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(d=96), "INVALID_ARG"), (dict(Hq=34, Hkv=2), "UNSUPPORTED"), (dict(Hq=3, Hkv=2), "INVALID_ARG"),
+    (dict(B=0), "INVALID_ARG"), (dict(T=100), "INVALID_ARG"), (dict(scale=0.0), "INVALID_ARG"),
+    (dict(ws_bytes=16), "INVALID_ARG"), (dict(ws=fake(20) + 16), "INVALID_ARG"), (dict(ws=0), "INVALID_ARG"),
+    (dict(q=fake(1) + 8), "INVALID_ARG"), (dict(lse=fake(5) + 2), "INVALID_ARG"),
+])
+def test_decode_rejects_bad_arguments_on_host(fa, kw, code):
+    a = dict(q=fake(1), k=fake(2), v=fake(3), o=fake(4), lse=fake(5), B=2, Hq=8, Hkv=2, N=512, d=64, T=1024,
+             scale=0.125, cu=None, ws=fake(20), ws_bytes=1 << 30)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    rc = fa.lib().fa_decode(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["o"]), vp(a["lse"]), a["B"], a["Hq"], a["Hkv"],
+                            a["N"], a["d"], a["T"], a["scale"], a["cu"], vp(a["ws"]), a["ws_bytes"], None)
+    assert rc == getattr(fa, "FA_ERR_" + code)
+    assert fa.lib().fa_last_error_string().decode()
