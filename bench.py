@@ -110,6 +110,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def traffic_entry(path, workload, kernel):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/traffic.json), or None."""
+    if not path or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entries = json.load(f).get("entries", [])
+    for e in entries:
+        if e.get("workload") == workload and e.get("kernel") == kernel:
+            return e.get("bytes_per_launch")
+    return None
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -268,11 +281,9 @@ def bench_ours(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
-    if args.traffic_file and os.path.exists(args.traffic_file):
-        with open(args.traffic_file) as f:
-            tr = json.load(f)
-        if tr.get("workload") == w.name and tr.get("kernel") == kern:
-            line["roofline"]["traffic"] = tr.get("bytes_per_launch")
+    tr = traffic_entry(args.traffic_file, w.name, kern)
+    if tr is not None:
+        line["roofline"]["traffic"] = tr
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     if pg:
@@ -405,11 +416,9 @@ def bench_decode(args, world, rank, local):
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
-    if args.traffic_file and os.path.exists(args.traffic_file):
-        with open(args.traffic_file) as f:
-            tr = json.load(f)
-        if tr.get("workload") == w.name:
-            line["roofline"]["traffic"] = tr.get("bytes_per_launch")
+    tr = traffic_entry(args.traffic_file, w.name, line["roofline"]["kernel"])
+    if tr is not None:
+        line["roofline"]["traffic"] = tr
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(w, budget_s=args.cpu_seconds)
     if pg:
