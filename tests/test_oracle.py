@@ -419,3 +419,65 @@ def test_decode_gqa_equals_repeated_heads():
     o2, l2 = DEC(q, rep(k), rep(v), cu, 0.4)
     np.testing.assert_allclose(o1, o2, rtol=1e-14)
     np.testing.assert_allclose(l1, l2, rtol=1e-14)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) K/V cache
+
+from oracle import quant as Q8  # noqa: E402
+
+
+def test_e4m3_decoding_of_every_code_matches_torch():
+    """All 256 codes against torch's float8_e4m3fn, a library implementation
+    of the same format (NaN codes: 0x7F and 0xFF)."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = Q8.e4m3_decode(codes)
+    nan = np.isnan(ref)
+    assert (nan == np.isnan(got)).all() and nan.sum() == 2
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def test_e4m3_rounding_matches_torch_and_round_trips():
+    """Every grid point, every midpoint (ties go to the even code) and random
+    float32 values within the range where torch does not overflow."""
+    import torch
+    grid = Q8.e4m3_decode(np.arange(256, dtype=np.uint8))
+    grid = np.unique(grid[np.isfinite(grid)])
+    mids = (grid[1:] + grid[:-1]) / 2
+    rnd = np.random.default_rng(0).uniform(-464, 464, 20000)
+    small = np.random.default_rng(1).uniform(-0.05, 0.05, 20000)
+    x = np.concatenate([grid, mids, [464.0, -464.0], rnd, small]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(Q8.e4m3_round(x.astype(np.float64)), ref)
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    np.testing.assert_array_equal(Q8.e4m3_encode(Q8.e4m3_decode(codes)), codes)
+
+
+def test_e4m3_saturates_and_rounds_ties_to_even():
+    assert Q8.e4m3_round(np.array([449.0, 470.0, 1e6, -500.0])).tolist() == [448.0, 448.0, 448.0, -448.0]
+    # 1.0625 lies halfway between 1.0 (mantissa 0) and 1.125 (mantissa 1): to 1.0
+    # 1.1875 lies halfway between 1.125 and 1.25 (mantissa 2): to 1.25
+    assert Q8.e4m3_round(np.array([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10])).tolist() == [
+        1.0, 1.25, 0.0, 2.0 ** -8]
+
+
+def test_row_quantisation_scale_rule_and_error_bound():
+    r = np.random.default_rng(2)
+    x = r.standard_normal((40, 3, 64)).astype(np.float32)
+    x[5, 1] = 0.0  # an all-zero row
+    x[7, 2] *= 1e-3
+    codes, s = Q8.quantize_rows_fp8(x)
+    assert codes.dtype == np.uint8 and s.dtype == np.float32 and s.shape == (40, 3)
+    deq = Q8.dequantize_rows_fp8(codes, s)
+    amax = np.abs(x).max(axis=-1)
+    live = amax > 0
+    np.testing.assert_array_equal(s[live], (amax[live] / np.float32(448)).astype(np.float32))
+    assert s[5, 1] == 1.0 and (codes[5, 1] == 0).all()
+    # the row's largest element lands on +-448 (to float32 rounding of x / s)
+    top = np.take_along_axis(np.abs(deq), np.abs(x).argmax(-1)[..., None], -1)[..., 0]
+    np.testing.assert_allclose(top[live], amax[live], rtol=2e-7)
+    # half a quantum: 2^-4 relative in the normal range, 2^-10 s below it
+    err = np.abs(deq - x)
+    assert (err <= 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * s[..., None] * (1 + 1e-6)).all()
