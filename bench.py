@@ -291,7 +291,7 @@ def bench_ours(args, world, rank, local):
     return line if rank == 0 else None
 
 
-DECODE_METRIC = "attention decode step, K/V cache bytes read per second (bf16, 1xGB300)"
+DECODE_METRIC = "attention decode step, K/V cache bytes read per second (1xGB300)"
 
 
 def bench_decode(args, world, rank, local):
@@ -321,9 +321,17 @@ def bench_decode(args, world, rank, local):
     lse = torch.empty(Hq, B, dtype=torch.float32, device=dev)
     ws = torch.empty(fa.fa_decode_workspace_size(B, Hq, d, N), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    if w.fp8:
+        # the cache is quantised when it is written, before the decoding steps
+        k8, ks = fa.kv_quantize_fp8(k)
+        v8, vs = fa.kv_quantize_fp8(v)
+        del k, v
 
     def step():
-        fa.fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, w.scale, cu, ws, stream)
+        if w.fp8:
+            fa.fa_decode_fp8(q, k8, v8, ks, vs, o, lse, B, Hq, Hkv, N, d, T, w.scale, cu, ws, stream)
+        else:
+            fa.fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, w.scale, cu, ws, stream)
 
     for _ in range(args.warmup):
         step()
@@ -399,16 +407,18 @@ def bench_decode(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3 cache, f16 products" if w.fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                    "seq_lengths": w.seq_lengths if w.varlen else None, "queries_per_sequence": 1,
+                   "kv_cache": "E4M3 codes + f32 per-token scales" if w.fp8 else "bf16",
                    "kv_cache_bytes": w.kv_cache_bytes(), "bytes_per_step": nbytes,
                    "gflop_per_step": round(w.decode_flops() / 1e9, 3),
                    "tokens_per_s": round(B * world / (avg_ms * 1e-3), 1),
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "fa_decode (split kernel + combine)", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": ("fa_decode_fp8" if w.fp8 else "fa_decode") + " (split kernel + combine)",
+                     "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None},
         "e2e": {"value": round(nbytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
@@ -440,10 +450,19 @@ def oracle_decode_sample(w, n_seq, seed=0):
     t = make_decode_qkv(n_seq, w.Hq, T, w.Hkv, w.d, seed=seed)
     f64 = {n: t[n].to(torch.float64).numpy() for n in t}
     cu = oracle.cu_from_lengths(lens)
+    if w.fp8:
+        from oracle import quant
+        k8, ks = quant.quantize_rows_fp8(t["k"].float().numpy())
+        v8, vs = quant.quantize_rows_fp8(t["v"].float().numpy())
     t0 = time.perf_counter()
-    oracle.attention_decode(f64["q"], f64["k"], f64["v"], cu, w.scale)
+    if w.fp8:
+        oracle.attention_decode(f64["q"], quant.dequantize_rows_fp8(k8, ks), quant.dequantize_rows_fp8(v8, vs), cu,
+                                w.scale)
+    else:
+        oracle.attention_decode(f64["q"], f64["k"], f64["v"], cu, w.scale)
     sec = time.perf_counter() - t0
-    nbytes = 2 * T * w.Hkv * w.d * 2 + 2 * n_seq * w.Hq * w.d * 2 + n_seq * w.Hq * 4
+    per_tok = 2 * w.Hkv * ((w.d + 4) if w.fp8 else 2 * w.d)
+    nbytes = T * per_tok + 2 * n_seq * w.Hq * w.d * 2 + n_seq * w.Hq * 4
     return sec, nbytes
 
 

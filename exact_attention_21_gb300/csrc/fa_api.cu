@@ -20,6 +20,9 @@ int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
 int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream);
+int launch_decode_fp8(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                      cudaStream_t stream);
+int launch_quantize_fp8(int d, const void* x, void* x8, float* scale, long long rows, cudaStream_t stream);
 }  // namespace fa
 
 namespace {
@@ -104,6 +107,23 @@ int make_map(CUtensorMap* map, const void* base, long long T, int H, int d, cons
   cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(fa::kTile)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+  return FA_OK;
+}
+
+// E4M3 [T, H, d] (one byte per element) viewed as (d, H, T); box = 128 columns
+// (one 128-byte row) x 1 head x 128 tokens with the 128-byte swizzle.  Rows
+// past T read as zeros.
+int make_map_u8(CUtensorMap* map, const void* base, long long T, int H, int d, const char* what) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H) * d};
+  cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(fa::kTile)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", what, (int)r);
@@ -286,18 +306,21 @@ size_t fa_decode_workspace_size(int B, int Hq, int d, int max_seqlen_k) {
   return up(rows * d * 4) + up(rows * 4);
 }
 
-int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
-              int d, long long T, float scale, const int* cu_seqlens_k, void* workspace, size_t workspace_bytes,
-              void* stream) {
-  g_err[0] = '\0';
+// Shared by fa_decode and fa_decode_fp8 (k_scale == nullptr: bf16 cache).
+static int decode_common(const void* q, const void* k, const void* v, const float* k_scale, const float* v_scale,
+                         void* o, float* lse, int B, int Hq, int Hkv, int N, int d, long long T, float scale,
+                         const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
+  const bool fp8 = k_scale != nullptr;
   Shape s;
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, 0, cu_seqlens_k, &s);
   if (rc) return rc;
   if (Hq / Hkv > 16) return fail(FA_ERR_UNSUPPORTED, "decode supports up to 16 query heads per K/V head");
-  if (!q || !k || !v || !o || !lse || !workspace) return fail(FA_ERR_INVALID_ARG, "null pointer");
+  if (fp8 && d != 128) return fail(FA_ERR_UNSUPPORTED, "the E4M3 cache is supported for d = 128");
+  if (!q || !k || !v || !o || !lse || !workspace || (fp8 && !v_scale)) return fail(FA_ERR_INVALID_ARG, "null pointer");
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
     return fail(FA_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned");
-  if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  if (!aligned(lse, 4) || (fp8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))))
+    return fail(FA_ERR_INVALID_ARG, "lse and the scales must be 4-byte aligned");
   if (!aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   const size_t need = fa_decode_workspace_size(B, Hq, d, N);
   if (workspace_bytes < need)
@@ -305,12 +328,18 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   DeviceState* dev = nullptr;
   if ((rc = device_state(&dev))) return rc;
   CUtensorMap tk, tv;
-  if ((rc = make_map(&tk, k, T, Hkv, d, "k")) || (rc = make_map(&tv, v, T, Hkv, d, "v"))) return rc;
+  if (fp8) {
+    if ((rc = make_map_u8(&tk, k, T, Hkv, d, "k")) || (rc = make_map_u8(&tv, v, T, Hkv, d, "v"))) return rc;
+  } else if ((rc = make_map(&tk, k, T, Hkv, d, "k")) || (rc = make_map(&tv, v, T, Hkv, d, "v"))) {
+    return rc;
+  }
   fa::DecodeParams p{};
   p.q = q;
   p.o = o;
   p.lse = lse;
   p.cu = cu_seqlens_k;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.status = dev->status;
   p.T = T;
   p.B = B;
@@ -324,9 +353,42 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.o_part = static_cast<float*>(workspace);
   p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * d * 4 + 255) / 256 * 256);
   p.scale_log2 = scale * 1.4426950408889634f;
-  int e = fa::launch_decode(d, tk, tv, p, static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int e = fp8 ? fa::launch_decode_fp8(d, tk, tv, p, st) : fa::launch_decode(d, tk, tv, p, st);
   if (e == -1) return fail(FA_ERR_UNSUPPORTED, "decode kernel unavailable for d = %d, group %d", d, p.group);
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "decode launch failed: %s", cudaGetErrorString((cudaError_t)e));
+  return FA_OK;
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+              int d, long long T, float scale, const int* cu_seqlens_k, void* workspace, size_t workspace_bytes,
+              void* stream) {
+  g_err[0] = '\0';
+  return decode_common(q, k, v, nullptr, nullptr, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace,
+                       workspace_bytes, stream);
+}
+
+int fa_decode_fp8(const void* q, const void* k8, const void* v8, const float* k_scale, const float* v_scale,
+                  void* o, float* lse, int B, int Hq, int Hkv, int N, int d, long long T, float scale,
+                  const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "null scale pointer");
+  return decode_common(q, k8, v8, k_scale, v_scale, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace,
+                       workspace_bytes, stream);
+}
+
+int fa_kv_quantize_fp8(const void* x, void* x8, float* scale, long long rows, int d, void* stream) {
+  g_err[0] = '\0';
+  if (d != 64 && d != 128) return fail(FA_ERR_INVALID_ARG, "d must be 64 or 128 (got %d)", d);
+  if (rows < 1 || rows > (1ll << 40) / d) return fail(FA_ERR_INVALID_ARG, "rows must be in [1, 2^40 / d]");
+  if (!x || !x8 || !scale) return fail(FA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scale, 4))
+    return fail(FA_ERR_INVALID_ARG, "x and x8 must be 16-byte aligned, scale 4-byte aligned");
+  DeviceState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc) return rc;
+  int e = fa::launch_quantize_fp8(d, x, x8, scale, rows, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "quantize launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;
 }
 

@@ -84,6 +84,8 @@ struct DecodeParams {
   float* o_part;      // f32 [B, Hq, n_splits, d]: normalised output of each split
   float* lse_part;    // f32 [B, Hq, n_splits]
   const int* cu;      // device int32 [B + 1] offsets into the K/V cache, or null
+  const float* k_scale;  // E4M3 cache only: f32 [T, Hkv] per-token scales
+  const float* v_scale;
   unsigned* status;
   long long T;        // cached tokens in all
   int B, Hq, Hkv, N, group;

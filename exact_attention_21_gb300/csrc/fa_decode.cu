@@ -28,6 +28,8 @@
 //            over one 1/(512/d) slice of the tile's keys; the slices are
 //            summed once at the end of the split.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "fa_common.cuh"
 
@@ -320,32 +322,51 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 //   warps 2-5  softmax warpgroup: thread = key row of S^T (TMEM lane) for the
 //              probabilities, and = dimension row of O^T for the rescale and
 //              the split's output.
+//   warps 6-9  (FP8 cache only) converter warpgroup: dequantises each E4M3
+//              K / V tile into a 16-bit tile in shared memory ("Attention 算子
+//              优化…", section 六: the cache stays FP8 in HBM, dequantisation
+//              happens on chip, the products run in 16-bit, softmax and
+//              accumulation in f32).
 // S^T is double-buffered in TMEM, so S^T of tile i+1 runs while the softmax
-// works on tile i; P^T (bf16, K-major: 16 head rows x 128 keys) is
+// works on tile i; P^T (16-bit, K-major: 16 head rows x 128 keys) is
 // double-buffered in shared memory.  The running max of a head only moves
 // when a tile's max exceeds it by more than kDecRescaleSlack (log2 units);
 // any common reference gives the same merge, so this is exact and O^T is
 // rarely rescaled.
+//
+// With the FP8 cache the products run in f16 (the E4M3 values and the bf16
+// query convert to f16 without rounding, apart from query elements below
+// 2^-14), and the per-token scales fold into the per-key work of the softmax
+// threads: s_k multiplies the key's scores, s_v its probabilities before the
+// P V product (the row sum keeps the unscaled probabilities).
 constexpr int kDecHeads = 16;               // MMA N: query heads per CTA, padded
 constexpr float kDecRescaleSlack = 8.f;
 
+template <bool FP8>
 struct DecTcLayout {
   static constexpr int D = 128;
-  static constexpr int kChunkBytes = kTile * 128;   // 128 keys x 64 dims
-  static constexpr int kTileBytes = 2 * kChunkBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kChunkBytes = kTile * 128;      // 16-bit tile chunk: 128 keys x 64 dims
+  static constexpr int kTileBytes = 2 * kChunkBytes;   // 16-bit 128 x 128 tile
+  static constexpr int kTile8Bytes = kTile * 128;      // E4M3 128 x 128 tile (one 128-byte row per key)
+  // TMA stages: 16-bit K and V tiles, or E4M3 K and V tiles
+  static constexpr int kStageBytes = FP8 ? 2 * kTile8Bytes : 2 * kTileBytes;
   static constexpr int kStages = 3;
-  static constexpr int kHChunkBytes = kDecHeads * 128;  // 16 rows x 64 elements
+  // FP8: dequantised K (two buffers, freed when S^T completes) and V (one
+  // buffer, freed when the previous P V completes)
+  static constexpr int kCvtBytes = FP8 ? 3 * kTileBytes : 0;
+  static constexpr int kHChunkBytes = kDecHeads * 128;  // 16 rows x 64 16-bit elements
   static constexpr int kQBytes = 2 * kHChunkBytes;      // Q: 16 heads x 128 dims, K-major
   static constexpr int kPBytes = 2 * kHChunkBytes;      // P^T: 16 heads x 128 keys, K-major
-  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffCvt = kStages * kStageBytes;
+  static constexpr int kOffQ = kOffCvt + kCvtBytes;
   static constexpr int kOffP = kOffQ + kQBytes;          // two buffers
   static constexpr int kOffRed = kOffP + 2 * kPBytes;    // f32 [4 warps][16 heads]
   static constexpr int kOffBar = kOffRed + 4 * kDecHeads * 4;
-  // full[3], empty[3], q_ready, s_full[2], p_ready[2], pv_done[2], drain
-  static constexpr int kNumBars = 2 * kStages + 8;
+  // full[], empty[], q_ready, s_full[2], p_ready[2], pv_done[2], drain, k_ready[2], v_ready
+  static constexpr int kNumBars = 2 * kStages + 11;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
+  static constexpr int kThreads = FP8 ? 320 : 192;
   static constexpr uint32_t kTmemCols = 64;
   static constexpr uint32_t kColS = 0, kColO = 32;  // S^T buffers at 0 and 16
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
@@ -365,13 +386,34 @@ __device__ __forceinline__ bool softmax_sync_and(bool v) {
   return r != 0;
 }
 
-__global__ void __launch_bounds__(192, 1)
+// Barrier among the 128 softmax threads; returns whether `v` held in any of them.
+__device__ __forceinline__ bool softmax_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+// Two E4M3 codes (low byte first) -> two f16 (low half first), exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(DecTcLayout<FP8>::kThreads, 1)
 fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const DecodeParams p) {
-  using Lay = DecTcLayout;
+  using Lay = DecTcLayout<FP8>;
   constexpr int NS = Lay::kStages;
   constexpr int D = Lay::D;
   constexpr int H = kDecHeads;
+  // the MMAs read 16-bit operands: bf16 for a bf16 cache, f16 for an E4M3 one
+  constexpr uint32_t id_s = FP8 ? idesc_f16_f32(kTile, H, false, false) : idesc_bf16_f32(kTile, H, false, false);
+  constexpr uint32_t id_o = FP8 ? idesc_f16_f32(D, H, true, false) : idesc_bf16_f32(D, H, true, false);
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   long long seq0;
@@ -392,25 +434,34 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint64_t* q_ready = empty + NS;
   uint64_t* s_full = q_ready + 1;
   uint64_t* p_ready = s_full + 2;
-  uint64_t* pv_done = p_ready + 2;
+  uint64_t* pv_done = p_ready + 2;  // FP8: also frees dequantised buffer i & 1
   uint64_t* drain = pv_done + 2;
+  uint64_t* k_ready = drain + 1;     // FP8 only: dequantised K of tile i in buffer i & 1
+  uint64_t* v_ready = k_ready + 2;   // FP8 only: dequantised V of the next tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
   auto stage = [&](int st) { return smem + st * Lay::kStageBytes; };
   auto pbuf = [&](int i) { return smem + Lay::kOffP + (i & 1) * Lay::kPBytes; };
+  // 16-bit K and V tiles the MMAs of tile i read
+  auto k16 = [&](int i) { return FP8 ? smem + Lay::kOffCvt + (i & 1) * Lay::kTileBytes : stage(i % NS); };
+  auto v16 = [&](int i) {
+    return FP8 ? smem + Lay::kOffCvt + 2 * Lay::kTileBytes : stage(i % NS) + Lay::kTileBytes;
+  };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full + i, 1);
-      mbar_init(empty + i, 1);
+      mbar_init(empty + i, FP8 ? 128 : 1);  // FP8: released by the converters
     }
     mbar_init(q_ready, 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_ready + i, 128);
       mbar_init(pv_done + i, 1);
+      mbar_init(k_ready + i, 128);
     }
+    mbar_init(v_ready, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -440,9 +491,14 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (i >= NS && !(ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag))) break;
         mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
         const int row = static_cast<int>(seq0 + static_cast<long long>(t0 + i) * kTile);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_3d(stage(st) + c * Lay::kChunkBytes, &tm_k, full + st, c * 64, g, row);
-          tma_load_3d(stage(st) + Lay::kTileBytes + c * Lay::kChunkBytes, &tm_v, full + st, c * 64, g, row);
+        if constexpr (FP8) {
+          tma_load_3d(stage(st), &tm_k, full + st, 0, g, row);
+          tma_load_3d(stage(st) + Lay::kTile8Bytes, &tm_v, full + st, 0, g, row);
+        } else {
+          for (int c = 0; c < 2; ++c) {
+            tma_load_3d(stage(st) + c * Lay::kChunkBytes, &tm_k, full + st, c * 64, g, row);
+            tma_load_3d(stage(st) + Lay::kTileBytes + c * Lay::kChunkBytes, &tm_v, full + st, c * 64, g, row);
+          }
         }
         ++issued;
       }
@@ -454,14 +510,13 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(kTile, H, false, false);  // K (K-major) x Q (K-major)
-      constexpr uint32_t id_o = idesc_bf16_f32(D, H, true, false);       // V^T (MN-major) x P^T (K-major)
       const uint32_t sQa = smem_u32(sQ);
       auto issue_s = [&](int i) -> bool {
-        const int st = i % NS;
-        if (!mbar_wait(full + st, (i / NS) & 1, abort_flag)) return false;
+        // the 16-bit K tile of tile i: loaded (bf16) or dequantised (FP8)
+        if (!mbar_wait(FP8 ? k_ready + (i & 1) : full + i % NS, FP8 ? (i >> 1) & 1 : (i / NS) & 1, abort_flag))
+          return false;
         tc_fence_after();
-        const uint32_t sKa = smem_u32(stage(st));
+        const uint32_t sKa = smem_u32(k16(i));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + Lay::kColS + (i & 1) * H,
@@ -474,16 +529,16 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (ok) ok = issue_s(0);
       if (ok && nt > 1) ok = issue_s(1);
       for (int i = 0; i < nt && ok; ++i) {
-        const int st = i % NS;
         // P^T of tile i written, S^T buffer i & 1 read, O^T rescaled
         if (!(ok = mbar_wait(p_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
+        if (FP8 && !(ok = mbar_wait(v_ready, i & 1, abort_flag))) break;
         tc_fence_after();
-        const uint32_t sVa = smem_u32(stage(st) + Lay::kTileBytes), sPa = smem_u32(pbuf(i));
+        const uint32_t sVa = smem_u32(v16(i)), sPa = smem_u32(pbuf(i));
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_ss(tmem + Lay::kColO, sdesc_sw128(sVa + kk * 2048, Lay::kChunkBytes, 1024),
                   sdesc_sw128(sPa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_o, (i > 0 || kk > 0));
-        umma_commit(empty + st);
+        if constexpr (!FP8) umma_commit(empty + i % NS);
         umma_commit(pv_done + (i & 1));
         if (i + 2 < nt && !(ok = issue_s(i + 2))) break;
       }
@@ -492,7 +547,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       int never = 0;
       mbar_wait(drain, 0, &never);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ softmax warpgroup
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // key row of S^T, dimension row of O^T
@@ -508,7 +563,15 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int u = u2 + j;  // unit of the 256-byte row: chunk u / 8, unit u % 8
-        const uint4 val = h < group ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+        uint4 val = h < group ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (FP8) {  // bf16 -> f16 for the f16 products
+          uint32_t* w = reinterpret_cast<uint32_t*>(&val);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 hh = __floats2half2_rn(bf16_lo(w[e]), bf16_hi(w[e]));
+            w[e] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+        }
         *reinterpret_cast<uint4*>(sQ + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = val;
       }
       fence_proxy_async_smem();
@@ -525,36 +588,60 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // need whole warps) and the loop ends only on a vote of all 128 threads.
     bool ok = true;
     for (int i = 0; i < nt; ++i) {
+      const int kpos = (t0 + i) * kTile + r;
+      const bool valid = kpos < L;
+      float sk = 1.f, sv = 1.f;  // per-token scales of this key (FP8 cache)
+      if constexpr (FP8) {
+        if (valid) {
+          const long long si = (seq0 + kpos) * p.Hkv + g;
+          sk = __ldg(p.k_scale + si);
+          sv = __ldg(p.v_scale + si);
+        }
+      }
       bool w = __all_sync(0xffffffffu, mbar_wait(s_full + (i & 1), (i >> 1) & 1, abort_flag));
       float x[H];
+      bool over = false;  // a score above its head's reference by more than the slack
       if (w) {
         tc_fence_after();
-        uint32_t sv[H];
-        tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (i & 1) * H, lane_base, 0), sv);
-        const bool valid = (t0 + i) * kTile + r < L;
+        uint32_t svv[H];
+        tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (i & 1) * H, lane_base, 0), svv);
+        const float ck = c * sk;
 #pragma unroll
         for (int h = 0; h < H; ++h) {
-          x[h] = valid ? __uint_as_float(sv[h]) * c : -INFINITY;
+          x[h] = valid ? __uint_as_float(svv[h]) * ck : -INFINITY;
+          over |= x[h] > m[h] + kDecRescaleSlack;  // always for a valid key on the first tile (m = -inf)
+        }
+      }
+      bool bump = false;
+      float alpha[H];
+#pragma unroll
+      for (int h = 0; h < H; ++h) alpha[h] = 1.f;
+      // One vote per tile: in the common case no reference moves and the
+      // probabilities are taken against the current m.  Otherwise (the first
+      // tile, a score jump, or a wait that gave up) the tile max of every
+      // head is reduced over the 128 keys.
+      if (softmax_sync_or(over || !w)) {
+        if (!(ok = softmax_sync_and(w))) break;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
           float mx = x[h];
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
           if (lane == 0) sRed[quad * H + h] = mx;
         }
-      }
-      if (!(ok = softmax_sync_and(w))) break;
-      bool bump = false;
-      float alpha[H];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
-        const float tm = fmaxf(fmaxf(sRed[h], sRed[H + h]), fmaxf(sRed[2 * H + h], sRed[3 * H + h]));
-        // the tile's key 0 is valid, so tm is finite
-        const bool up = tm > m[h] + kDecRescaleSlack;  // always on the first tile (m = -inf)
-        const float mn = up ? tm : m[h];
-        alpha[h] = up ? ex2_approx(m[h] - mn) : 1.f;
-        bump |= up;
-        m[h] = mn;
+        for (int h = 0; h < H; ++h) {
+          const float tm = fmaxf(fmaxf(sRed[h], sRed[H + h]), fmaxf(sRed[2 * H + h], sRed[3 * H + h]));
+          // the tile's key 0 is valid, so tm is finite
+          const bool up = tm > m[h] + kDecRescaleSlack;
+          const float mn = up ? tm : m[h];
+          alpha[h] = up ? ex2_approx(m[h] - mn) : 1.f;
+          bump |= up;
+          m[h] = mn;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // sRed is rewritten by the next reduction
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // sRed is rewritten by the next tile
       // P^T buffer i & 1 was last read by P V of tile i - 2
       w = i < 2 || __all_sync(0xffffffffu, mbar_wait(pv_done + (i & 1), ((i - 2) >> 1) & 1, abort_flag));
       if (w) {
@@ -564,8 +651,15 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int h = 0; h < H; ++h) {
           const float pv = ex2_approx(x[h] - m[h]);  // masked keys: 0
           lt[h] = fmaf(lt[h], alpha[h], pv);
-          const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
-          sts_u16(pb + h * 128 + ((pu ^ (h & 7)) << 4), *reinterpret_cast<const uint16_t*>(&pb16));
+          uint16_t bits;
+          if constexpr (FP8) {
+            const __half ph = __float2half_rn(pv * sv);
+            bits = *reinterpret_cast<const uint16_t*>(&ph);
+          } else {
+            const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
+            bits = *reinterpret_cast<const uint16_t*>(&pb16);
+          }
+          sts_u16(pb + h * 128 + ((pu ^ (h & 7)) << 4), bits);
         }
       }
       // m is the same in every thread, so bump is uniform
@@ -618,6 +712,48 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
       }
     }
+  } else if constexpr (FP8) {
+    // ------------------------------------------------------------ converter warpgroup
+    // Thread r dequantises key row r of the tile's K and V: 8 units of 16
+    // E4M3 codes each, into 16 f16 units of the 128-byte-swizzled 16-bit
+    // tiles the MMAs read.  The per-token scales are applied elsewhere.  K of
+    // tile i goes to buffer i & 1 once S^T of tile i - 2 is done with it; V to
+    // the single V buffer once P V of tile i - 1 is done; then the E4M3 stage
+    // is released, so the loads run ahead of the products.
+    const int r = (warp - 6) * 32 + lane;
+    auto convert = [&](const uint8_t* src_tile, uint8_t* dst_tile) {
+      const uint8_t* src = src_tile + r * 128;
+      uint8_t* dst = dst_tile + r * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 e = *reinterpret_cast<const uint4*>(src + ((u ^ (r & 7)) << 4));  // dims 16u .. 16u+15
+        const uint32_t w[4] = {e.x, e.y, e.z, e.w};
+        uint32_t h16[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          h16[2 * j] = e4m3x2_to_f16x2(w[j]);
+          h16[2 * j + 1] = e4m3x2_to_f16x2(w[j] >> 16);
+        }
+        uint8_t* chunk = dst + (u / 4) * Lay::kChunkBytes;
+        const int u0 = 2 * (u % 4);
+        *reinterpret_cast<uint4*>(chunk + ((u0 ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+        *reinterpret_cast<uint4*>(chunk + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+      }
+      fence_proxy_async_smem();
+    };
+    bool ok = true;
+    for (int i = 0; i < nt && ok; ++i) {
+      const int st = i % NS;
+      if (!(ok = mbar_wait(full + st, (i / NS) & 1, abort_flag))) break;
+      if (i >= 2 && !(ok = mbar_wait(s_full + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) break;
+      convert(stage(st), k16(i));
+      mbar_arrive(k_ready + (i & 1));
+      if (i >= 1 && !(ok = mbar_wait(pv_done + ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag))) break;
+      convert(stage(st) + Lay::kTile8Bytes, v16(i));
+      mbar_arrive(v_ready);
+      mbar_arrive(empty + st);  // the E4M3 stage has been read
+    }
+    if (!ok) give_up();
   }
 
   tc_fence_before();
@@ -696,13 +832,15 @@ int launch_decode_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodePa
   return -1;
 }
 
+template <bool FP8>
 int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
-  using Lay = DecTcLayout;
+  using Lay = DecTcLayout<FP8>;
   if (p.group > kDecHeads) return -1;
-  cudaError_t e = cudaFuncSetAttribute(fa_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_decode_tc_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_splits, p.Hkv, p.B);
-  fa_decode_tc_kernel<<<grid, 192, Lay::kBytes, stream>>>(tk, tv, p);
+  fa_decode_tc_kernel<FP8><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(p.B) * p.Hq;
@@ -712,8 +850,58 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
 
 int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
   if (d == 64) return launch_decode_d<64>(tk, tv, p, stream);
-  if (d == 128) return launch_decode_tc(tk, tv, p, stream);
+  if (d == 128) return launch_decode_tc<false>(tk, tv, p, stream);
   return -1;
+}
+
+int launch_decode_fp8(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                      cudaStream_t stream) {
+  if (d == 128) return launch_decode_tc<true>(tk, tv, p, stream);
+  return -1;
+}
+
+// E4M3 quantisation of [rows, D] bf16 rows ("Attention 算子优化…", section 六):
+// one warp per row; s = max|x| / 448 in f32 (1 for an all-zero row),
+// codes = e4m3(x / s) with round-to-nearest-even and saturation.
+template <int D>
+__global__ void __launch_bounds__(256) fa_quantize_fp8_kernel(const __nv_bfloat16* x, uint8_t* x8, float* scale,
+                                                               long long rows) {
+  constexpr int E = D / 32;  // elements per lane
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  float v[E];
+  const __nv_bfloat16* src = x + row * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = __bfloat162float(src[e]);
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint8_t* dst = x8 + row * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const __nv_fp8x2_storage_t two =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(v[e], s), __fdiv_rn(v[e + 1], s)), __NV_SATFINITE, __NV_E4M3);
+    *reinterpret_cast<__nv_fp8x2_storage_t*>(dst + e) = two;
+  }
+  if (lane == 0) scale[row] = s;
+}
+
+int launch_quantize_fp8(int d, const void* x, void* x8, float* scale, long long rows, cudaStream_t stream) {
+  const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+  if (d == 64) {
+    fa_quantize_fp8_kernel<64><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
+                                                           static_cast<uint8_t*>(x8), scale, rows);
+  } else if (d == 128) {
+    fa_quantize_fp8_kernel<128><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
+                                                            static_cast<uint8_t*>(x8), scale, rows);
+  } else {
+    return -1;
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace fa

@@ -23,8 +23,9 @@ FA_ERR_LAUNCH = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_UNSUPPORTED = 5
 
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_workspace_size",
-           "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
+           "fa_decode_workspace_size", "fa_kv_quantize_fp8", "fa_tile_counts", "fa_stream_status",
+           "fa_last_error_string")
 
 
 class FAError(RuntimeError):
@@ -56,6 +57,11 @@ def lib():
         L.fa_bwd_workspace_size.restype = ctypes.c_size_t
         L.fa_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, vp, vp, ctypes.c_size_t, vp]
         L.fa_decode.restype = i32
+        L.fa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, vp, vp,
+                                    ctypes.c_size_t, vp]
+        L.fa_decode_fp8.restype = i32
+        L.fa_kv_quantize_fp8.argtypes = [vp, vp, vp, i64, i32, vp]
+        L.fa_kv_quantize_fp8.restype = i32
         L.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         L.fa_decode_workspace_size.restype = ctypes.c_size_t
         L.fa_tile_counts.argtypes = [i32, ctypes.POINTER(ctypes.c_int), i32, ctypes.POINTER(ctypes.c_longlong)]
@@ -122,6 +128,28 @@ def fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspa
                            _stream(stream)))
 
 
+def fa_decode_fp8(q, k8, v8, k_scale, v_scale, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace,
+                  stream=None):
+    """One decoding step over an E4M3 cache (uint8 codes, f32 per-token scales)."""
+    _check(lib().fa_decode_fp8(_ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), _ptr(o), _ptr(lse), B, Hq,
+                               Hkv, N, d, T, float(scale), _ptr(cu_seqlens_k), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_kv_quantize_fp8(x, x8, scale, stream=None):
+    """Quantises bf16 rows x [..., d] into E4M3 codes x8 (uint8, same shape) and scales [...] (f32)."""
+    d = x.shape[-1]
+    _check(lib().fa_kv_quantize_fp8(_ptr(x), _ptr(x8), _ptr(scale), x.numel() // d, d, _stream(stream)))
+
+
+def kv_quantize_fp8(x, stream=None):
+    """Allocates and returns (codes uint8 [..., d], scales f32 [...]) for bf16 rows x."""
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    fa_kv_quantize_fp8(x, x8, scale, stream)
+    return x8, scale
+
+
 def fa_decode_workspace_size(B, Hq, d, max_seqlen_k):
     return int(lib().fa_decode_workspace_size(B, Hq, d, max_seqlen_k))
 
@@ -182,6 +210,22 @@ def attention_decode(q, k, v, scale=None, cu_seqlens_k=None, max_seqlen_k=None, 
     o = torch.empty_like(q)
     lse = torch.empty(Hq, B, dtype=torch.float32, device=q.device)
     fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace, stream)
+    return o, lse
+
+
+def attention_decode_fp8(q, k8, v8, k_scale, v_scale, scale=None, cu_seqlens_k=None, max_seqlen_k=None,
+                         workspace=None, stream=None):
+    """:func:`attention_decode` over an E4M3 cache (see :func:`kv_quantize_fp8`)."""
+    B, Hq, d = q.shape
+    T, Hkv, _ = k8.shape
+    if scale is None:
+        scale = d ** -0.5
+    N = max_seqlen_k if (cu_seqlens_k is not None or max_seqlen_k) else T // B
+    if workspace is None:
+        workspace = torch.empty(fa_decode_workspace_size(B, Hq, d, N), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, B, dtype=torch.float32, device=q.device)
+    fa_decode_fp8(q, k8, v8, k_scale, v_scale, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace, stream)
     return o, lse
 
 

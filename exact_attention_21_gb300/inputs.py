@@ -39,6 +39,7 @@ class Workload:
     lengths: tuple = field(default=())  # packed sequences; empty = batched
     backward: bool = False
     decode: bool = False  # one new query per sequence against a K/V cache of the lengths above
+    fp8: bool = False     # decoding over an E4M3 cache with per-token f32 scales
 
     @property
     def seq_lengths(self) -> list:
@@ -57,7 +58,10 @@ class Workload:
         return bool(self.lengths)
 
     def kv_cache_bytes(self) -> int:
-        """Bytes of the K and V caches a decoding step reads (bf16)."""
+        """Bytes of the K and V caches a decoding step reads (bf16, or E4M3
+        codes plus one f32 scale per token and K/V head)."""
+        if self.fp8:
+            return 2 * self.T * self.Hkv * (self.d + 4)
         return 2 * self.T * self.Hkv * self.d * 2
 
     def decode_bytes(self) -> int:
@@ -99,6 +103,9 @@ WORKLOADS = {
     # step reads 1.07 GB of K/V cache.
     "decode_b64_hq64_hkv8_n4096_d128": Workload(
         "decode_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True),
+    # the same step over an E4M3 cache (per-token scales)
+    "decode_fp8_b64_hq64_hkv8_n4096_d128": Workload(
+        "decode_fp8_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True, True),
     # the packed workload's sequences and heads, one new token each
     "decode_varlen8_hq32_hkv8_d128": Workload(
         "decode_varlen8_hq32_hkv8_d128", 8, 32, 8, max(VARLEN_LENGTHS), 128, False, VARLEN_LENGTHS, False,

@@ -150,6 +150,36 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
               int B, int Hq, int Hkv, int N, int d, long long T, float scale,
               const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * E4M3 quantisation of K/V cache rows, as written back to the cache
+ * ("Attention 算子优化…", section 六: FP8 K/V cache with per-token scales).
+ * Each row of d elements (one token of one K/V head) gets the f32 scale
+ * s = max|x| / 448 (1 for an all-zero row) and the codes e4m3(x / s), rounded
+ * to nearest even and saturated to +-448 (the "fn" E4M3 variant: no infinities).
+ *
+ *   x      [rows, d] bf16, 16-byte aligned, e.g. a [T, Hkv, d] cache (rows = T * Hkv)  (in)
+ *   x8     [rows, d] E4M3 codes (one byte each), 16-byte aligned                      (out)
+ *   scale  [rows] f32, 4-byte aligned                                                 (out)
+ *   d      64 or 128.
+ * Asynchronous on `stream`; errors as for fa_fwd.
+ */
+int fa_kv_quantize_fp8(const void* x, void* x8, float* scale, long long rows, int d, void* stream);
+
+/*
+ * One decoding step (as fa_decode) over an E4M3 K/V cache produced by
+ * fa_kv_quantize_fp8: the cache stays compressed in HBM and is dequantised in
+ * shared memory; the products run in f16 with f32 accumulation, the softmax
+ * in f32 ("Attention 算子优化…", section 六).  The result is the attention of
+ * q over the dequantised cache k8 * k_scale, v8 * v_scale.
+ *
+ *   k8, v8    [T, Hkv, d] E4M3 codes, 16-byte aligned                 (in)
+ *   k_scale, v_scale  [T, Hkv] f32 per-token scales, 4-byte aligned   (in)
+ *   Other arguments as for fa_decode; d must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ */
+int fa_decode_fp8(const void* q, const void* k8, const void* v8, const float* k_scale, const float* v_scale,
+                  void* o, float* lse, int B, int Hq, int Hkv, int N, int d, long long T, float scale,
+                  const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace fa_decode needs for B sequences, Hq query heads, head
  * dimension d and caches of at most max_seqlen_k tokens (an upper bound over
  * every split length the library picks).  Returns 0 for non-positive
