@@ -322,11 +322,11 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 //   warps 2-5  softmax warpgroup: thread = key row of S^T (TMEM lane) for the
 //              probabilities, and = dimension row of O^T for the rescale and
 //              the split's output.
-//   warps 6-9  (FP8 cache only) converter warpgroup: dequantises each E4M3
-//              K / V tile into a 16-bit tile in shared memory ("Attention 算子
-//              优化…", section 六: the cache stays FP8 in HBM, dequantisation
-//              happens on chip, the products run in 16-bit, softmax and
-//              accumulation in f32).
+//   warps 6-9, 10-13  (FP8 cache only) converter warpgroups for K and for V:
+//              dequantise each E4M3 tile into a 16-bit tile in shared memory
+//              ("Attention 算子优化…", section 六: the cache stays FP8 in HBM,
+//              dequantisation happens on chip, the products run in 16-bit,
+//              softmax and accumulation in f32).
 // S^T is double-buffered in TMEM, so S^T of tile i+1 runs while the softmax
 // works on tile i; P^T (16-bit, K-major: 16 head rows x 128 keys) is
 // double-buffered in shared memory.  The running max of a head only moves
@@ -350,10 +350,10 @@ struct DecTcLayout {
   static constexpr int kTile8Bytes = kTile * 128;      // E4M3 128 x 128 tile (one 128-byte row per key)
   // TMA stages: 16-bit K and V tiles, or E4M3 K and V tiles
   static constexpr int kStageBytes = FP8 ? 2 * kTile8Bytes : 2 * kTileBytes;
-  static constexpr int kStages = 3;
-  // FP8: dequantised K (two buffers, freed when S^T completes) and V (one
-  // buffer, freed when the previous P V completes)
-  static constexpr int kCvtBytes = FP8 ? 3 * kTileBytes : 0;
+  static constexpr int kStages = FP8 ? 2 : 3;
+  // FP8: dequantised K and V, two buffers each (K freed when S^T completes,
+  // V when P V completes)
+  static constexpr int kCvtBytes = FP8 ? 4 * kTileBytes : 0;
   static constexpr int kHChunkBytes = kDecHeads * 128;  // 16 rows x 64 16-bit elements
   static constexpr int kQBytes = 2 * kHChunkBytes;      // Q: 16 heads x 128 dims, K-major
   static constexpr int kPBytes = 2 * kHChunkBytes;      // P^T: 16 heads x 128 keys, K-major
@@ -362,11 +362,11 @@ struct DecTcLayout {
   static constexpr int kOffP = kOffQ + kQBytes;          // two buffers
   static constexpr int kOffRed = kOffP + 2 * kPBytes;    // f32 [4 warps][16 heads]
   static constexpr int kOffBar = kOffRed + 4 * kDecHeads * 4;
-  // full[], empty[], q_ready, s_full[2], p_ready[2], pv_done[2], drain, k_ready[2], v_ready
-  static constexpr int kNumBars = 2 * kStages + 11;
+  // full[], empty[], q_ready, s_full[2], p_ready[2], pv_done[2], drain, k_ready[2], v_ready[2]
+  static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
-  static constexpr int kThreads = FP8 ? 320 : 192;
+  static constexpr int kThreads = FP8 ? 448 : 192;
   static constexpr uint32_t kTmemCols = 64;
   static constexpr uint32_t kColS = 0, kColO = 32;  // S^T buffers at 0 and 16
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
@@ -437,7 +437,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint64_t* pv_done = p_ready + 2;  // FP8: also frees dequantised buffer i & 1
   uint64_t* drain = pv_done + 2;
   uint64_t* k_ready = drain + 1;     // FP8 only: dequantised K of tile i in buffer i & 1
-  uint64_t* v_ready = k_ready + 2;   // FP8 only: dequantised V of the next tile
+  uint64_t* v_ready = k_ready + 2;   // FP8 only: dequantised V of tile i in buffer i & 1
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
   auto stage = [&](int st) { return smem + st * Lay::kStageBytes; };
@@ -445,14 +445,14 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   // 16-bit K and V tiles the MMAs of tile i read
   auto k16 = [&](int i) { return FP8 ? smem + Lay::kOffCvt + (i & 1) * Lay::kTileBytes : stage(i % NS); };
   auto v16 = [&](int i) {
-    return FP8 ? smem + Lay::kOffCvt + 2 * Lay::kTileBytes : stage(i % NS) + Lay::kTileBytes;
+    return FP8 ? smem + Lay::kOffCvt + (2 + (i & 1)) * Lay::kTileBytes : stage(i % NS) + Lay::kTileBytes;
   };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full + i, 1);
-      mbar_init(empty + i, FP8 ? 128 : 1);  // FP8: released by the converters
+      mbar_init(empty + i, FP8 ? 256 : 1);  // FP8: released by both converter warpgroups
     }
     mbar_init(q_ready, 128);
     for (int i = 0; i < 2; ++i) {
@@ -460,8 +460,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       mbar_init(p_ready + i, 128);
       mbar_init(pv_done + i, 1);
       mbar_init(k_ready + i, 128);
+      mbar_init(v_ready + i, 128);
     }
-    mbar_init(v_ready, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -531,7 +531,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       for (int i = 0; i < nt && ok; ++i) {
         // P^T of tile i written, S^T buffer i & 1 read, O^T rescaled
         if (!(ok = mbar_wait(p_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
-        if (FP8 && !(ok = mbar_wait(v_ready, i & 1, abort_flag))) break;
+        if (FP8 && !(ok = mbar_wait(v_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t sVa = smem_u32(v16(i)), sPa = smem_u32(pbuf(i));
 #pragma unroll
@@ -713,17 +713,26 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
     }
   } else if constexpr (FP8) {
-    // ------------------------------------------------------------ converter warpgroup
-    // Thread r dequantises key row r of the tile's K and V: 8 units of 16
-    // E4M3 codes each, into 16 f16 units of the 128-byte-swizzled 16-bit
-    // tiles the MMAs read.  The per-token scales are applied elsewhere.  K of
-    // tile i goes to buffer i & 1 once S^T of tile i - 2 is done with it; V to
-    // the single V buffer once P V of tile i - 1 is done; then the E4M3 stage
-    // is released, so the loads run ahead of the products.
-    const int r = (warp - 6) * 32 + lane;
-    auto convert = [&](const uint8_t* src_tile, uint8_t* dst_tile) {
-      const uint8_t* src = src_tile + r * 128;
-      uint8_t* dst = dst_tile + r * 128;
+    // ------------------------------------------------------------ converter warpgroups
+    // Thread r dequantises key row r of the tile's K (warps 6-9) or V (warps
+    // 10-13): 8 units of 16 E4M3 codes each, into 16 f16 units of the
+    // 128-byte-swizzled 16-bit tiles the MMAs read.  The per-token scales are
+    // applied elsewhere.  K and V of tile i go to buffers i & 1 once S^T and
+    // P V of tile i - 2 are done with them.  The E4M3 stage is released when
+    // both halves are converted, so the loads run ahead of the products.
+    const bool is_v = warp >= 10;
+    const int r = (warp - (is_v ? 10 : 6)) * 32 + lane;
+    bool ok = true;
+    for (int i = 0; i < nt && ok; ++i) {
+      const int st = i % NS;
+      if (!(ok = mbar_wait(full + st, (i / NS) & 1, abort_flag))) break;
+      if (!is_v) {
+        if (i >= 2 && !(ok = mbar_wait(s_full + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) break;
+      } else if (i >= 2 && !(ok = mbar_wait(pv_done + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) {
+        break;
+      }
+      const uint8_t* src = stage(st) + (is_v ? Lay::kTile8Bytes : 0) + r * 128;
+      uint8_t* dst = (is_v ? v16(i) : k16(i)) + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint4 e = *reinterpret_cast<const uint4*>(src + ((u ^ (r & 7)) << 4));  // dims 16u .. 16u+15
@@ -740,18 +749,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         *reinterpret_cast<uint4*>(chunk + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
       }
       fence_proxy_async_smem();
-    };
-    bool ok = true;
-    for (int i = 0; i < nt && ok; ++i) {
-      const int st = i % NS;
-      if (!(ok = mbar_wait(full + st, (i / NS) & 1, abort_flag))) break;
-      if (i >= 2 && !(ok = mbar_wait(s_full + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) break;
-      convert(stage(st), k16(i));
-      mbar_arrive(k_ready + (i & 1));
-      if (i >= 1 && !(ok = mbar_wait(pv_done + ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag))) break;
-      convert(stage(st) + Lay::kTile8Bytes, v16(i));
-      mbar_arrive(v_ready);
-      mbar_arrive(empty + st);  // the E4M3 stage has been read
+      mbar_arrive((is_v ? v_ready : k_ready) + (i & 1));
+      mbar_arrive(empty + st);  // this half of the E4M3 stage has been read
     }
     if (!ok) give_up();
   }
