@@ -7,6 +7,7 @@ for the FP8 (E4M3) K/V cache, ``oracle/quant.py``.
 from .attention import (  # noqa: F401
     attention_backward,
     attention_decode,
+    attention_decode_paged,
     attention_forward,
     attention_forward_rows,
     cu_from_lengths,

@@ -46,6 +46,12 @@ notes):
   O = 0 and LSE = -inf.
 * In a decoding step the new query is the newest token of its sequence and its
   own K/V row is already in the cache, so it sees every cached key: no mask.
+* Paged K/V cache ("Attention 算子优化…", section 五, PagedAttention): the cache
+  is a pool of fixed-size pages ``[num_pages, page_size, Hkv, d]``; sequence b
+  owns logical pages 0, 1, ... whose physical pages are
+  ``block_table[b, 0], block_table[b, 1], ...``, and its first ``seqlens[b]``
+  logical tokens are its cache.  Table entries past the cache and page
+  contents past it are not read.
 * Layout: tokens-major ``[T, H, d]`` for q/k/v/o and their gradients, ``[Hq, T]``
   for the LSE; sequence s covers tokens ``cu_seqlens[s] .. cu_seqlens[s+1]-1``.
 
@@ -64,6 +70,7 @@ import numpy as np
 
 __all__ = [
     "attention_decode",
+    "attention_decode_paged",
     "attention_forward",
     "attention_forward_rows",
     "attention_backward",
@@ -215,6 +222,34 @@ def attention_decode(q, k, v, cu_seqlens_k, scale):
             o[b, h, :] = (P @ v[a:e, kv, :])[0]
             lse[h, b] = lse_row[0]
     return o, lse
+
+
+def attention_decode_paged(q, k_pages, v_pages, block_table, seqlens, scale):
+    """One decoding step over a paged K/V cache (fp64).
+
+    q: [B, Hq, d]; k_pages, v_pages: [num_pages, page_size, Hkv, d];
+    block_table: [B, max_pages] physical page of each logical page; seqlens:
+    [B] cache lengths.  Gathers each sequence's pages in logical order into a
+    packed cache and evaluates :func:`attention_decode` on it.
+    """
+    k_pages = np.asarray(k_pages, dtype=np.float64)
+    v_pages = np.asarray(v_pages, dtype=np.float64)
+    table = np.asarray(block_table, dtype=np.int64)
+    lens = np.asarray(seqlens, dtype=np.int64)
+    page = k_pages.shape[1]
+    ks, vs = [], []
+    for b in range(len(lens)):
+        L = int(lens[b])
+        n = (L + page - 1) // page
+        if n > table.shape[1]:
+            raise ValueError("block table too short for the cache length")
+        rows_k = np.concatenate([k_pages[table[b, j]] for j in range(n)], axis=0)[:L] if n else k_pages[:0, 0]
+        rows_v = np.concatenate([v_pages[table[b, j]] for j in range(n)], axis=0)[:L] if n else v_pages[:0, 0]
+        ks.append(rows_k)
+        vs.append(rows_v)
+    k = np.concatenate(ks, axis=0)
+    v = np.concatenate(vs, axis=0)
+    return attention_decode(q, k, v, cu_from_lengths(lens), scale)
 
 
 def attention_backward(q, k, v, do, cu_seqlens, scale, causal, return_rowsum=False):

@@ -481,3 +481,64 @@ def test_row_quantisation_scale_rule_and_error_bound():
     # half a quantum: 2^-4 relative in the normal range, 2^-10 s below it
     err = np.abs(deq - x)
     assert (err <= 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * s[..., None] * (1 + 1e-6)).all()
+
+
+# ---------------------------------------------------------------- paged K/V cache
+
+def _paged_case(lengths, page, Hkv=2, d=8, seed=30, shuffle=True):
+    """A packed cache cut into pages, placed at random physical pages of a
+    pool that also holds garbage pages; returns (packed k, v, cu, pages, table)."""
+    r = np.random.default_rng(seed)
+    cu = oracle.cu_from_lengths(lengths)
+    T = int(cu[-1])
+    k = r.standard_normal((T, Hkv, d))
+    v = r.standard_normal((T, Hkv, d))
+    npg = [(L + page - 1) // page for L in lengths]
+    total = sum(npg) + 5
+    phys = r.permutation(total) if shuffle else np.arange(total)
+    kp = r.standard_normal((total, page, Hkv, d)) * 100  # garbage everywhere first
+    vp = r.standard_normal((total, page, Hkv, d)) * 100
+    table = np.full((len(lengths), max(npg + [1]) + 2), -7, dtype=np.int64)  # unused entries: junk
+    nxt = 0
+    for b, L in enumerate(lengths):
+        for j in range(npg[b]):
+            pg = phys[nxt]
+            nxt += 1
+            table[b, j] = pg
+            a, e = cu[b] + j * page, min(cu[b] + (j + 1) * page, cu[b + 1])
+            kp[pg, :e - a] = k[a:e]
+            vp[pg, :e - a] = v[a:e]
+    return k, v, cu, kp, vp, table
+
+
+@pytest.mark.parametrize("page", [1, 4, 16])
+def test_paged_decode_equals_packed_decode(page):
+    """Any page size, any placement of the pages in the pool and junk in the
+    unused table entries and page tails give the packed cache's result."""
+    lengths = [37, 0, 16, 5, 64]
+    k, v, cu, kp, vp, table = _paged_case(lengths, page)
+    q = np.random.default_rng(31).standard_normal((5, 4, 8))
+    o_ref, l_ref = DEC(q, k, v, cu, 0.35)
+    o, l = oracle.attention_decode_paged(q, kp, vp, table, lengths, 0.35)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(l, l_ref)
+
+
+def test_paged_decode_reads_the_right_pages():
+    """Attention over a cache is invariant under permuting its keys, so a
+    swap of two full pages changes nothing; swapping the partly filled last
+    page with a full one makes the gather read other rows (garbage past the
+    cache) and changes that sequence's result, and only that one."""
+    lengths = [44, 40]  # page 8: sequence 0 has 6 pages, the last with 4 rows
+    k, v, cu, kp, vp, table = _paged_case(lengths, 8, seed=32)
+    q = np.random.default_rng(33).standard_normal((2, 2, 8))
+    o1, _ = oracle.attention_decode_paged(q, kp, vp, table, lengths, 0.5)
+    t_full = table.copy()
+    t_full[0, [0, 3]] = t_full[0, [3, 0]]
+    o2, _ = oracle.attention_decode_paged(q, kp, vp, t_full, lengths, 0.5)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
+    t_tail = table.copy()
+    t_tail[0, [0, 5]] = t_tail[0, [5, 0]]
+    o3, _ = oracle.attention_decode_paged(q, kp, vp, t_tail, lengths, 0.5)
+    assert np.abs(o1[0] - o3[0]).max() > 1e-3
+    np.testing.assert_array_equal(o1[1], o3[1])
