@@ -321,6 +321,10 @@ def bench_decode(args, world, rank, local):
     lse = torch.empty(Hq, B, dtype=torch.float32, device=dev)
     ws = torch.empty(fa.fa_decode_workspace_size(B, Hq, d, N), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    if w.page_size:
+        # the cache lives in pages scattered over a pool, reached through the table
+        k, v = host["k_pages"].to(dev), host["v_pages"].to(dev)
+        table, seqlens = host["block_table"].to(dev), host["seqlens"].to(dev)
     if w.fp8:
         # the cache is quantised when it is written, before the decoding steps
         k8, ks = fa.kv_quantize_fp8(k)
@@ -328,7 +332,11 @@ def bench_decode(args, world, rank, local):
         del k, v
 
     def step():
-        if w.fp8:
+        if w.page_size and w.fp8:
+            fa.fa_decode_paged_fp8(q, k8, v8, ks, vs, table, seqlens, o, lse, w.page_size, w.scale, ws, stream)
+        elif w.page_size:
+            fa.fa_decode_paged(q, k, v, table, seqlens, o, lse, w.page_size, w.scale, ws, stream)
+        elif w.fp8:
             fa.fa_decode_fp8(q, k8, v8, ks, vs, o, lse, B, Hq, Hkv, N, d, T, w.scale, cu, ws, stream)
         else:
             fa.fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, w.scale, cu, ws, stream)
@@ -411,13 +419,15 @@ def bench_decode(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                    "seq_lengths": w.seq_lengths if w.varlen else None, "queries_per_sequence": 1,
-                   "kv_cache": "E4M3 codes + f32 per-token scales" if w.fp8 else "bf16",
+                   "kv_cache": ("E4M3 codes + f32 per-token scales" if w.fp8 else "bf16")
+                   + (f", pages of {w.page_size} tokens at random pool positions" if w.page_size else ""),
                    "kv_cache_bytes": w.kv_cache_bytes(), "bytes_per_step": nbytes,
                    "gflop_per_step": round(w.decode_flops() / 1e9, 3),
                    "tokens_per_s": round(B * world / (avg_ms * 1e-3), 1),
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": ("fa_decode_fp8" if w.fp8 else "fa_decode") + " (split kernel + combine)",
+        "roofline": {"bound": "hbm", "kernel": "fa_decode" + ("_paged" if w.page_size else "") + ("_fp8" if w.fp8 else "")
+                     + " (split kernel + combine)",
                      "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None},

@@ -99,12 +99,12 @@ int device_state(DeviceState** out) {
 // [T, H, d] bf16 viewed as a 3-D tensor (d, H, T); box = 64 columns x 1 head
 // x 128 tokens with the 128-byte swizzle, which is the K-major SW128 operand
 // layout the MMAs read.  Rows past T read as zeros.
-int make_map(CUtensorMap* map, const void* base, long long T, int H, int d, const char* what) {
+int make_map(CUtensorMap* map, const void* base, long long T, int H, int d, const char* what, int box_rows = fa::kTile) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(fa::kTile)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -116,12 +116,13 @@ int make_map(CUtensorMap* map, const void* base, long long T, int H, int d, cons
 // E4M3 [T, H, d] (one byte per element) viewed as (d, H, T); box = 128 columns
 // (one 128-byte row) x 1 head x 128 tokens with the 128-byte swizzle.  Rows
 // past T read as zeros.
-int make_map_u8(CUtensorMap* map, const void* base, long long T, int H, int d, const char* what) {
+int make_map_u8(CUtensorMap* map, const void* base, long long T, int H, int d, const char* what,
+                int box_rows = fa::kTile) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(FA_ERR_LAUNCH, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H) * d};
-  cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(fa::kTile)};
+  cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -306,13 +307,32 @@ size_t fa_decode_workspace_size(int B, int Hq, int d, int max_seqlen_k) {
   return up(rows * d * 4) + up(rows * 4);
 }
 
-// Shared by fa_decode and fa_decode_fp8 (k_scale == nullptr: bf16 cache).
+// Page table of a paged cache (block_table == nullptr: packed or batched cache).
+struct Paging {
+  const int* block_table = nullptr;
+  const int* seqlens = nullptr;
+  int page_size = 0, num_pages = 0, max_pages = 0;
+};
+
+// Shared by the four decoding entry points (k_scale == nullptr: bf16 cache).
 static int decode_common(const void* q, const void* k, const void* v, const float* k_scale, const float* v_scale,
                          void* o, float* lse, int B, int Hq, int Hkv, int N, int d, long long T, float scale,
-                         const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
+                         const int* cu_seqlens_k, const Paging& pg, void* workspace, size_t workspace_bytes,
+                         void* stream) {
   const bool fp8 = k_scale != nullptr;
+  const bool paged = pg.block_table != nullptr;
+  if (paged) {
+    if (pg.page_size != 8 && pg.page_size != 16 && pg.page_size != 32 && pg.page_size != 64 && pg.page_size != 128)
+      return fail(FA_ERR_INVALID_ARG, "page_size must be 8, 16, 32, 64 or 128 (got %d)", pg.page_size);
+    if (pg.num_pages < 1 || pg.max_pages < 1) return fail(FA_ERR_INVALID_ARG, "num_pages and max_pages must be >= 1");
+    if (static_cast<long long>(pg.max_pages) * pg.page_size > (1ll << 30) ||
+        static_cast<long long>(pg.num_pages) * pg.page_size > (1ll << 31) - 1)
+      return fail(FA_ERR_INVALID_ARG, "page pool or page table too large");
+    if (!pg.seqlens || !aligned(pg.block_table, 4) || !aligned(pg.seqlens, 4))
+      return fail(FA_ERR_INVALID_ARG, "block_table and seqlens must be non-null and 4-byte aligned");
+  }
   Shape s;
-  int rc = check_shape(B, Hq, Hkv, N, d, T, scale, 0, cu_seqlens_k, &s);
+  int rc = check_shape(B, Hq, Hkv, N, d, T, scale, 0, paged ? pg.seqlens : cu_seqlens_k, &s);
   if (rc) return rc;
   if (Hq / Hkv > 16) return fail(FA_ERR_UNSUPPORTED, "decode supports up to 16 query heads per K/V head");
   if (fp8 && d != 128) return fail(FA_ERR_UNSUPPORTED, "the E4M3 cache is supported for d = 128");
@@ -328,9 +348,10 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   DeviceState* dev = nullptr;
   if ((rc = device_state(&dev))) return rc;
   CUtensorMap tk, tv;
+  const int box = paged ? pg.page_size : fa::kTile;
   if (fp8) {
-    if ((rc = make_map_u8(&tk, k, T, Hkv, d, "k")) || (rc = make_map_u8(&tv, v, T, Hkv, d, "v"))) return rc;
-  } else if ((rc = make_map(&tk, k, T, Hkv, d, "k")) || (rc = make_map(&tv, v, T, Hkv, d, "v"))) {
+    if ((rc = make_map_u8(&tk, k, T, Hkv, d, "k", box)) || (rc = make_map_u8(&tv, v, T, Hkv, d, "v", box))) return rc;
+  } else if ((rc = make_map(&tk, k, T, Hkv, d, "k", box)) || (rc = make_map(&tv, v, T, Hkv, d, "v", box))) {
     return rc;
   }
   fa::DecodeParams p{};
@@ -340,6 +361,11 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   p.cu = cu_seqlens_k;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.block_table = pg.block_table;
+  p.seqlens = pg.seqlens;
+  p.page_size = pg.page_size;
+  p.max_pages = pg.max_pages;
+  p.num_pages = pg.num_pages;
   p.status = dev->status;
   p.T = T;
   p.B = B;
@@ -347,7 +373,7 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   p.Hkv = Hkv;
   p.N = N;
   p.group = Hq / Hkv;
-  p.split_tiles = decode_split_tiles(B, Hkv, s.n_tiles, T, cu_seqlens_k != nullptr, dev->sms);
+  p.split_tiles = decode_split_tiles(B, Hkv, s.n_tiles, T, !paged && cu_seqlens_k != nullptr, dev->sms);
   p.n_splits = (s.n_tiles + p.split_tiles - 1) / p.split_tiles;
   const size_t rows = static_cast<size_t>(B) * Hq * p.n_splits;
   p.o_part = static_cast<float*>(workspace);
@@ -364,8 +390,8 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
               int d, long long T, float scale, const int* cu_seqlens_k, void* workspace, size_t workspace_bytes,
               void* stream) {
   g_err[0] = '\0';
-  return decode_common(q, k, v, nullptr, nullptr, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace,
-                       workspace_bytes, stream);
+  return decode_common(q, k, v, nullptr, nullptr, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, Paging{},
+                       workspace, workspace_bytes, stream);
 }
 
 int fa_decode_fp8(const void* q, const void* k8, const void* v8, const float* k_scale, const float* v_scale,
@@ -373,8 +399,38 @@ int fa_decode_fp8(const void* q, const void* k8, const void* v8, const float* k_
                   const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
   g_err[0] = '\0';
   if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "null scale pointer");
-  return decode_common(q, k8, v8, k_scale, v_scale, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, workspace,
-                       workspace_bytes, stream);
+  return decode_common(q, k8, v8, k_scale, v_scale, o, lse, B, Hq, Hkv, N, d, T, scale, cu_seqlens_k, Paging{},
+                       workspace, workspace_bytes, stream);
+}
+
+int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                    const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv, int d, int page_size,
+                    int num_pages, int max_pages, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!block_table) return fail(FA_ERR_INVALID_ARG, "null block_table");
+  if (page_size < 1 || max_pages < 1 || num_pages < 1 || static_cast<long long>(max_pages) * page_size > (1ll << 30) ||
+      static_cast<long long>(num_pages) * page_size > (1ll << 31) - 1)
+    return fail(FA_ERR_INVALID_ARG, "page_size, num_pages and max_pages must be >= 1 and the pool below 2^31 rows");
+  Paging pg{block_table, seqlens, page_size, num_pages, max_pages};
+  const long long rows = static_cast<long long>(num_pages) * page_size;
+  return decode_common(q, k_pages, v_pages, nullptr, nullptr, o, lse, B, Hq, Hkv, max_pages * page_size, d, rows,
+                       scale, nullptr, pg, workspace, workspace_bytes, stream);
+}
+
+int fa_decode_paged_fp8(const void* q, const void* k8_pages, const void* v8_pages, const float* k_scale,
+                        const float* v_scale, const int* block_table, const int* seqlens, void* o, float* lse, int B,
+                        int Hq, int Hkv, int d, int page_size, int num_pages, int max_pages, float scale,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!block_table) return fail(FA_ERR_INVALID_ARG, "null block_table");
+  if (!k_scale || !v_scale) return fail(FA_ERR_INVALID_ARG, "null scale pointer");
+  if (page_size < 1 || max_pages < 1 || num_pages < 1 || static_cast<long long>(max_pages) * page_size > (1ll << 30) ||
+      static_cast<long long>(num_pages) * page_size > (1ll << 31) - 1)
+    return fail(FA_ERR_INVALID_ARG, "page_size, num_pages and max_pages must be >= 1 and the pool below 2^31 rows");
+  Paging pg{block_table, seqlens, page_size, num_pages, max_pages};
+  const long long rows = static_cast<long long>(num_pages) * page_size;
+  return decode_common(q, k8_pages, v8_pages, k_scale, v_scale, o, lse, B, Hq, Hkv, max_pages * page_size, d, rows,
+                       scale, nullptr, pg, workspace, workspace_bytes, stream);
 }
 
 int fa_kv_quantize_fp8(const void* x, void* x8, float* scale, long long rows, int d, void* stream) {

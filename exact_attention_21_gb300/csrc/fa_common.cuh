@@ -86,6 +86,9 @@ struct DecodeParams {
   const int* cu;      // device int32 [B + 1] offsets into the K/V cache, or null
   const float* k_scale;  // E4M3 cache only: f32 [T, Hkv] per-token scales
   const float* v_scale;
+  const int* block_table;  // paged cache only: device int32 [B, max_pages], else null
+  const int* seqlens;      // paged cache only: device int32 [B]
+  int page_size, max_pages, num_pages;
   unsigned* status;
   long long T;        // cached tokens in all
   int B, Hq, Hkv, N, group;

@@ -71,6 +71,94 @@ __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
+// ---------------------------------------------------------------------------
+// Where a sequence's cache lives.  Packed or batched caches: rows seq0 ..
+// seq0 + L - 1 of the [T, Hkv, d] cache.  Paged caches ("Attention 算子优化…",
+// section 五, PagedAttention): a pool of pages of page_size rows; logical key
+// j of sequence b is row  block_table[b][j / page_size] * page_size +
+// j % page_size  of the pool, and L = seqlens[b].
+
+// Cache length (and start row, unpaged) of sequence b; false (and a status
+// bit) when the offsets or the length are out of range.
+__device__ __forceinline__ bool decode_bounds(const DecodeParams& p, int b, long long& seq0, int& L) {
+  if (p.block_table == nullptr) return sequence_bounds(p.cu, b, p.N, p.T, seq0, L, p.status);
+  const int l = __ldg(p.seqlens + b);
+  if (l < 0 || l > p.max_pages * p.page_size) {
+    atomicOr(p.status, kStatusBadOffsets);
+    return false;
+  }
+  seq0 = 0;
+  L = l;
+  return true;
+}
+
+// Physical page of logical page lp of sequence b.  Pages past the cache may
+// hold anything (their keys are masked), so page 0 is read for them; a table
+// entry inside the cache that is out of range sets a status bit and is
+// replaced by page 0 as well.
+__device__ __forceinline__ int decode_page(const DecodeParams& p, int b, int lp, int L) {
+  const bool live = lp * p.page_size < L;
+  int phys = live ? __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + lp) : 0;
+  if (phys < 0 || phys >= p.num_pages) {
+    atomicOr(p.status, kStatusBadOffsets);
+    phys = 0;
+  }
+  return phys;
+}
+
+// Cache row of logical key kpos (kpos < L) of sequence b.
+__device__ __forceinline__ long long decode_row(const DecodeParams& p, int b, long long seq0, int kpos, int L) {
+  if (p.block_table == nullptr) return seq0 + kpos;
+  return static_cast<long long>(decode_page(p, b, kpos / p.page_size, L)) * p.page_size + kpos % p.page_size;
+}
+
+// TMA loads of the K and V tile of logical keys k0 .. k0 + 127 of sequence b
+// (K/V head g): CHUNKS boxes of 64 (16-bit) or 128 (8-bit) columns per tile,
+// each CHUNK_BYTES apart in shared memory; paged caches take one box of
+// page_size rows per page (1 KB-aligned in shared memory for page_size >= 8,
+// so the 128-byte swizzle pattern continues across boxes).
+template <int CHUNKS, int CHUNK_BYTES, int COLS>
+__device__ __forceinline__ void load_kv_tile(const DecodeParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                             uint8_t* dst_k, uint8_t* dst_v, uint64_t* bar, int b, int g,
+                                             long long seq0, int k0, int L) {
+  if (p.block_table == nullptr) {
+    const int row = static_cast<int>(seq0 + k0);
+    for (int c = 0; c < CHUNKS; ++c) {
+      tma_load_3d(dst_k + c * CHUNK_BYTES, tm_k, bar, c * COLS, g, row);
+      tma_load_3d(dst_v + c * CHUNK_BYTES, tm_v, bar, c * COLS, g, row);
+    }
+    return;
+  }
+  // the tile's table entries are read together first: the copies below are
+  // ordered memory operations, and reading each entry right before its copy
+  // would pay one load latency per page
+  const int ps = p.page_size;
+  const int np = kTile / ps;
+  const int* entries = p.block_table + static_cast<long long>(b) * p.max_pages + k0 / ps;
+  int phys[kTile / 8];
+#pragma unroll
+  for (int j = 0; j < kTile / 8; ++j)  // plain loads only, so they can all be in flight at once
+    phys[j] = (j < np && (k0 / ps + j) * ps < L) ? __ldg(entries + j) : 0;
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < kTile / 8; ++j) {
+    const bool out = phys[j] < 0 || phys[j] >= p.num_pages;  // see decode_page
+    bad |= out;
+    phys[j] = out ? 0 : phys[j];
+  }
+  if (bad) atomicOr(p.status, kStatusBadOffsets);
+#pragma unroll
+  for (int j = 0; j < kTile / 8; ++j) {
+    if (j < np) {
+      const int row = phys[j] * ps;
+      for (int c = 0; c < CHUNKS; ++c) {
+        tma_load_3d(dst_k + c * CHUNK_BYTES + j * ps * 128, tm_k, bar, c * COLS, g, row);
+        tma_load_3d(dst_v + c * CHUNK_BYTES + j * ps * 128, tm_v, bar, c * COLS, g, row);
+      }
+    }
+  }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(288, 1)
 fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -82,7 +170,7 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   long long seq0;
   int L;
-  if (!sequence_bounds(p.cu, b, p.N, p.T, seq0, L, p.status)) return;
+  if (!decode_bounds(p, b, seq0, L)) return;
   const int seq_tiles = (L + kTile - 1) / kTile;
   const int t0 = split * p.split_tiles;
   if (t0 >= seq_tiles) return;  // past the end of this sequence's cache: the combine skips it
@@ -121,11 +209,8 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
         const int st = i % NS;
         if (i >= NS && !(ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag))) break;
         mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
-        const int row = static_cast<int>(seq0 + static_cast<long long>(t0 + i) * kTile);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(stage(st) + c * Lay::kChunkBytes, &tm_k, full + st, c * 64, g, row);
-          tma_load_3d(stage(st) + Lay::kTileBytes + c * Lay::kChunkBytes, &tm_v, full + st, c * 64, g, row);
-        }
+        load_kv_tile<D / 64, Lay::kChunkBytes, 64>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTileBytes, full + st,
+                                                   b, g, seq0, (t0 + i) * kTile, L);
         ++issued;
       }
       if (!ok) give_up();
@@ -418,7 +503,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   long long seq0;
   int L;
-  if (!sequence_bounds(p.cu, b, p.N, p.T, seq0, L, p.status)) return;
+  if (!decode_bounds(p, b, seq0, L)) return;
   const int seq_tiles = (L + kTile - 1) / kTile;
   const int t0 = split * p.split_tiles;
   if (t0 >= seq_tiles) return;  // past the end of this sequence's cache: the combine skips it
@@ -490,15 +575,12 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const int st = i % NS;
         if (i >= NS && !(ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag))) break;
         mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
-        const int row = static_cast<int>(seq0 + static_cast<long long>(t0 + i) * kTile);
         if constexpr (FP8) {
-          tma_load_3d(stage(st), &tm_k, full + st, 0, g, row);
-          tma_load_3d(stage(st) + Lay::kTile8Bytes, &tm_v, full + st, 0, g, row);
+          load_kv_tile<1, Lay::kTile8Bytes, 128>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTile8Bytes, full + st, b,
+                                                  g, seq0, (t0 + i) * kTile, L);
         } else {
-          for (int c = 0; c < 2; ++c) {
-            tma_load_3d(stage(st) + c * Lay::kChunkBytes, &tm_k, full + st, c * 64, g, row);
-            tma_load_3d(stage(st) + Lay::kTileBytes + c * Lay::kChunkBytes, &tm_v, full + st, c * 64, g, row);
-          }
+          load_kv_tile<2, Lay::kChunkBytes, 64>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTileBytes, full + st, b,
+                                                 g, seq0, (t0 + i) * kTile, L);
         }
         ++issued;
       }
@@ -593,7 +675,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       float sk = 1.f, sv = 1.f;  // per-token scales of this key (FP8 cache)
       if constexpr (FP8) {
         if (valid) {
-          const long long si = (seq0 + kpos) * p.Hkv + g;
+          const long long si = decode_row(p, b, seq0, kpos, L) * p.Hkv + g;
           sk = __ldg(p.k_scale + si);
           sv = __ldg(p.v_scale + si);
         }
@@ -772,7 +854,10 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
   if (row >= static_cast<long long>(p.B) * p.Hq) return;
   const int b = static_cast<int>(row / p.Hq), h = static_cast<int>(row % p.Hq);
   int L = p.N;
-  if (p.cu != nullptr) {
+  if (p.block_table != nullptr) {
+    const int l = __ldg(p.seqlens + b);
+    L = (l >= 0 && l <= p.max_pages * p.page_size) ? l : 0;  // bad lengths: reported by the split kernel
+  } else if (p.cu != nullptr) {
     const int a = __ldg(p.cu + b), e = __ldg(p.cu + b + 1);
     L = (a >= 0 && e >= a && e <= p.T && e - a <= p.N) ? e - a : 0;  // bad offsets: reported by the split kernel
   }

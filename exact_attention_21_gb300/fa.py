@@ -24,8 +24,8 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_UNSUPPORTED = 5
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
-           "fa_decode_workspace_size", "fa_kv_quantize_fp8", "fa_tile_counts", "fa_stream_status",
-           "fa_last_error_string")
+           "fa_decode_paged", "fa_decode_paged_fp8", "fa_decode_workspace_size", "fa_kv_quantize_fp8",
+           "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
 
 
 class FAError(RuntimeError):
@@ -60,6 +60,12 @@ def lib():
         L.fa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, vp, vp,
                                     ctypes.c_size_t, vp]
         L.fa_decode_fp8.restype = i32
+        L.fa_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp,
+                                      ctypes.c_size_t, vp]
+        L.fa_decode_paged.restype = i32
+        L.fa_decode_paged_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                          vp, ctypes.c_size_t, vp]
+        L.fa_decode_paged_fp8.restype = i32
         L.fa_kv_quantize_fp8.argtypes = [vp, vp, vp, i64, i32, vp]
         L.fa_kv_quantize_fp8.restype = i32
         L.fa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
@@ -134,6 +140,46 @@ def fa_decode_fp8(q, k8, v8, k_scale, v_scale, o, lse, B, Hq, Hkv, N, d, T, scal
     _check(lib().fa_decode_fp8(_ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), _ptr(o), _ptr(lse), B, Hq,
                                Hkv, N, d, T, float(scale), _ptr(cu_seqlens_k), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, page_size, scale, workspace, stream=None):
+    """One decoding step over a paged cache: pools [num_pages * page_size, Hkv, d], table [B, max_pages]."""
+    B, Hq, d = q.shape
+    Hkv = k_pages.shape[1]
+    _check(lib().fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens), _ptr(o),
+                                 _ptr(lse), B, Hq, Hkv, d, page_size, k_pages.shape[0] // page_size,
+                                 block_table.shape[1], float(scale), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_decode_paged_fp8(q, k8_pages, v8_pages, k_scale, v_scale, block_table, seqlens, o, lse, page_size, scale,
+                        workspace, stream=None):
+    """:func:`fa_decode_paged` over an E4M3 pool with per-token scales [num_pages * page_size, Hkv]."""
+    B, Hq, d = q.shape
+    Hkv = k8_pages.shape[1]
+    _check(lib().fa_decode_paged_fp8(_ptr(q), _ptr(k8_pages), _ptr(v8_pages), _ptr(k_scale), _ptr(v_scale),
+                                     _ptr(block_table), _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, page_size,
+                                     k8_pages.shape[0] // page_size, block_table.shape[1], float(scale),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def attention_decode_paged(q, k_pages, v_pages, block_table, seqlens, page_size, scale=None, k_scale=None,
+                           v_scale=None, stream=None):
+    """Allocates o, lse and the workspace and runs a decoding step over a paged
+    cache (bf16 pools, or E4M3 pools when k_scale and v_scale are given)."""
+    B, Hq, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    ws = torch.empty(fa_decode_workspace_size(B, Hq, d, block_table.shape[1] * page_size), dtype=torch.uint8,
+                     device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, B, dtype=torch.float32, device=q.device)
+    if k_scale is None:
+        fa_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, page_size, scale, ws, stream)
+    else:
+        fa_decode_paged_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seqlens, o, lse, page_size, scale,
+                            ws, stream)
+    return o, lse
 
 
 def fa_kv_quantize_fp8(x, x8, scale, stream=None):

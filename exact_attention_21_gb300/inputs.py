@@ -24,7 +24,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_decode_qkv", "make_inputs", "make_qkv"]
+__all__ = ["Workload", "WORKLOADS", "make_decode_qkv", "make_inputs", "make_paged_cache", "make_qkv"]
 
 
 @dataclass(frozen=True)
@@ -40,6 +40,7 @@ class Workload:
     backward: bool = False
     decode: bool = False  # one new query per sequence against a K/V cache of the lengths above
     fp8: bool = False     # decoding over an E4M3 cache with per-token f32 scales
+    page_size: int = 0    # decoding over a paged cache with pages of this many tokens (0: packed)
 
     @property
     def seq_lengths(self) -> list:
@@ -106,6 +107,9 @@ WORKLOADS = {
     # the same step over an E4M3 cache (per-token scales)
     "decode_fp8_b64_hq64_hkv8_n4096_d128": Workload(
         "decode_fp8_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True, True),
+    # the same step with the cache in 16-token pages scattered over a pool
+    "decode_paged16_b64_hq64_hkv8_n4096_d128": Workload(
+        "decode_paged16_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True, False, 16),
     # the packed workload's sequences and heads, one new token each
     "decode_varlen8_hq32_hkv8_d128": Workload(
         "decode_varlen8_hq32_hkv8_d128", 8, 32, 8, max(VARLEN_LENGTHS), 128, False, VARLEN_LENGTHS, False,
@@ -149,12 +153,47 @@ def make_decode_qkv(B, Hq, T, Hkv, d, seed=0):
     return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
 
 
+def make_paged_cache(k, v, lengths, page_size, seed=0, spare_pages=3):
+    """Lays a packed cache k, v [T, Hkv, d] out as a page pool.
+
+    Each sequence's rows are cut into pages of ``page_size`` tokens, and the
+    pages (plus ``spare_pages`` unused ones) are placed at a seeded random
+    permutation of the pool's pages.  Unused pool rows are filled with seeded
+    noise.  Returns (k_pages, v_pages [num_pages * page_size, Hkv, d],
+    block_table int32 [B, max_pages] with -1 in unused entries)."""
+    g = torch.Generator().manual_seed(seed + 7919)
+    T, Hkv, d = k.shape
+    npg = [(int(L) + page_size - 1) // page_size for L in lengths]
+    total = sum(npg) + spare_pages
+    max_pages = max(npg + [1])
+    perm = torch.randperm(total, generator=g)
+    kp = torch.randn(total * page_size, Hkv, d, generator=g).to(k.dtype)
+    vp = torch.randn(total * page_size, Hkv, d, generator=g).to(v.dtype)
+    table = torch.full((len(lengths), max_pages), -1, dtype=torch.int32)
+    nxt, start = 0, 0
+    for b, L in enumerate(lengths):
+        L = int(L)
+        for j in range(npg[b]):
+            pg = int(perm[nxt])
+            nxt += 1
+            table[b, j] = pg
+            a, e = start + j * page_size, min(start + (j + 1) * page_size, start + L)
+            kp[pg * page_size:pg * page_size + e - a] = k[a:e]
+            vp[pg * page_size:pg * page_size + e - a] = v[a:e]
+        start += L
+    return kp, vp, table
+
+
 def make_inputs(w: Workload, seed=0, with_do=None):
     """Inputs of workload ``w`` on the CPU: q, k, v (, do) bf16 and cu_seqlens int32
     (decoding workloads: q [B,Hq,d], the K/V cache and its offsets)."""
     if w.decode:
         t = make_decode_qkv(w.B, w.Hq, w.T, w.Hkv, w.d, seed=seed)
         t["cu_seqlens"] = cu_seqlens_of(w.seq_lengths)
+        if w.page_size:
+            t["k_pages"], t["v_pages"], t["block_table"] = make_paged_cache(t["k"], t["v"], w.seq_lengths,
+                                                                           w.page_size, seed=seed)
+            t["seqlens"] = torch.tensor(w.seq_lengths, dtype=torch.int32)
         return t
     if with_do is None:
         with_do = w.backward

@@ -180,6 +180,39 @@ int fa_decode_fp8(const void* q, const void* k8, const void* v8, const float* k_
                   void* o, float* lse, int B, int Hq, int Hkv, int N, int d, long long T, float scale,
                   const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * One decoding step (as fa_decode) over a paged K/V cache ("Attention 算子优化…",
+ * section 五, PagedAttention): the cache is a pool of fixed-size pages and each
+ * sequence reaches its pages through a page table, so caches need not be
+ * contiguous.  Logical key j of sequence b is row
+ *     block_table[b * max_pages + j / page_size] * page_size + j % page_size
+ * of the pool.  Table entries past a sequence's cache are not read.
+ *
+ *   k_pages, v_pages  [num_pages * page_size, Hkv, d] bf16 page pool, 16-byte aligned (in)
+ *   block_table       device int32 [B, max_pages]: physical page of each logical page (in)
+ *   seqlens           device int32 [B]: cache length of each sequence, at most
+ *                     max_pages * page_size (in)
+ *   page_size         8, 16, 32, 64 or 128 tokens.
+ *   workspace         at least fa_decode_workspace_size(B, Hq, d, max_pages * page_size) bytes.
+ *   Other arguments as for fa_decode.  A length out of range, or a table
+ *   entry inside a cache that is not a page of the pool, is detected on the
+ *   device: that sequence's result is not valid and the next
+ *   fa_stream_status() reports FA_ERR_INVALID_ARG.
+ */
+int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                    const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv, int d, int page_size,
+                    int num_pages, int max_pages, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_decode_paged over an E4M3 page pool (codes from fa_kv_quantize_fp8 and
+ * f32 per-token scales k_scale, v_scale [num_pages * page_size, Hkv], laid
+ * out like the pool).  d must be 128.
+ */
+int fa_decode_paged_fp8(const void* q, const void* k8_pages, const void* v8_pages, const float* k_scale,
+                        const float* v_scale, const int* block_table, const int* seqlens, void* o, float* lse, int B,
+                        int Hq, int Hkv, int d, int page_size, int num_pages, int max_pages, float scale,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace fa_decode needs for B sequences, Hq query heads, head
  * dimension d and caches of at most max_seqlen_k tokens (an upper bound over
  * every split length the library picks).  Returns 0 for non-positive
