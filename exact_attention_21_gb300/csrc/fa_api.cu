@@ -18,7 +18,8 @@ namespace fa {
 int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                cudaStream_t stream);
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
+               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool deterministic,
+               cudaStream_t stream);
 int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream);
 int launch_decode_fp8(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                       cudaStream_t stream);
@@ -248,10 +249,11 @@ size_t fa_bwd_workspace_size(int Hq, long long T, int d) {
   return up(static_cast<size_t>(Hq) * T * 4) + up(static_cast<size_t>(T) * Hq * d * 4);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
-           void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
-           const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream) {
-  g_err[0] = '\0';
+// Shared by fa_bwd and fa_bwd_deterministic.
+static int bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                      long long T, float scale, int causal, const int* cu_seqlens, void* workspace,
+                      size_t workspace_bytes, bool deterministic, void* stream) {
   Shape s;
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, &s);
   if (rc) return rc;
@@ -294,7 +296,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   p.n_kvtiles = s.n_tiles;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  int e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream));
+  int e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, deterministic, static_cast<cudaStream_t>(stream));
   if (e == -1) return fail(FA_ERR_UNSUPPORTED, "backward kernel unavailable for d = %d", d);
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;
@@ -446,6 +448,23 @@ int fa_kv_quantize_fp8(const void* x, void* x8, float* scale, long long rows, in
   int e = fa::launch_quantize_fp8(d, x, x8, scale, rows, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "quantize launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
+           const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace,
+                    workspace_bytes, false, stream);
+}
+
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                         long long T, float scale, int causal, const int* cu_seqlens, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace,
+                    workspace_bytes, true, stream);
 }
 
 int fa_tile_counts(int B, const int* lengths, int causal, long long* out) {

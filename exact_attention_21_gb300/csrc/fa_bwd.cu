@@ -76,7 +76,9 @@ struct BwdLayout {
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
-template <int D>
+// DQ = false compiles the dQ product and the dQ warpgroup out (the
+// deterministic backward computes dQ in a separate kernel).
+template <int D, bool DQ>
 __global__ void __launch_bounds__(448, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -245,7 +247,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       auto issue_next = [&](int m) -> bool {
         if (!mbar_wait(qdo_full + m % NS, (m / NS) & 1, abort_flag)) return false;
         if (m >= 1 && !mbar_wait(dp_free, (m - 1) & 1, abort_flag)) return false;
-        if (m >= 2 && !mbar_wait(dq_free, (m - 2) & 1, abort_flag)) return false;
+        if (DQ && m >= 2 && !mbar_wait(dq_free, (m - 2) & 1, abort_flag)) return false;
         tc_fence_after();
         issue_sdp(m);
         return true;
@@ -274,13 +276,15 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           umma_ss(tmem + Lay::kColDK, sdesc_sw128(dsb + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
                   sdesc_sw128(sQa + kk * 2048, Lay::kChunkBytes, 1024), id_dk, (n > 0 || kk > 0));
         umma_commit(qdo_empty + st);
-        // dQ_n = dS K into the step region of n, whose dQ_{n-2} was read before
-        // S^T_n was issued  (A: the dS^T tile read query-major, MN-major; B: K, MN-major)
+        if constexpr (DQ) {
+          // dQ_n = dS K into the step region of n, whose dQ_{n-2} was read before
+          // S^T_n was issued  (A: the dS^T tile read query-major, MN-major; B: K, MN-major)
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
-                  sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
-        umma_commit(dq_full);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
+                    sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
+          umma_commit(dq_full);
+        }
         if (n + 2 < nsteps && !(ok = issue_next(n + 2))) break;
       }
       if (ok) umma_commit(epi);
@@ -381,7 +385,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
     }
-  } else {
+  } else if (DQ) {
     // ------------------------------------------------------------ dQ warpgroup
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
@@ -483,11 +487,16 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdParams p, long 
 }
 
 int launch_bwd128_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream);
+                       const CUtensorMap& tdq, const BwdParams& p, bool dq, cudaStream_t stream);
+int launch_bwd_dq_det(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
 
+// deterministic: dK and dV by the gradient kernel without its dQ part, dQ
+// by fa_bwd_dq_det_kernel (one CTA per query tile, key tiles in a fixed
+// order), so no sum depends on the order in which CTAs run.
 template <int D>
 int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                 const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
+                 const CUtensorMap& tdq, const BwdParams& p, bool deterministic, cudaStream_t stream) {
   const long long rows = p.T * p.Hq;
   const long long pre_blocks = (rows * 8 + 255) / 256;
   fa_bwd_rowdot_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, stream>>>(p);
@@ -495,24 +504,26 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   if (e != cudaSuccess) return e;
   if constexpr (D == 64) {
     using Lay = BwdLayout<D>;
-    e = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+    auto kern = deterministic ? fa_bwd_kernel<D, false> : fa_bwd_kernel<D, true>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.Hkv, p.n_kvtiles, p.B);
-    fa_bwd_kernel<D><<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+    kern<<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     e = cudaGetLastError();
   } else {
-    e = static_cast<cudaError_t>(launch_bwd128_main(tq, tk, tv, tdo, tdq, p, stream));
+    e = static_cast<cudaError_t>(launch_bwd128_main(tq, tk, tv, tdo, tdq, p, !deterministic, stream));
   }
   if (e != cudaSuccess) return e;
+  if (deterministic) return launch_bwd_dq_det(D, tq, tk, tv, tdo, p, stream);
   const long long n8 = rows * D / 8;
   fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
   return cudaGetLastError();
 }
 
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-               const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
-  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, p, stream);
-  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, p, stream);
+               const CUtensorMap& tdq, const BwdParams& p, bool deterministic, cudaStream_t stream) {
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, p, deterministic, stream);
+  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, p, deterministic, stream);
   return -1;
 }
 

@@ -70,6 +70,9 @@ struct Bwd128Layout {
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
+// DQ = false compiles the dQ product and the dQ warpgroup out (the
+// deterministic backward computes dQ in a separate kernel).
+template <bool DQ>
 __global__ void __launch_bounds__(448, 1)
 fa_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -247,7 +250,7 @@ fa_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         umma_commit(s_full);
         // dP^T = V dO^T into the region the previous dQ has been read out of
         if (!(ok = mbar_wait(do_full, n & 1, abort_flag))) break;
-        if (n >= 1 && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
+        if (DQ && n >= 1 && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -272,13 +275,15 @@ fa_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           umma_ss(tmem + Lay::kColDK, sdesc_sw128(sDSa + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
                   sdesc_sw128(sQa + kk * 2048, Lay::kChunkBytes, 1024), id_tmn, (n > 0 || kk > 0));
         umma_commit(q_empty + st);
-        // dQ_n = dS K into the dP^T region, which phase 2 has finished reading
-        // (A: the dS^T tile read query-major, MN-major; B: K, MN-major)
+        if constexpr (DQ) {
+          // dQ_n = dS K into the dP^T region, which phase 2 has finished reading
+          // (A: the dS^T tile read query-major, MN-major; B: K, MN-major)
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(tmem + Lay::kColDP, sdesc_sw128(sDSa + kk * 2048, Lay::kChunkBytes, 1024),
-                  sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_mnmn, kk > 0);
-        umma_commit(dq_full);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ss(tmem + Lay::kColDP, sdesc_sw128(sDSa + kk * 2048, Lay::kChunkBytes, 1024),
+                    sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_mnmn, kk > 0);
+          umma_commit(dq_full);
+        }
       }
       if (ok) umma_commit(epi);
       if (!ok) give_up();
@@ -391,7 +396,7 @@ fa_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
       }
     }
-  } else {
+  } else if (DQ) {
     // ------------------------------------------------------------ dQ warpgroup
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row within the tile
@@ -452,12 +457,13 @@ fa_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 }
 
 int launch_bwd128_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tdq, const BwdParams& p, cudaStream_t stream) {
+                       const CUtensorMap& tdq, const BwdParams& p, bool dq, cudaStream_t stream) {
   using Lay = Bwd128Layout;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+  auto kern = dq ? fa_bwd128_kernel<true> : fa_bwd128_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Hkv, p.n_kvtiles, p.B);
-  fa_bwd128_kernel<<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+  kern<<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 

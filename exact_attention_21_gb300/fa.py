@@ -23,7 +23,7 @@ FA_ERR_LAUNCH = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_UNSUPPORTED = 5
 
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_deterministic", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
            "fa_decode_paged", "fa_decode_paged_fp8", "fa_decode_workspace_size", "fa_kv_quantize_fp8",
            "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
 
@@ -50,6 +50,8 @@ def lib():
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp,
                              ctypes.c_size_t, vp]
         L.fa_bwd.restype = i32
+        L.fa_bwd_deterministic.argtypes = list(L.fa_bwd.argtypes)
+        L.fa_bwd_deterministic.restype = i32
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32,
                                      vp, vp]
         L.fa_bwd_noalloc.restype = i32
@@ -107,6 +109,14 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal
     _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                         B, Hq, Hkv, N, d, T, float(scale), int(causal), _ptr(cu_seqlens), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens,
+                         workspace, stream=None):
+    """:func:`fa_bwd` with run-to-run bitwise reproducible results."""
+    _check(lib().fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), B, Hq, Hkv, N, d, T, float(scale), int(causal), _ptr(cu_seqlens),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens=None,
@@ -276,7 +286,7 @@ def attention_decode_fp8(q, k8, v8, k_scale, v_scale, scale=None, cu_seqlens_k=N
 
 
 def attention_backward(q, k, v, o, lse, dout, causal, scale=None, cu_seqlens=None, max_seqlen=None,
-                       workspace=None, stream=None):
+                       workspace=None, stream=None, deterministic=False):
     """Allocates dq, dk, dv (and the workspace if not given) and calls :func:`fa_bwd`."""
     T, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -293,5 +303,6 @@ def attention_backward(q, k, v, o, lse, dout, causal, scale=None, cu_seqlens=Non
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace, stream)
+    call = fa_bwd_deterministic if deterministic else fa_bwd
+    call(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace, stream)
     return dq, dk, dv

@@ -111,6 +111,21 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
            const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward pass with results that do not depend on the order in which the
+ * GPU runs thread blocks: bitwise identical outputs for identical inputs.
+ * fa_bwd sums dQ over key tiles with bulk reduce-adds whose order varies from
+ * run to run (an f32 sum is not associative); here dK and dV come from the
+ * same kernel without its dQ part, and each query tile's dQ is accumulated by
+ * one thread block over the key tiles in ascending order, recomputing S and
+ * dP for it ("Attention 算子优化…", section 四: recomputation).  About 1.4x the
+ * tensor-core work of fa_bwd.  Arguments, workspace and errors as for fa_bwd.
+ */
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv,
+                         int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
+                         const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace fa_bwd needs: the row dots D (f32 [Hq, T]) and the f32 dQ
  * accumulator ([T, Hq, d]), each rounded up to 256 bytes.  Returns 0 for
  * non-positive arguments. */

@@ -93,3 +93,64 @@ def test_bwd_workload(cuda_device, name):
         for gname, x, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
             e = rel_fro(x[sl, h:h + 1], r)
             assert e <= BWD_REL_FRO, (b, h, gname, e)
+
+
+# ---------------------------------------------------------------- deterministic backward
+
+def run_bwd_det(t, causal, lengths=None, N=None, repeats=1):
+    fa = fa_module()
+    dev = torch.device("cuda:0")
+    q, k, v, do = (t[n].to(dev).contiguous() for n in ("q", "k", "v", "do"))
+    T = q.shape[0]
+    if lengths is None:
+        N = N or T
+        cu = None
+    else:
+        N = max(max(lengths), 1)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=dev)
+    o, lse = fa.attention_forward(q, k, v, causal, cu_seqlens=cu, max_seqlen=N)
+    outs = []
+    for _ in range(repeats):
+        outs.append(fa.attention_backward(q, k, v, o, lse, do, causal, cu_seqlens=cu, max_seqlen=N,
+                                          deterministic=True))
+    fast = fa.attention_backward(q, k, v, o, lse, do, causal, cu_seqlens=cu, max_seqlen=N)
+    fa.fa_stream_status()
+    return outs, fast
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("case", ["single", "gqa", "packed"])
+def test_bwd_deterministic_parity(cuda_device, d, causal, case):
+    if case == "single":
+        t, kw, T = make_qkv(300, 2, 2, d, seed=20, with_do=True), {}, 300
+    elif case == "gqa":
+        t, kw, T = make_qkv(3 * 384, 8, 2, d, seed=21, with_do=True), {"N": 384}, 3 * 384
+    else:
+        lengths = [5, 1, 300, 128, 129, 0, 640, 77]
+        t, kw, T = make_qkv(sum(lengths), 4, 1, d, seed=22, with_do=True), {"lengths": lengths}, sum(lengths)
+    outs, _ = run_bwd_det(t, causal, **kw)
+    got = [x.float().cpu().numpy() for x in outs[0]]
+    ref = oracle.attention_backward(f64(t["q"]), f64(t["k"]), f64(t["v"]), f64(t["do"]),
+                                    cu_of(T, kw.get("lengths"), kw.get("N")), d ** -0.5, causal)
+    for name, x, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.isfinite(x).all(), name
+        assert rel_fro(x, r) <= BWD_REL_FRO, (name, rel_fro(x, r))
+
+
+@pytest.mark.parametrize("name", ["fwdbwd_b2_h16_n4096_d64_causal", "fwdbwd_b2_h32_n4096_d128_causal"])
+def test_bwd_deterministic_is_bitwise_reproducible(cuda_device, name):
+    """Three runs give identical bits; dK and dV also equal the fast
+    backward's bit for bit (the same kernel without its dQ part), and dQ
+    agrees with the fast backward's to its rounding."""
+    w = WORKLOADS[name]
+    t = make_inputs(w)
+    outs, fast = run_bwd_det(t, w.causal, N=w.N, repeats=3)
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(outs[0], outs[2]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int16), fast[1].view(torch.int16))
+    assert torch.equal(outs[0][2].view(torch.int16), fast[2].view(torch.int16))
+    dq_d, dq_f = outs[0][0].float(), fast[0].float()
+    assert ((dq_d - dq_f).norm() / dq_f.norm()).item() <= 1e-2
