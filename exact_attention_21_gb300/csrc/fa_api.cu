@@ -26,6 +26,38 @@ int launch_decode_fp8(int d, const CUtensorMap& tk, const CUtensorMap& tv, const
 int launch_quantize_fp8(int d, const void* x, void* x8, float* scale, long long rows, cudaStream_t stream);
 }  // namespace fa
 
+namespace fa {
+// A wait that nothing ever completes, through the kernels' own bounded wait:
+// warp 1 waits on an mbarrier that warp 0 initialises and never arrives on;
+// when the wait gives up it latches the timeout bit in the status word and
+// raises the CTA's abort flag, as a kernel role would, and warp 0 (which
+// waits on the abort flag) winds down with it.
+__global__ void __launch_bounds__(64) fa_selftest_timeout_kernel(unsigned* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int* ab = &abort_flag;
+  if (threadIdx.x == 32) {
+    if (!mbar_wait_limit(&bar, 0, ab, limit_ns)) {
+      atomicOr(status, kStatusTimeout);
+      *ab = 1;
+    }
+  } else if (threadIdx.x == 0) {
+    // a role that would arrive on the barrier once its work is done; it only
+    // waits for the abort, with a bound of its own
+    const uint64_t t0 = globaltimer_ns();
+    while (!*ab && globaltimer_ns() - t0 < 4 * limit_ns) {
+    }
+  }
+  __syncthreads();
+}
+}  // namespace fa
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -465,6 +497,19 @@ int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void
   g_err[0] = '\0';
   return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace,
                     workspace_bytes, true, stream);
+}
+
+int fa_selftest_wait_timeout(int limit_ms, void* stream) {
+  g_err[0] = '\0';
+  if (limit_ms < 1 || limit_ms > 10000) return fail(FA_ERR_INVALID_ARG, "limit_ms must be in [1, 10000]");
+  DeviceState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc) return rc;
+  fa::fa_selftest_timeout_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(
+      dev->status, static_cast<unsigned long long>(limit_ms) * 1000000ull);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "self-test launch failed: %s", cudaGetErrorString(e));
+  return FA_OK;
 }
 
 int fa_tile_counts(int B, const int* lengths, int causal, long long* out) {

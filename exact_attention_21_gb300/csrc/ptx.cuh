@@ -64,9 +64,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with parity `parity` to complete.  Gives up
-// (returns false) when *abort_flag becomes non-zero or after
-// FA_WAIT_LIMIT_NS; the caller then records the timeout and winds down.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// (returns false) when *abort_flag becomes non-zero or after limit_ns of
+// %globaltimer; the caller then records the timeout and winds down.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -75,8 +76,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > FA_WAIT_LIMIT_NS) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// mbar_wait_limit with the library's limit, FA_WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_wait_limit(bar, parity, abort_flag, FA_WAIT_LIMIT_NS);
 }
 
 // ------------------------------------------------------------------ TMA

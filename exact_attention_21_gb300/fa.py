@@ -25,7 +25,7 @@ FA_ERR_UNSUPPORTED = 5
 
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_deterministic", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
            "fa_decode_paged", "fa_decode_paged_fp8", "fa_decode_workspace_size", "fa_kv_quantize_fp8",
-           "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
+           "fa_selftest_wait_timeout", "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
 
 
 class FAError(RuntimeError):
@@ -74,6 +74,8 @@ def lib():
         L.fa_decode_workspace_size.restype = ctypes.c_size_t
         L.fa_tile_counts.argtypes = [i32, ctypes.POINTER(ctypes.c_int), i32, ctypes.POINTER(ctypes.c_longlong)]
         L.fa_tile_counts.restype = i32
+        L.fa_selftest_wait_timeout.argtypes = [i32, vp]
+        L.fa_selftest_wait_timeout.restype = i32
         L.fa_stream_status.argtypes = [vp]
         L.fa_stream_status.restype = i32
         L.fa_last_error_string.argtypes = []
@@ -216,6 +218,11 @@ def fa_tile_counts(lengths, causal):
     out = (ctypes.c_longlong * max(n, 1))()
     _check(lib().fa_tile_counts(n, arr, int(causal), out))
     return [int(out[i]) for i in range(n)]
+
+
+def fa_selftest_wait_timeout(limit_ms, stream=None):
+    """Runs the bounded-wait self-test (a wait that nothing completes)."""
+    _check(lib().fa_selftest_wait_timeout(int(limit_ms), _stream(stream)))
 
 
 def fa_stream_status(stream=None):

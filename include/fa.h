@@ -276,6 +276,19 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
                    const int* cu_seqlens, void* stream);
 
+/*
+ * Self-test of failure detection (no passage of the source pages has a
+ * counterpart).  Every wait inside the kernels is bounded: a wait that runs
+ * out latches a bit in the device status word, the kernel winds down without
+ * trapping, and the next fa_stream_status() returns FA_ERR_TIMEOUT while the
+ * CUDA context stays usable.  This launches one block whose bounded wait, the
+ * kernels' own, waits on a barrier nothing ever completes, with a limit of
+ * limit_ms milliseconds (1..10000) instead of the kernels' 2 s, so that a
+ * caller or a test can exercise that path on demand.  After it,
+ * fa_stream_status(stream) returns FA_ERR_TIMEOUT (and clears the word).
+ */
+int fa_selftest_wait_timeout(int limit_ms, void* stream);
+
 /* Synchronises `stream`, then reports and clears the device status word:
  * FA_ERR_TIMEOUT if a bounded wait gave up, FA_ERR_INVALID_ARG if packed
  * offsets were out of range, FA_ERR_LAUNCH if the stream itself failed. */

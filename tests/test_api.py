@@ -113,3 +113,8 @@ def test_decode_rejects_bad_arguments_on_host(fa, kw, code):
                             a["N"], a["d"], a["T"], a["scale"], a["cu"], vp(a["ws"]), a["ws_bytes"], None)
     assert rc == getattr(fa, "FA_ERR_" + code)
     assert fa.lib().fa_last_error_string().decode()
+
+
+@pytest.mark.parametrize("ms", [0, -5, 10001])
+def test_selftest_rejects_bad_limits_on_host(fa, ms):
+    assert fa.lib().fa_selftest_wait_timeout(ms, None) == fa.FA_ERR_INVALID_ARG
