@@ -123,6 +123,24 @@ def traffic_entry(path, workload, kernel):
     return None
 
 
+def max_over_ranks(pg, values, device):
+    """Each value's maximum over all ranks: the job takes as long as its
+    slowest rank.  pg is torch.distributed (or None for one process)."""
+    if pg is None:
+        return [float(x) for x in values]
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_rate(units_per_step, steps, world, total_ms):
+    """Whole-job throughput: every rank processes units_per_step per step
+    (weak scaling: replicas, no data-path collective), over the slowest
+    rank's time."""
+    return units_per_step * steps * world / (total_ms * 1e-3)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -231,14 +249,11 @@ def bench_ours(args, world, rank, local):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     fa.fa_stream_status(stream)
 
-    if pg:
-        t = torch.tensor([total_ms, e2e_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks(pg, [total_ms, e2e_ms], dev)
 
     flops_step = w.fwd_flops() + (w.bwd_flops() if w.backward else 0.0)
-    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
-    e2e_value = flops_step * world / (e2e_ms * 1e-3) / 1e12
+    value = job_rate(flops_step, args.steps, world, total_ms) / 1e12
+    e2e_value = job_rate(flops_step, 1, world, e2e_ms) / 1e12
 
     peaks, peak_src = load_peaks()
     fwd_avg = statistics.mean(fwd_ms)
@@ -393,13 +408,10 @@ def bench_decode(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     fa.fa_stream_status(stream)
-    if pg:
-        t = torch.tensor([total_ms, e2e_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks(pg, [total_ms, e2e_ms], dev)
 
     nbytes = w.decode_bytes()
-    value = nbytes * args.steps * world / (total_ms * 1e-3) / 1e9
+    value = job_rate(nbytes, args.steps, world, total_ms) / 1e9
     avg_ms = total_ms / args.steps
     peaks, peak_src = load_peaks()
     peak = peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])
@@ -431,7 +443,7 @@ def bench_decode(args, world, rank, local):
                      "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None},
-        "e2e": {"value": round(nbytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_rate(nbytes, 1, world, e2e_ms) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
