@@ -123,6 +123,13 @@ def traffic_entry(path, workload, kernel):
     return None
 
 
+def step_stats(step_ms):
+    """Median and 90th percentile of per-step event times (ms)."""
+    xs = sorted(step_ms)
+    return {"ms_median": round(statistics.median(xs), 4),
+            "ms_p90": round(xs[min(len(xs) - 1, int(0.9 * len(xs)))], 4)}
+
+
 def max_over_ranks(pg, values, device):
     """Each value's maximum over all ranks: the job takes as long as its
     slowest rank.  pg is torch.distributed (or None for one process)."""
@@ -257,6 +264,8 @@ def bench_ours(args, world, rank, local):
 
     peaks, peak_src = load_peaks()
     fwd_avg = statistics.mean(fwd_ms)
+    # q, k, v read and o written once (bf16), and the LSE (f32)
+    fwd_bytes = 2 * T * d * (2 * Hq + 2 * Hkv) + 4 * Hq * T
     bwd_avg = statistics.mean(bwd_ms) if w.backward else 0.0
     if w.backward and bwd_avg > fwd_avg:
         kern, kflops, kms = "fa_bwd (row-dot, backward kernel, dQ convert)", w.bwd_flops(), bwd_avg
@@ -290,7 +299,11 @@ def bench_ours(args, world, rank, local):
         "pct_of_bf16_peak": round(100 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "kernel": kern, "achieved": round(achieved, 2), "peak": peak,
                      "peak_source": f"{peak_src} bf16_tflops (burst)", "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None},
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac_of_sustained": round(achieved / peaks.get("bf16_tflops_sustained",
+                                                                      PEAKS_FALLBACK["bf16_tflops_sustained"]), 4)},
+        "step_times": step_stats(step_ms),
+        "algorithmic_gbs_fwd": round(fwd_bytes / (fwd_avg * 1e-3) / 1e9, 1),
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
@@ -438,6 +451,7 @@ def bench_decode(args, world, rank, local):
                    "tokens_per_s": round(B * world / (avg_ms * 1e-3), 1),
                    "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"replicas x{world}"},
+        "step_times": step_stats(step_ms),
         "roofline": {"bound": "hbm", "kernel": "fa_decode" + ("_paged" if w.page_size else "") + ("_fp8" if w.fp8 else "")
                      + " (split kernel + combine)",
                      "achieved": round(achieved, 1),
