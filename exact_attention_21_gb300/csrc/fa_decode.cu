@@ -407,11 +407,10 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 //   warps 2-5  softmax warpgroup: thread = key row of S^T (TMEM lane) for the
 //              probabilities, and = dimension row of O^T for the rescale and
 //              the split's output.
-//   warps 6-9, 10-13  (FP8 cache only) converter warpgroups for K and for V:
-//              dequantise each E4M3 tile into a 16-bit tile in shared memory
-//              ("Attention 算子优化…", section 六: the cache stays FP8 in HBM,
-//              dequantisation happens on chip, the products run in 16-bit,
-//              softmax and accumulation in f32).
+//   warps 6-9  (FP8 cache only) converter warpgroup: dequantises each E4M3
+//              V tile into a 16-bit tile in shared memory ("Attention 算子优化…",
+//              section 六: the cache stays FP8 in HBM, dequantisation happens
+//              on chip, softmax and accumulation in f32).
 // S^T is double-buffered in TMEM, so S^T of tile i+1 runs while the softmax
 // works on tile i; P^T (16-bit, K-major: 16 head rows x 128 keys) is
 // double-buffered in shared memory.  The running max of a head only moves
@@ -419,9 +418,13 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 // any common reference gives the same merge, so this is exact and O^T is
 // rarely rescaled.
 //
-// With the FP8 cache the products run in f16 (the E4M3 values and the bf16
-// query convert to f16 without rounding, apart from query elements below
-// 2^-14), and the per-token scales fold into the per-key work of the softmax
+// With the FP8 cache S^T reads the E4M3 K tile as it arrived, in a
+// kind::f8f6f4 MMA: each head's query is scaled by s_q = 448 / max|q| and
+// written as three E4M3 rows, q1 = e4m3(s_q q), q2 = e4m3(s_q q - q1) and
+// q3 = e4m3(s_q q - q1 - q2), which carry s_q q to about 2^-12 relative, so
+// S^T (N = 48: 16 columns per term) loses nothing a bf16 query would keep;
+// the softmax threads add the three columns of a head and divide by s_q.  P V runs in f16 over V dequantised to f16 (exact) with P
+// in f16.  The per-token scales fold into the per-key work of the softmax
 // threads: s_k multiplies the key's scores, s_v its probabilities before the
 // P V product (the row sum keeps the unscaled probabilities).
 constexpr int kDecHeads = 16;               // MMA N: query heads per CTA, padded
@@ -435,25 +438,28 @@ struct DecTcLayout {
   static constexpr int kTile8Bytes = kTile * 128;      // E4M3 128 x 128 tile (one 128-byte row per key)
   // TMA stages: 16-bit K and V tiles, or E4M3 K and V tiles
   static constexpr int kStageBytes = FP8 ? 2 * kTile8Bytes : 2 * kTileBytes;
-  static constexpr int kStages = FP8 ? 2 : 3;
-  // FP8: dequantised K and V, two buffers each (K freed when S^T completes,
-  // V when P V completes)
-  static constexpr int kCvtBytes = FP8 ? 4 * kTileBytes : 0;
+  static constexpr int kStages = FP8 ? 4 : 3;
+  // FP8: dequantised V, two buffers (freed when P V completes)
+  static constexpr int kCvtBytes = FP8 ? 2 * kTileBytes : 0;
   static constexpr int kHChunkBytes = kDecHeads * 128;  // 16 rows x 64 16-bit elements
-  static constexpr int kQBytes = 2 * kHChunkBytes;      // Q: 16 heads x 128 dims, K-major
+  // Q: 16 heads x 128 dims, K-major, bf16; FP8: 48 E4M3 rows (three terms per head) x 128 dims
+  static constexpr int kQBytes = (FP8 ? 3 : 2) * kHChunkBytes;
   static constexpr int kPBytes = 2 * kHChunkBytes;      // P^T: 16 heads x 128 keys, K-major
   static constexpr int kOffCvt = kStages * kStageBytes;
   static constexpr int kOffQ = kOffCvt + kCvtBytes;
   static constexpr int kOffP = kOffQ + kQBytes;          // two buffers
   static constexpr int kOffRed = kOffP + 2 * kPBytes;    // f32 [4 warps][16 heads]
-  static constexpr int kOffBar = kOffRed + 4 * kDecHeads * 4;
+  static constexpr int kOffInvSq = kOffRed + 4 * kDecHeads * 4;  // FP8: f32 1 / s_q [16 heads]
+  static constexpr int kOffBar = kOffInvSq + kDecHeads * 4;
   // full[], empty[], q_ready, s_full[2], p_ready[2], pv_done[2], drain, k_ready[2], v_ready[2]
   static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
-  static constexpr int kThreads = FP8 ? 448 : 192;
-  static constexpr uint32_t kTmemCols = 64;
-  static constexpr uint32_t kColS = 0, kColO = 32;  // S^T buffers at 0 and 16
+  static constexpr int kThreads = FP8 ? 320 : 192;
+  // S^T buffers of kSCols columns at 0 and kSCols (FP8: a column per head and term), O^T after them
+  static constexpr int kSCols = FP8 ? 3 * kDecHeads : kDecHeads;
+  static constexpr uint32_t kTmemCols = FP8 ? 128 : 64;
+  static constexpr uint32_t kColS = 0, kColO = 2 * kSCols;
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -497,7 +503,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   constexpr int D = Lay::D;
   constexpr int H = kDecHeads;
   // the MMAs read 16-bit operands: bf16 for a bf16 cache, f16 for an E4M3 one
-  constexpr uint32_t id_s = FP8 ? idesc_f16_f32(kTile, H, false, false) : idesc_bf16_f32(kTile, H, false, false);
+  // S^T: E4M3 K x the E4M3 query terms for an FP8 cache, bf16 otherwise; P V: 16-bit
+  constexpr uint32_t id_s = FP8 ? idesc_e4m3_f32(kTile, 3 * H) : idesc_bf16_f32(kTile, H, false, false);
   constexpr uint32_t id_o = FP8 ? idesc_f16_f32(D, H, true, false) : idesc_bf16_f32(D, H, true, false);
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -519,32 +526,31 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint64_t* q_ready = empty + NS;
   uint64_t* s_full = q_ready + 1;
   uint64_t* p_ready = s_full + 2;
-  uint64_t* pv_done = p_ready + 2;  // FP8: also frees dequantised buffer i & 1
+  uint64_t* pv_done = p_ready + 2;  // FP8: also frees dequantised V buffer i & 1
   uint64_t* drain = pv_done + 2;
-  uint64_t* k_ready = drain + 1;     // FP8 only: dequantised K of tile i in buffer i & 1
-  uint64_t* v_ready = k_ready + 2;   // FP8 only: dequantised V of tile i in buffer i & 1
+  uint64_t* v_ready = drain + 1;     // FP8 only: dequantised V of tile i in buffer i & 1
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
   auto stage = [&](int st) { return smem + st * Lay::kStageBytes; };
   auto pbuf = [&](int i) { return smem + Lay::kOffP + (i & 1) * Lay::kPBytes; };
-  // 16-bit K and V tiles the MMAs of tile i read
-  auto k16 = [&](int i) { return FP8 ? smem + Lay::kOffCvt + (i & 1) * Lay::kTileBytes : stage(i % NS); };
+  // the K tile S^T of tile i reads (E4M3 for an FP8 cache) and the 16-bit V tile of P V
+  auto ktile = [&](int i) { return stage(i % NS); };
   auto v16 = [&](int i) {
-    return FP8 ? smem + Lay::kOffCvt + (2 + (i & 1)) * Lay::kTileBytes : stage(i % NS) + Lay::kTileBytes;
+    return FP8 ? smem + Lay::kOffCvt + (i & 1) * Lay::kTileBytes : stage(i % NS) + Lay::kTileBytes;
   };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full + i, 1);
-      mbar_init(empty + i, FP8 ? 256 : 1);  // FP8: released by both converter warpgroups
+      // FP8: released by S^T's commit (K) and the converter warpgroup (V)
+      mbar_init(empty + i, FP8 ? 129 : 1);
     }
     mbar_init(q_ready, 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_ready + i, 128);
       mbar_init(pv_done + i, 1);
-      mbar_init(k_ready + i, 128);
       mbar_init(v_ready + i, 128);
     }
     mbar_init(drain, 1);
@@ -594,17 +600,24 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     if (lane == 0) {
       const uint32_t sQa = smem_u32(sQ);
       auto issue_s = [&](int i) -> bool {
-        // the 16-bit K tile of tile i: loaded (bf16) or dequantised (FP8)
-        if (!mbar_wait(FP8 ? k_ready + (i & 1) : full + i % NS, FP8 ? (i >> 1) & 1 : (i / NS) & 1, abort_flag))
-          return false;
+        if (!mbar_wait(full + i % NS, (i / NS) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t sKa = smem_u32(k16(i));
+        const uint32_t sKa = smem_u32(ktile(i));
+        if constexpr (FP8) {
+          // E4M3 K (one 128-byte row per key) x the 48 E4M3 query rows, 32 elements per step
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + Lay::kColS + (i & 1) * H,
-                  sdesc_sw128(sKa + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
-                  sdesc_sw128(sQa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_s, kk > 0);
+          for (int kk = 0; kk < D / 32; ++kk)
+            umma_ss_f8(tmem + Lay::kColS + (i & 1) * Lay::kSCols, sdesc_sw128(sKa + kk * 32, 16, 1024),
+                       sdesc_sw128(sQa + kk * 32, 16, 1024), id_s, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + Lay::kColS + (i & 1) * Lay::kSCols,
+                    sdesc_sw128(sKa + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
+                    sdesc_sw128(sQa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_s, kk > 0);
+        }
         umma_commit(s_full + (i & 1));
+        if constexpr (FP8) umma_commit(empty + i % NS);  // the K half of the stage has been read
         return true;
       };
       bool ok = mbar_wait(q_ready, 0, abort_flag);
@@ -637,27 +650,74 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const int group = p.group;
     const int hq0 = g * group;
     const float c = p.scale_log2;
-    // Q (16 head rows x 128 dims, K-major, 128-byte swizzle); padded heads are 0
-    {
+    // Q, K-major with the 128-byte swizzle; padded heads are 0
+    float inv_sq[H];  // FP8: 1 / s_q of each head
+    if constexpr (FP8) {
+      // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h; thread r
+      // takes dims 16 (r % 8) .. +15 of head r / 8 (one 16-byte unit per row)
+      const int h = r / 8, sub = r % 8;
+      float v[16];
+      if (h < group) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                          (static_cast<long long>(b) * p.Hq + hq0 + h) * D + 16 * sub);
+        const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
+        const uint32_t wq[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          v[2 * e] = bf16_lo(wq[e]);
+          v[2 * e + 1] = bf16_hi(wq[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
+      // the 8 threads of a head are 8 consecutive lanes
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const float sq = amax > 0.f ? 448.f / amax : 1.f;
+      uint32_t term[3][4] = {};
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        float2 y = make_float2(v[e] * sq, v[e + 1] * sq);  // remainder still to represent
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+          const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+          const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(c2, __NV_E4M3);
+          y.x -= __half2float(*reinterpret_cast<const __half*>(&hb.x));  // exact in f32
+          y.y -= __half2float(*reinterpret_cast<const __half*>(&hb.y));
+          term[t][e / 4] |= static_cast<uint32_t>(c2) << (16 * ((e / 2) & 1));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 3; ++t) {
+        const int row = t * kDecHeads + h;
+        *reinterpret_cast<uint4*>(sQ + row * 128 + ((sub ^ (row & 7)) << 4)) =
+            make_uint4(term[t][0], term[t][1], term[t][2], term[t][3]);
+      }
+      float* sInvSq = reinterpret_cast<float*>(smem + Lay::kOffInvSq);
+      if (sub == 0) sInvSq[h] = 1.f / sq;
+      fence_proxy_async_smem();
+      mbar_arrive(q_ready);
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // every head's 1 / s_q written
+#pragma unroll
+      for (int hh = 0; hh < H; ++hh) inv_sq[hh] = sInvSq[hh];
+    } else {
       const int h = r / 8, u2 = (r % 8) * 2;  // 8 threads per head row, two 16-byte units each
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
                                                         (static_cast<long long>(b) * p.Hq + hq0 + h) * D);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int u = u2 + j;  // unit of the 256-byte row: chunk u / 8, unit u % 8
-        uint4 val = h < group ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-        if constexpr (FP8) {  // bf16 -> f16 for the f16 products
-          uint32_t* w = reinterpret_cast<uint32_t*>(&val);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2 hh = __floats2half2_rn(bf16_lo(w[e]), bf16_hi(w[e]));
-            w[e] = *reinterpret_cast<const uint32_t*>(&hh);
-          }
-        }
+        const uint4 val = h < group ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(sQ + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = val;
       }
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
+#pragma unroll
+      for (int hh = 0; hh < H; ++hh) inv_sq[hh] = 1.f;
     }
     float m[H], lt[H];
 #pragma unroll
@@ -685,12 +745,23 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       bool over = false;  // a score above its head's reference by more than the slack
       if (w) {
         tc_fence_after();
-        uint32_t svv[H];
-        tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (i & 1) * H, lane_base, 0), svv);
+        uint32_t svv[Lay::kSCols];
+        float sc[H];
+        if constexpr (FP8) {
+          const uint32_t ts = tmem + Lay::kColS + (i & 1) * Lay::kSCols;
+          tmem_ld_x16_x32_pair(tmem_addr(ts, lane_base, 2 * H), svv + 2 * H, tmem_addr(ts, lane_base, 0), svv);
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+            sc[h] = (__uint_as_float(svv[h]) + __uint_as_float(svv[H + h]) + __uint_as_float(svv[2 * H + h])) * inv_sq[h];
+        } else {
+          tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (i & 1) * Lay::kSCols, lane_base, 0), svv);
+#pragma unroll
+          for (int h = 0; h < H; ++h) sc[h] = __uint_as_float(svv[h]);
+        }
         const float ck = c * sk;
 #pragma unroll
         for (int h = 0; h < H; ++h) {
-          x[h] = valid ? __uint_as_float(svv[h]) * ck : -INFINITY;
+          x[h] = valid ? sc[h] * ck : -INFINITY;
           over |= x[h] > m[h] + kDecRescaleSlack;  // always for a valid key on the first tile (m = -inf)
         }
       }
@@ -795,26 +866,19 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
     }
   } else if constexpr (FP8) {
-    // ------------------------------------------------------------ converter warpgroups
-    // Thread r dequantises key row r of the tile's K (warps 6-9) or V (warps
-    // 10-13): 8 units of 16 E4M3 codes each, into 16 f16 units of the
-    // 128-byte-swizzled 16-bit tiles the MMAs read.  The per-token scales are
-    // applied elsewhere.  K and V of tile i go to buffers i & 1 once S^T and
-    // P V of tile i - 2 are done with them.  The E4M3 stage is released when
-    // both halves are converted, so the loads run ahead of the products.
-    const bool is_v = warp >= 10;
-    const int r = (warp - (is_v ? 10 : 6)) * 32 + lane;
+    // ------------------------------------------------------------ converter warpgroup
+    // Thread r dequantises key row r of the tile's V: 8 units of 16 E4M3 codes
+    // each, into 16 f16 units of the 128-byte-swizzled 16-bit tile P V reads
+    // (buffer i & 1, once P V of tile i - 2 is done with it).  The per-token
+    // scales are applied elsewhere.
+    const int r = (warp - 6) * 32 + lane;
     bool ok = true;
     for (int i = 0; i < nt && ok; ++i) {
       const int st = i % NS;
       if (!(ok = mbar_wait(full + st, (i / NS) & 1, abort_flag))) break;
-      if (!is_v) {
-        if (i >= 2 && !(ok = mbar_wait(s_full + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) break;
-      } else if (i >= 2 && !(ok = mbar_wait(pv_done + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) {
-        break;
-      }
-      const uint8_t* src = stage(st) + (is_v ? Lay::kTile8Bytes : 0) + r * 128;
-      uint8_t* dst = (is_v ? v16(i) : k16(i)) + r * 128;
+      if (i >= 2 && !(ok = mbar_wait(pv_done + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) break;
+      const uint8_t* src = stage(st) + Lay::kTile8Bytes + r * 128;
+      uint8_t* dst = v16(i) + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint4 e = *reinterpret_cast<const uint4*>(src + ((u ^ (r & 7)) << 4));  // dims 16u .. 16u+15
@@ -831,8 +895,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         *reinterpret_cast<uint4*>(chunk + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
       }
       fence_proxy_async_smem();
-      mbar_arrive((is_v ? v_ready : k_ready) + (i & 1));
-      mbar_arrive(empty + st);  // this half of the E4M3 stage has been read
+      mbar_arrive(v_ready + (i & 1));
+      mbar_arrive(empty + st);  // the V half of the E4M3 stage has been read
     }
     if (!ok) give_up();
   }
