@@ -8,7 +8,7 @@
 //     S^T  = K_j Q_i^T                 P^T = exp2(S^T * c - LSE * log2 e)
 //     dP^T = V_j dO_i^T                dS^T = P^T * (dP^T - D)
 //     dV_j += P^T dO_i                 dK_j += dS^T Q_i
-//     dQ_i += dS K_j   (f32 bulk reduce-add into a global accumulator)
+//     dQ_i += dS K_j   (f32 bulk reduce-adds into a global accumulator)
 // and finally dK *= scale, dQ = scale * dQ_acc.  P is recomputed already
 // normalised from the LSE, so no running max is needed.
 //
@@ -22,25 +22,29 @@
 // the group accumulate in TMEM with no atomics.  Warp roles:
 //   warp 0       producer: K_j, V_j once (TMA); per step Q_i, dO_i (TMA) and
 //                the LSE / D values of the tile (plain loads) into a 3-stage ring.
-//   warp 1       TMEM allocator and MMA issuer (one thread).
+//   warp 1       TMEM allocator; MMA issuer A (one thread): dV.
+//   warp 14      MMA issuer B (one thread): dP^T, dK and dQ.
+//   warp 15      MMA issuer C (one thread): S^T.
 //   warps 2..9   two score warpgroups: thread = key row (TMEM lane); the
 //                first takes query columns 0..63, the second 64..127; P^T to
-//                TMEM (bf16) and dS^T to shared memory; dV / dK epilogue.
-//   warps 10..13 dQ warpgroup: dQ tile TMEM -> swizzled shared memory -> TMA
-//                bulk reduce-add (f32), in two 32-column halves per step.
-// MMA issue order: once the score warpgroups finish step n, dV += P^T_n dO_n,
-// dK += dS^T_n Q_n, dQ_n = dS_n K; then, as soon as the score warpgroups of
-// step n+1 have read their dP^T and the dQ of step n has been read out,
-// S^T_{n+2} and dP^T_{n+2}.  The scores of the next step are thus computed
-// while the score warpgroups still work on the current one.
-// TMEM (d = 64, 512 columns): two step regions of 128 columns (S^T f32; P^T
-// bf16 for queries 0..63 over columns 0..31 and for queries 64..127 over
-// columns 64..95, each written by the warpgroup that read those S^T columns;
-// dQ f32 over columns 64..127, written by an MMA issued after the dV product
-// that reads P^T),
-// dP^T [256, 384), dV [384, 448), dK [448, 512).  dS^T lives in shared memory
-// only (double-buffered); the same swizzled tile is the K-major A operand of
-// dK (rows = keys) and the MN-major A operand of dQ (rows = queries).
+//                TMEM (bf16), dS^T to TMEM and (for dQ) shared memory; dV / dK
+//                epilogue.
+//   warps 10..13 dQ warpgroup: dQ tile TMEM -> swizzled shared memory (the
+//                step's dS^T buffer, free once the dQ product has read it) ->
+//                two TMA bulk reduce-adds (f32) into the global accumulator.
+// MMA issue order: once the score warpgroups finish step n, dV += P^T_n dO_n
+// (A) and dK += dS^T_n Q_n (B) run side by side, then dQ_n = dS_n K (B, after
+// dV_n has read its operand); S^T_{n+2} (C) follows as soon as the dQ of step
+// n has been read out, and dP^T_{n+2} (B) as soon as the score warpgroups of
+// step n+1 have read their dP^T.  The scores of the next step are thus
+// computed while the score warpgroups still work on the current one.
+// TMEM (d = 64, 512 columns): two step regions of 128 columns (S^T f32; each
+// 32-column chunk of S^T, once read, takes the bf16 P^T of its 32 queries in
+// its first 16 columns and their bf16 dS^T in the last 16, so dV and dK both
+// take their A operand from TMEM; dQ f32 over columns 64..127, written by an
+// MMA issued after the dV and dK products that read them),
+// dP^T [256, 384), dV [384, 448), dK [448, 512).  dS^T also goes to shared
+// memory (double-buffered) as the MN-major A operand of dQ (rows = queries).
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
@@ -56,16 +60,15 @@ struct BwdLayout {
   static constexpr int kStatBytes = 2 * kTile * 4;  // lse2[128], rowdot[128]
   static constexpr int kStageBytes = (2 * kTileBytes + kStatBytes + 1023) / 1024 * 1024;
   static constexpr int kDSBytes = 2 * kChunkBytes;  // 128 keys x 128 queries bf16
-  static constexpr int kDQBytes = kTile * 32 * 4;   // 128 queries x 32 f32 staging half-tile
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffDS = kOffV + kTileBytes;  // two buffers
-  static constexpr int kOffDQ = kOffDS + 2 * kDSBytes;
-  static constexpr int kOffRing = kOffDQ + kDQBytes;
+  // two buffers; each also stages the f32 dQ tile of its step (32 KB as well)
+  static constexpr int kOffDS = kOffV + kTileBytes;
+  static constexpr int kOffRing = kOffDS + 2 * kDSBytes;
   static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
-  // kv_full, qdo_full[], qdo_empty[], sdp_full, ps_ready[2], dp_free, dq_full, dq_free,
-  // dq_staged, dq_stage_free, epi, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 11;
+  // kv_full, qdo_full[], qdo_empty[], sdp_full[2], ps_ready[2], dp_free, dq_full[2], dq_free[2],
+  // dq_staged, ds_free[2], epi, drain, dv_done[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 17;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -76,10 +79,13 @@ struct BwdLayout {
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
+constexpr int kWarpIssuerB = 14, kWarpIssuerC = 15;
+constexpr int kBwdThreads = 32 * (kWarpIssuerC + 1);
+
 // DQ = false compiles the dQ product and the dQ warpgroup out (the
 // deterministic backward computes dQ in a separate kernel).
 template <int D, bool DQ>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
@@ -105,21 +111,21 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint8_t* sK = smem + Lay::kOffK;
   uint8_t* sV = smem + Lay::kOffV;
   uint8_t* sDS = smem + Lay::kOffDS;
-  uint8_t* sDQ = smem + Lay::kOffDQ;
   uint8_t* ring = smem + Lay::kOffRing;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
   uint64_t* kv_full = bars;
   uint64_t* qdo_full = kv_full + 1;
   uint64_t* qdo_empty = qdo_full + NS;
-  uint64_t* sdp_full = qdo_empty + NS;
-  uint64_t* ps_ready = sdp_full + 1;
+  uint64_t* sdp_full = qdo_empty + NS;  // sdp_full[n & 1]
+  uint64_t* ps_ready = sdp_full + 2;
   uint64_t* dp_free = ps_ready + 2;  // ps_ready[n & 1]: one per step parity
-  uint64_t* dq_full = dp_free + 1;
-  uint64_t* dq_free = dq_full + 1;
-  uint64_t* dq_staged = dq_free + 1;
-  uint64_t* dq_stage_free = dq_staged + 1;
-  uint64_t* epi = dq_stage_free + 1;
+  uint64_t* dq_full = dp_free + 1;  // dq_full[n & 1]
+  uint64_t* dq_free = dq_full + 2;  // dq_free[n & 1]
+  uint64_t* dq_staged = dq_free + 2;
+  uint64_t* ds_free = dq_staged + 1;  // ds_free[n & 1]
+  uint64_t* epi = ds_free + 2;
   uint64_t* drain = epi + 1;
+  uint64_t* dv_done = drain + 1;  // dv_done[n & 1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
 
@@ -130,17 +136,26 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < NS; ++i) { mbar_init(qdo_full + i, 32); mbar_init(qdo_empty + i, 1); }
-    mbar_init(sdp_full, 1);
+    // the MMA issuers: S^T and dP^T commit on sdp_full (one barrier per step
+    // parity: S^T_{m+1} has no reason to wait for dP^T_m), dV and dK on
+    // qdo_empty and epi, all three on drain
+    for (int i = 0; i < NS; ++i) { mbar_init(qdo_full + i, 32); mbar_init(qdo_empty + i, 2); }
+    mbar_init(sdp_full, 2);
+    mbar_init(sdp_full + 1, 2);
     mbar_init(ps_ready, 256);
     mbar_init(ps_ready + 1, 256);
     mbar_init(dp_free, 256);
     mbar_init(dq_full, 1);
+    mbar_init(dq_full + 1, 1);
     mbar_init(dq_free, 128);
+    mbar_init(dq_free + 1, 128);
     mbar_init(dq_staged, 128);
-    mbar_init(dq_stage_free, 1);
-    mbar_init(epi, 1);
-    mbar_init(drain, 1);
+    mbar_init(ds_free, 1);
+    mbar_init(ds_free + 1, 1);
+    mbar_init(epi, 2);
+    mbar_init(drain, 3);
+    mbar_init(dv_done, 1);
+    mbar_init(dv_done + 1, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -216,78 +231,95 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int i = 0; i < NS; ++i)
         if (uses[i]) mbar_wait(qdo_full + i, (uses[i] - 1) & 1, &never);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kWarpIssuerB || warp == kWarpIssuerC) {
+    // ------------------------------------------------------------ MMA issuers
+    // Three issuing threads, each with its own order of waits, so that no
+    // product queues behind a wait that belongs to another (one thread also
+    // starts an N = 64 product only about every 55 cycles, half the tensor
+    // core's rate for that shape).  A (warp 1): dV.  B: dK, dQ, dP^T.  C: S^T.
     if (lane == 0) {
+      const int role = warp == 1 ? 0 : (warp == kWarpIssuerB ? 1 : 2);
       constexpr uint32_t id_sdp = idesc_bf16_f32(kTile, kTile, false, false);  // K-major x K-major
-      constexpr uint32_t id_dv = idesc_bf16_f32(kTile, D, false, true);        // TMEM A x MN-major B
-      constexpr uint32_t id_dk = idesc_bf16_f32(kTile, D, false, true);        // K-major A x MN-major B
+      constexpr uint32_t id_dvk = idesc_bf16_f32(kTile, D, false, true);       // TMEM A x MN-major B
       constexpr uint32_t id_dq = idesc_bf16_f32(kTile, D, true, true);         // MN-major A x MN-major B
       const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV), sDSa = smem_u32(sDS);
-      auto issue_sdp = [&](int n) {
-        const int st = n % NS;
-        const uint32_t sQa = smem_u32(stage_q(st)), sDOa = smem_u32(stage_do(st));
+      // S^T_m (C) or dP^T_m (B) = K or V times the Q or dO tile of step m
+      auto issue_score = [&](int m) {
+        const int st = m % NS;
+        const bool s_t = role == 2;
+        const uint32_t xa = s_t ? sKa : sVa;
+        const uint32_t ya = smem_u32(s_t ? stage_q(st) : stage_do(st));
+        const uint32_t dst = s_t ? region(m) : tmem + Lay::kColDP;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32;
-          umma_ss(region(n), sdesc_sw128(sKa + off, 16, 1024), sdesc_sw128(sQa + off, 16, 1024), id_sdp, kk > 0);
+          umma_ss(dst, sdesc_sw128(xa + off, 16, 1024), sdesc_sw128(ya + off, 16, 1024), id_sdp, kk > 0);
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32;
-          umma_ss(tmem + Lay::kColDP, sdesc_sw128(sVa + off, 16, 1024), sdesc_sw128(sDOa + off, 16, 1024), id_sdp,
-                  kk > 0);
-        }
-        umma_commit(sdp_full);
+        umma_commit(sdp_full + (m & 1));
       };
-      // S^T_m and dP^T_m need: the Q/dO stage of step m, the dP^T region
-      // released by the score warpgroups of step m-1 (they arrive on dp_free
-      // once their last dP^T load is done), and the step region of m-2,
-      // whose dQ the dQ warpgroup must have read.
+      // S^T_m needs the Q stage of step m and the step region of m-2: its dQ
+      // read out, or (no dQ) its dV and dK products done.  dP^T_m needs the
+      // dO stage and the dP^T region, which the score warpgroups of step m-1
+      // release (dp_free) once their dP^T loads are done.
       auto issue_next = [&](int m) -> bool {
         if (!mbar_wait(qdo_full + m % NS, (m / NS) & 1, abort_flag)) return false;
-        if (m >= 1 && !mbar_wait(dp_free, (m - 1) & 1, abort_flag)) return false;
-        if (DQ && m >= 2 && !mbar_wait(dq_free, (m - 2) & 1, abort_flag)) return false;
+        if (role == 2 && m >= 2) {
+          const int r = m - 2;
+          if (DQ ? !mbar_wait(dq_free + (r & 1), (r >> 1) & 1, abort_flag)
+                 : !mbar_wait(qdo_empty + r % NS, (r / NS) & 1, abort_flag))
+            return false;
+        }
+        if (role == 1 && m >= 1 && !mbar_wait(dp_free, (m - 1) & 1, abort_flag)) return false;
         tc_fence_after();
-        issue_sdp(m);
+        issue_score(m);
         return true;
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag);
       tc_fence_after();
-      if (ok) ok = issue_next(0);
-      if (ok && nsteps > 1) ok = issue_next(1);
-      for (int n = 0; n < nsteps && ok; ++n) {
-        const int st = n % NS;
-        // Score warpgroups may finish step n + 1 before this thread looks at
-        // step n, so each step parity has its own barrier: step n + 2 cannot
-        // start before S^T_{n+2} is issued below.
-        if (!(ok = mbar_wait(ps_ready + (n & 1), (n >> 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t sQa = smem_u32(stage_q(st)), sDOa = smem_u32(stage_do(st));
-        const uint32_t dsb = sDSa + (n & 1) * Lay::kDSBytes;
-        // dV += P^T dO  (A: P^T in TMEM; B: dO rows = queries = K, MN-major)
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ts(tmem + Lay::kColDV, region(n) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                  sdesc_sw128(sDOa + kk * 2048, Lay::kChunkBytes, 1024), id_dv, (n > 0 || kk > 0));
-        // dK += dS^T Q  (A: dS^T tile, rows = keys, K-major; B: Q rows = K, MN-major)
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(tmem + Lay::kColDK, sdesc_sw128(dsb + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
-                  sdesc_sw128(sQa + kk * 2048, Lay::kChunkBytes, 1024), id_dk, (n > 0 || kk > 0));
-        umma_commit(qdo_empty + st);
-        if constexpr (DQ) {
-          // dQ_n = dS K into the step region of n, whose dQ_{n-2} was read before
-          // S^T_n was issued  (A: the dS^T tile read query-major, MN-major; B: K, MN-major)
+      if (role == 2) {
+        for (int m = 0; m < nsteps && ok; ++m) ok = issue_next(m);
+      } else {
+        if (ok && role == 1) ok = issue_next(0);
+        if (ok && role == 1 && nsteps > 1) ok = issue_next(1);
+        for (int n = 0; n < nsteps && ok; ++n) {
+          const int st = n % NS;
+          // Score warpgroups may finish step n + 1 before this thread looks at
+          // step n, so each step parity has its own barrier: step n + 2 cannot
+          // start before its S^T and dP^T are issued.
+          if (!(ok = mbar_wait(ps_ready + (n & 1), (n >> 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          // dV += P^T dO (A) or dK += dS^T Q (B)  (A operand: P^T or dS^T in
+          // TMEM, queries 16 kk .. 16 kk + 15 at the columns the score
+          // warpgroups chose; B operand: dO or Q, rows = queries = K, MN-major)
+          const uint32_t ya = smem_u32(role == 0 ? stage_do(st) : stage_q(st));
+          const uint32_t acc = tmem + (role == 0 ? Lay::kColDV : Lay::kColDK);
+          const uint32_t a0 = region(n) + (role == 0 ? 0 : 16);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
-                    sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
-          umma_commit(dq_full);
+            umma_ts(acc, a0 + 64 * (kk / 4) + 32 * ((kk % 4) / 2) + 8 * (kk % 2),
+                    sdesc_sw128(ya + kk * 2048, Lay::kChunkBytes, 1024), id_dvk, (n > 0 || kk > 0));
+          if (role == 0) umma_commit(dv_done + (n & 1));
+          umma_commit(qdo_empty + st);
+          if (role == 1) {
+            if (DQ) {
+              // dQ_n = dS K into the step region of n, once dV_n has read the
+              // P^T there (dK_n, issued above by this thread, comes first
+              // anyway); its dQ_{n-2} was read before S^T_n was issued  (A: the
+              // dS^T tile read query-major, MN-major; B: K, MN-major)
+              if (!(ok = mbar_wait(dv_done + (n & 1), (n >> 1) & 1, abort_flag))) break;
+              tc_fence_after();
+              const uint32_t dsb = sDSa + (n & 1) * Lay::kDSBytes;
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
+                        sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
+              umma_commit(dq_full + (n & 1));
+            }
+            if (n + 2 < nsteps && !(ok = issue_next(n + 2))) break;
+          }
         }
-        if (n + 2 < nsteps && !(ok = issue_next(n + 2))) break;
+        if (ok) umma_commit(epi);
       }
-      if (ok) umma_commit(epi);
       if (!ok) give_up();
       umma_commit(drain);
       int never = 0;
@@ -306,7 +338,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
       const int st = n % NS;
-      if (!(ok = mbar_wait(sdp_full, n & 1, abort_flag))) break;
+      if (!(ok = mbar_wait(sdp_full + (n & 1), (n >> 1) & 1, abort_flag))) break;
       if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
       tc_fence_after();
       const float2* nlse2 = reinterpret_cast<const float2*>(stage_stats(st)) + half * 32;
@@ -344,16 +376,24 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           pk[t] = pack_bf16x2(pv.x, pv.y);
           dsk[t] = pack_bf16x2(dd.x, dd.y);
         }
-        // P^T overwrites S^T columns this thread has already read.
-        tmem_st_x16(tmem_addr(reg, lane_base, half * 64 + cl * 16), pk);
+        // P^T and dS^T (bf16) overwrite the 32 S^T columns this chunk has
+        // just read: P^T in the first 16, dS^T in the last 16.
+        tmem_st_x16(tmem_addr(reg, lane_base, col0), pk);
+        tmem_st_x16(tmem_addr(reg, lane_base, col0 + 16), dsk);
+        // The dS^T buffer of this step parity is free once the bulk reduces
+        // of dQ_{n-2}, staged there, have read it (one vote per warp, so the
+        // warp stays together for the TMEM loads that follow).
+        if (DQ && cl == 0 && n >= 2)
+          ok = __all_sync(0xffffffffu, mbar_wait(ds_free + (n & 1), ((n - 2) >> 1) & 1, abort_flag));
         // dS^T row r into the 128B-swizzled tile (query-contiguous rows).
 #pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
+        for (int u4 = 0; u4 < 4 && DQ && ok; ++u4) {
           const int u = cl * 4 + u4;
           *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
               make_uint4(dsk[4 * u4], dsk[4 * u4 + 1], dsk[4 * u4 + 2], dsk[4 * u4 + 3]);
         }
       }
+      if (!ok) break;
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -393,36 +433,40 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const bool issuer = (warp == 10 && lane == 0);
     bool ok = true;
     for (int n = 0; n < nsteps && ok; ++n) {
-      if (!(ok = mbar_wait(dq_full, n & 1, abort_flag))) break;
+      if (!(ok = mbar_wait(dq_full + (n & 1), (n >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       uint32_t v[D];
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) tmem_ld_x32(tmem_addr(region(n), lane_base, Lay::kColDQ + cc * 32), v + 32 * cc);
       tc_fence_before();
-      mbar_arrive(dq_free);
+      mbar_arrive(dq_free + (n & 1));
       const int h = step_head(n), q0 = step_qtile(n) * kTile;
+      // Stage dQ_n in the dS^T buffer of step n, which the dQ product has
+      // finished reading: two f32 boxes of 32 columns x 128 rows, 128-byte
+      // swizzle, added to the accumulator by two bulk reduces in flight at once.
+      uint8_t* buf = sDS + (n & 1) * Lay::kDSBytes;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
-        const int use = n * (D / 32) + cc;  // staging-tile use counter
-        // the previous reduce has finished reading the staging tile
-        if (use > 0 && !(ok = mbar_wait(dq_stage_free, (use - 1) & 1, abort_flag))) break;
-        // f32 box of 32 columns x 128 rows, 128-byte swizzle
-        uint8_t* row = sDQ + r * 128;
+        uint8_t* row = buf + cc * kTile * 128 + r * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4)) =
               make_uint4(v[32 * cc + 4 * u], v[32 * cc + 4 * u + 1], v[32 * cc + 4 * u + 2], v[32 * cc + 4 * u + 3]);
-        fence_proxy_async_smem();
-        mbar_arrive(dq_staged);
-        if (issuer) {
-          if (!(ok = mbar_wait(dq_staged, use & 1, abort_flag))) break;
-          // Rows past the sequence end hold exact zeros (P = 0 there), so the
-          // whole tile can be added; rows past T are clipped by the TMA unit.
-          tma_reduce_add_3d(&tm_dq, sDQ, cc * 32, h, static_cast<int>(seq0 + q0));
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(dq_stage_free);
-        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(dq_staged);
+      if (issuer) {
+        if (!(ok = mbar_wait(dq_staged, n & 1, abort_flag))) break;
+        // Rows past the sequence end hold exact zeros (P = 0 there), so the
+        // whole tile can be added; rows past T are clipped by the TMA unit.
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc)
+          tma_reduce_add_3d(&tm_dq, buf + cc * kTile * 128, cc * 32, h, static_cast<int>(seq0 + q0));
+        bulk_commit_group();
+        // the buffer goes back to the score warpgroups (dS^T of step n + 2)
+        // once the reduces have read it
+        bulk_wait_group_read0();
+        mbar_arrive(ds_free + (n & 1));
       }
     }
     if (issuer) bulk_wait_group0();
@@ -508,7 +552,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.Hkv, p.n_kvtiles, p.B);
-    kern<<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+    kern<<<grid, kBwdThreads, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     e = cudaGetLastError();
   } else {
     e = static_cast<cudaError_t>(launch_bwd128_main(tq, tk, tv, tdo, tdq, p, !deterministic, stream));
