@@ -345,12 +345,6 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Four f32 atomic adds to consecutive floats (16-byte aligned), no return value.
-__device__ __forceinline__ void red_add_v4_f32(float* p, float4 v) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
-}
-
 // ------------------------------------------------------------------ math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
