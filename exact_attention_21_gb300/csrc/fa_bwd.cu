@@ -57,20 +57,28 @@ struct BwdLayout {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kStages = 3;
-  static constexpr int kStatBytes = 2 * kTile * 4;  // lse2[128], rowdot[128]
-  static constexpr int kStageBytes = (2 * kTileBytes + kStatBytes + 1023) / 1024 * 1024;
-  static constexpr int kDSBytes = 2 * kChunkBytes;  // 128 keys x 128 queries bf16
+  static constexpr int kStageBytes = 2 * kTileBytes;  // Q_i, dO_i
+  static constexpr int kDSBytes = 2 * kChunkBytes;    // 128 keys x 128 queries bf16
+  static constexpr int kDSBufs = 3;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  // two buffers; each also stages the f32 dQ tile of its step (32 KB as well)
+  // dS^T of step n in buffer n % 3, which then stages the f32 dQ tile of the
+  // step (32 KB as well) for its bulk reduce-adds
   static constexpr int kOffDS = kOffV + kTileBytes;
-  static constexpr int kOffRing = kOffDS + 2 * kDSBytes;
-  static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
+  static constexpr int kOffRing = kOffDS + kDSBufs * kDSBytes;
+  // -LSE log2 e and -D of the step's 128 queries, f32, in slot n % 2: the
+  // score warpgroups read them during step n only
+  static constexpr int kOffStats = kOffRing + kStages * kStageBytes;
+  static constexpr int kStatBytes = 2 * kTile * 4;
+  static constexpr int kOffBar = kOffStats + 2 * kStatBytes;
   // kv_full, qdo_full[], qdo_empty[], sdp_full[2], ps_ready[2], dp_free, dq_full[2], dq_free[2],
-  // dq_staged, ds_free[2], epi, drain, dv_done[2]
-  static constexpr int kNumBars = 1 + 2 * kStages + 17;
+  // dq_staged, ds_free[3], epi, drain, dv_done[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16 + 1024;
+  // no room to round the dynamic shared memory base up to the 1 KB alignment
+  // of the 128-byte swizzle: the kernel requires an aligned base (it is, with
+  // no static shared memory) and otherwise sets a status bit and does nothing
+  static constexpr int kBytes = kOffMisc + 16;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColStep = 0;      // + 128 * (n & 1)
   static constexpr uint32_t kColDQ = 64;       // within a step region
@@ -106,8 +114,12 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int per_head = nqt - i0;
   const int nsteps = p.group * per_head;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusSmemAlign);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sK = smem + Lay::kOffK;
   uint8_t* sV = smem + Lay::kOffV;
   uint8_t* sDS = smem + Lay::kOffDS;
@@ -122,8 +134,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* dq_full = dp_free + 1;  // dq_full[n & 1]
   uint64_t* dq_free = dq_full + 2;  // dq_free[n & 1]
   uint64_t* dq_staged = dq_free + 2;
-  uint64_t* ds_free = dq_staged + 1;  // ds_free[n & 1]
-  uint64_t* epi = ds_free + 2;
+  uint64_t* ds_free = dq_staged + 1;  // ds_free[n % 3]
+  uint64_t* epi = ds_free + Lay::kDSBufs;
   uint64_t* drain = epi + 1;
   uint64_t* dv_done = drain + 1;  // dv_done[n & 1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
@@ -131,7 +143,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   auto stage_q = [&](int st) { return ring + st * Lay::kStageBytes; };
   auto stage_do = [&](int st) { return ring + st * Lay::kStageBytes + Lay::kTileBytes; };
-  auto stage_stats = [&](int st) { return reinterpret_cast<float*>(ring + st * Lay::kStageBytes + 2 * Lay::kTileBytes); };
+  auto step_stats = [&](int n) { return reinterpret_cast<float*>(smem + Lay::kOffStats + (n & 1) * Lay::kStatBytes); };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -150,8 +162,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(dq_free, 128);
     mbar_init(dq_free + 1, 128);
     mbar_init(dq_staged, 128);
-    mbar_init(ds_free, 1);
-    mbar_init(ds_free + 1, 1);
+    for (int i = 0; i < Lay::kDSBufs; ++i) mbar_init(ds_free + i, 1);
     mbar_init(epi, 2);
     mbar_init(drain, 3);
     mbar_init(dv_done, 1);
@@ -197,7 +208,6 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (n >= NS && !(ok = mbar_wait(qdo_empty + st, ((n / NS) - 1) & 1, abort_flag))) break;
       const int h = step_head(n), q0 = step_qtile(n) * kTile;
       if (lane == 0) {
-        // tiles first, so their latency overlaps the plain loads below
         mbar_expect_tx(qdo_full + st, 2 * Lay::kTileBytes);
         const int row = static_cast<int>(seq0 + q0);
         for (int c = 0; c < Lay::kChunks; ++c) {
@@ -205,7 +215,6 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           tma_load_3d(stage_do(st) + c * Lay::kChunkBytes, &tm_do, qdo_full + st, c * 64, h, row);
         }
       }
-      float* stats = stage_stats(st);
       const long long lrow = static_cast<long long>(h) * p.T + seq0 + q0;
       float lv[kTile / 32], dv[kTile / 32];
 #pragma unroll
@@ -215,14 +224,23 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         lv[t] = valid ? __ldg(p.lse + lrow + idx) : INFINITY;
         dv[t] = valid ? __ldg(p.rowdot + lrow + idx) : 0.f;
       }
+      // the stats slot of this step parity: the score warpgroups are done
+      // with step n - 2 (on a failed wait the stage still completes, so the
+      // drain below covers the loads already issued)
+      if (n >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(ps_ready + (n & 1), ((n - 2) >> 1) & 1, abort_flag));
+      if (ok) {
+        float* stats = step_stats(n);
 #pragma unroll
-      for (int t = 0; t < kTile / 32; ++t) {
-        // stored negated: -LSE * log2 e and -D (queries past the end: P = 0)
-        stats[lane + 32 * t] = -lv[t] * kLog2e;
-        stats[kTile + lane + 32 * t] = -dv[t];
+        for (int t = 0; t < kTile / 32; ++t) {
+          // stored negated: -LSE * log2 e and -D (queries past the end: P = 0)
+          stats[lane + 32 * t] = -lv[t] * kLog2e;
+          stats[kTile + lane + 32 * t] = -dv[t];
+        }
       }
       mbar_arrive(qdo_full + st);
       ++uses[st];
+      if (!ok) break;
     }
     if (!ok && lane == 0) give_up();
     if (lane == 0) {
@@ -308,7 +326,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               // dS^T tile read query-major, MN-major; B: K, MN-major)
               if (!(ok = mbar_wait(dv_done + (n & 1), (n >> 1) & 1, abort_flag))) break;
               tc_fence_after();
-              const uint32_t dsb = sDSa + (n & 1) * Lay::kDSBytes;
+              const uint32_t dsb = sDSa + (n % Lay::kDSBufs) * Lay::kDSBytes;
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk)
                 umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
@@ -341,14 +359,14 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (!(ok = mbar_wait(sdp_full + (n & 1), (n >> 1) & 1, abort_flag))) break;
       if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
       tc_fence_after();
-      const float2* nlse2 = reinterpret_cast<const float2*>(stage_stats(st)) + half * 32;
-      const float2* ndot2 = nlse2 + kTile / 2;
       const int q0 = step_qtile(n) * kTile;
+      const float2* nlse2 = reinterpret_cast<const float2*>(step_stats(n)) + half * 32;
+      const float2* ndot2 = nlse2 + kTile / 2;
       // Keys past the sequence end and keys after the query (diagonal tile,
       // causal) get P = 0: query columns below zero_below are zeroed.
       // Queries past the end carry -LSE = -inf, so their P is 0 already.
       const int zero_below = !key_ok ? kTile : ((causal && q0 == k0) ? r : 0);
-      uint8_t* ds_row = sDS + (n & 1) * Lay::kDSBytes + half * Lay::kChunkBytes + r * 128;
+      uint8_t* ds_row = sDS + (n % Lay::kDSBufs) * Lay::kDSBytes + half * Lay::kChunkBytes + r * 128;
       const uint32_t reg = region(n);
 #pragma unroll
       for (int cl = 0; cl < 2; ++cl) {
@@ -380,11 +398,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // just read: P^T in the first 16, dS^T in the last 16.
         tmem_st_x16(tmem_addr(reg, lane_base, col0), pk);
         tmem_st_x16(tmem_addr(reg, lane_base, col0 + 16), dsk);
-        // The dS^T buffer of this step parity is free once the bulk reduces
-        // of dQ_{n-2}, staged there, have read it (one vote per warp, so the
+        // The dS^T buffer of this step (n % 3) is free once the bulk reduces
+        // of dQ_{n-3}, staged there, have read it (one vote per warp, so the
         // warp stays together for the TMEM loads that follow).
-        if (DQ && cl == 0 && n >= 2)
-          ok = __all_sync(0xffffffffu, mbar_wait(ds_free + (n & 1), ((n - 2) >> 1) & 1, abort_flag));
+        if (DQ && cl == 0 && n >= Lay::kDSBufs)
+          ok = __all_sync(0xffffffffu, mbar_wait(ds_free + n % Lay::kDSBufs, (n / Lay::kDSBufs - 1) & 1, abort_flag));
         // dS^T row r into the 128B-swizzled tile (query-contiguous rows).
 #pragma unroll
         for (int u4 = 0; u4 < 4 && DQ && ok; ++u4) {
@@ -444,7 +462,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       // Stage dQ_n in the dS^T buffer of step n, which the dQ product has
       // finished reading: two f32 boxes of 32 columns x 128 rows, 128-byte
       // swizzle, added to the accumulator by two bulk reduces in flight at once.
-      uint8_t* buf = sDS + (n & 1) * Lay::kDSBytes;
+      uint8_t* buf = sDS + (n % Lay::kDSBufs) * Lay::kDSBytes;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint8_t* row = buf + cc * kTile * 128 + r * 128;
@@ -463,10 +481,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int cc = 0; cc < D / 32; ++cc)
           tma_reduce_add_3d(&tm_dq, buf + cc * kTile * 128, cc * 32, h, static_cast<int>(seq0 + q0));
         bulk_commit_group();
-        // the buffer goes back to the score warpgroups (dS^T of step n + 2)
-        // once the reduces have read it
-        bulk_wait_group_read0();
-        mbar_arrive(ds_free + (n & 1));
+        // The buffer of step n - 1 goes back to the score warpgroups (dS^T of
+        // step n + 2) once its reduces have read it; those of step n stay in
+        // flight meanwhile.
+        bulk_wait_group_read1();
+        if (n >= 1) mbar_arrive(ds_free + (n - 1) % Lay::kDSBufs);
       }
     }
     if (issuer) bulk_wait_group0();
