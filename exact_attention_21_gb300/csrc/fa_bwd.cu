@@ -22,8 +22,8 @@
 // the group accumulate in TMEM with no atomics.  Warp roles:
 //   warp 0       producer: K_j, V_j once (TMA); per step Q_i, dO_i (TMA) and
 //                the LSE / D values of the tile (plain loads) into a 3-stage ring.
-//   warp 1       TMEM allocator; MMA issuer A (one thread): dV.
-//   warp 14      MMA issuer B (one thread): dP^T, dK and dQ.
+//   warp 1       TMEM allocator; MMA issuer A (one thread): dV and dQ.
+//   warp 14      MMA issuer B (one thread): dP^T and dK.
 //   warp 15      MMA issuer C (one thread): S^T.
 //   warps 2..9   two score warpgroups: thread = key row (TMEM lane); the
 //                first takes query columns 0..63, the second 64..127; P^T to
@@ -33,9 +33,10 @@
 //                step's dS^T buffer, free once the dQ product has read it) ->
 //                two TMA bulk reduce-adds (f32) into the global accumulator.
 // MMA issue order: once the score warpgroups finish step n, dV += P^T_n dO_n
-// (A) and dK += dS^T_n Q_n (B) run side by side, then dQ_n = dS_n K (B, after
-// dV_n has read its operand); S^T_{n+2} (C) follows as soon as the dQ of step
-// n has been read out, and dP^T_{n+2} (B) as soon as the score warpgroups of
+// (A) and dK += dS^T_n Q_n (B) run side by side, both taking queries 64..127
+// first, then dQ_n = dS_n K (A, once dK_n has read those queries, whose
+// columns dQ_n overwrites); S^T_{n+2} (C) follows as soon as the dQ of step n
+// has been read out, and dP^T_{n+2} (B) as soon as the score warpgroups of
 // step n+1 have read their dP^T.  The scores of the next step are thus
 // computed while the score warpgroups still work on the current one.
 // TMEM (d = 64, 512 columns): two step regions of 128 columns (S^T f32; each
@@ -72,7 +73,7 @@ struct BwdLayout {
   static constexpr int kStatBytes = 2 * kTile * 4;
   static constexpr int kOffBar = kOffStats + 2 * kStatBytes;
   // kv_full, qdo_full[], qdo_empty[], sdp_full[2], ps_ready[2], dp_free, dq_full[2], dq_free[2],
-  // dq_staged, ds_free[3], epi, drain, dv_done[2]
+  // dq_staged, ds_free[3], epi, drain, dk_hi[2]
   static constexpr int kNumBars = 1 + 2 * kStages + 18;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // no room to round the dynamic shared memory base up to the 1 KB alignment
@@ -137,7 +138,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* ds_free = dq_staged + 1;  // ds_free[n % 3]
   uint64_t* epi = ds_free + Lay::kDSBufs;
   uint64_t* drain = epi + 1;
-  uint64_t* dv_done = drain + 1;  // dv_done[n & 1]
+  uint64_t* dk_hi = drain + 1;  // dk_hi[n & 1]: dK_n has read queries 64..127
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
 
@@ -165,8 +166,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     for (int i = 0; i < Lay::kDSBufs; ++i) mbar_init(ds_free + i, 1);
     mbar_init(epi, 2);
     mbar_init(drain, 3);
-    mbar_init(dv_done, 1);
-    mbar_init(dv_done + 1, 1);
+    mbar_init(dk_hi, 1);
+    mbar_init(dk_hi + 1, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -254,7 +255,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // Three issuing threads, each with its own order of waits, so that no
     // product queues behind a wait that belongs to another (one thread also
     // starts an N = 64 product only about every 55 cycles, half the tensor
-    // core's rate for that shape).  A (warp 1): dV.  B: dK, dQ, dP^T.  C: S^T.
+    // core's rate for that shape).  A (warp 1): dV, dQ.  B: dK, dP^T.  C: S^T.
     if (lane == 0) {
       const int role = warp == 1 ? 0 : (warp == kWarpIssuerB ? 1 : 2);
       constexpr uint32_t id_sdp = idesc_bf16_f32(kTile, kTile, false, false);  // K-major x K-major
@@ -312,29 +313,31 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const uint32_t ya = smem_u32(role == 0 ? stage_do(st) : stage_q(st));
           const uint32_t acc = tmem + (role == 0 ? Lay::kColDV : Lay::kColDK);
           const uint32_t a0 = region(n) + (role == 0 ? 0 : 16);
+          // queries 64..127 first: their columns are where dQ_n goes
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
+          for (int j = 0; j < kTile / 16; ++j) {
+            const int kk = (j + 4) % 8;
             umma_ts(acc, a0 + 64 * (kk / 4) + 32 * ((kk % 4) / 2) + 8 * (kk % 2),
-                    sdesc_sw128(ya + kk * 2048, Lay::kChunkBytes, 1024), id_dvk, (n > 0 || kk > 0));
-          if (role == 0) umma_commit(dv_done + (n & 1));
-          umma_commit(qdo_empty + st);
-          if (role == 1) {
-            if (DQ) {
-              // dQ_n = dS K into the step region of n, once dV_n has read the
-              // P^T there (dK_n, issued above by this thread, comes first
-              // anyway); its dQ_{n-2} was read before S^T_n was issued  (A: the
-              // dS^T tile read query-major, MN-major; B: K, MN-major)
-              if (!(ok = mbar_wait(dv_done + (n & 1), (n >> 1) & 1, abort_flag))) break;
-              tc_fence_after();
-              const uint32_t dsb = sDSa + (n % Lay::kDSBufs) * Lay::kDSBytes;
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
-                        sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
-              umma_commit(dq_full + (n & 1));
-            }
-            if (n + 2 < nsteps && !(ok = issue_next(n + 2))) break;
+                    sdesc_sw128(ya + kk * 2048, Lay::kChunkBytes, 1024), id_dvk, (n > 0 || j > 0));
+            if (role == 1 && j == 3) umma_commit(dk_hi + (n & 1));  // dK has read queries 64..127
           }
+          umma_commit(qdo_empty + st);
+          if (role == 0 && DQ) {
+            // dQ_n = dS K into columns 64..127 of the step region of n, once
+            // dV_n (above, this thread) and the first half of dK_n (thread B)
+            // have read the P^T / dS^T there; its dQ_{n-2} was read before
+            // S^T_n was issued  (A: the dS^T tile read query-major, MN-major;
+            // B: K, MN-major)
+            if (!(ok = mbar_wait(dk_hi + (n & 1), (n >> 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t dsb = sDSa + (n % Lay::kDSBufs) * Lay::kDSBytes;
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
+                      sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
+            umma_commit(dq_full + (n & 1));
+          }
+          if (role == 1 && n + 2 < nsteps && !(ok = issue_next(n + 2))) break;
         }
         if (ok) umma_commit(epi);
       }
