@@ -69,13 +69,19 @@ struct FwdLayout {
   static constexpr int kOffL = kOffX + 2 * 2 * kTile * 4;      // final row-sum exchange [2 parity][2 halves][128]
   static constexpr int kOffBar = kOffL + 2 * 2 * kTile * 4;
   static constexpr int kSBufs = 3;
+  // d = 64: the two softmax warpgroups keep separate statistics for their key
+  // halves and P V accumulates each half in its own O (TMEM has room for two
+  // 64-column accumulators next to the three score buffers); the halves are
+  // merged once per unit.  d = 128: one O, statistics exchanged per key tile.
+  static constexpr bool kSplit = D == 64;
+  static constexpr int kThreads = kSplit ? 416 : 384;  // warp 12: second P V issuer
   // q_full[2], q_empty[2], k_full[], k_empty[], v_full[], v_empty[], s_full[3], s_free[3],
-  // p_full[3], pv_done[2], xchg, o_final, o_free, drain
-  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 3 * kSBufs + 2 + 4;
+  // p_full[2][3], pv_done[2][2], xchg, o_final, o_free, drain
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 4 * kSBufs + 4 + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColO = 384;
+  static constexpr uint32_t kColS = 0, kColO = 384, kColO1 = 448;  // kColO1: second half's O (d = 64)
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -83,7 +89,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // P values stay below 2^8 between rescales
 
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(FwdLayout<D>::kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Lay = FwdLayout<D>;
@@ -140,9 +146,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   constexpr int NB = Lay::kSBufs;
   uint64_t* s_full = v_empty + NV;
   uint64_t* s_free = s_full + NB;
-  uint64_t* p_full = s_free + NB;
-  uint64_t* pv_done = p_full + NB;  // two, alternating by key-tile parity
-  uint64_t* xchg = pv_done + 2;
+  uint64_t* p_full = s_free + NB;   // [half (split) or 0][buffer]
+  uint64_t* pv_done = p_full + 2 * NB;  // [half (split) or 0][key-tile parity]
+  uint64_t* xchg = pv_done + 4;
   uint64_t* o_final = xchg + 1;
   uint64_t* o_free = o_final + 1;
   uint64_t* drain = o_free + 1;
@@ -154,13 +160,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) { mbar_init(q_full + i, 1); mbar_init(q_empty + i, 1); }
     for (int i = 0; i < NK; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
-    for (int i = 0; i < NV; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1); }
-    for (int i = 0; i < NB; ++i) { mbar_init(s_full + i, 1); mbar_init(s_free + i, 1); mbar_init(p_full + i, 256); }
-    for (int i = 0; i < 2; ++i) mbar_init(pv_done + i, 1);
+    // split: both P V issuers release score buffers and V stages and finish O
+    constexpr uint32_t npv = Lay::kSplit ? 2 : 1;
+    for (int i = 0; i < NV; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, npv); }
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(s_free + i, npv);
+      mbar_init(p_full + i, Lay::kSplit ? 128 : 256);
+      mbar_init(p_full + NB + i, 128);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(pv_done + i, 1);
     mbar_init(xchg, 256);
-    mbar_init(o_final, 1);
+    mbar_init(o_final, npv);
     mbar_init(o_free, 256);
-    mbar_init(drain, 2);
+    mbar_init(drain, npv + 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -273,9 +286,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int never = 0;
       mbar_wait(drain, 0, &never);
     }
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ P V issuer
+  } else if (warp == 2 || (Lay::kSplit && warp == 12)) {
+    // ------------------------------------------------------------ P V issuer(s)
+    // split: warp 2 accumulates keys 0..63 of every tile into O, warp 12 keys
+    // 64..127 into O1 (two threads also keep two N = 64 products in flight)
     if (lane == 0) {
+      const int hv = warp == 2 ? 0 : 1;
       constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, false, true);
       const uint64_t v_desc = sdesc_sw128(smem_u32(sV), Lay::kChunkBytes, 1024);
       int g = 0, uc = 0;  // score tiles and units so far
@@ -288,18 +304,26 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         ++uc;
         for (int j = 0; j < w.nkv; ++j, ++g) {
           const int b = g % NB, vs = g % NV;
-          if (!(ok = mbar_wait(p_full + b, (g / NB) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(p_full + hv * NB + b, (g / NB) & 1, abort_flag))) break;
           if (!(ok = mbar_wait(v_full + vs, (g / NV) & 1, abort_flag))) break;
           tc_fence_after();
           const uint64_t vd = v_desc + static_cast<uint64_t>((vs * Lay::kTileBytes) >> 4);
           const uint32_t a_tm = tmem + Lay::kColS + b * kTile;  // P, bf16 pairs
+          if constexpr (Lay::kSplit) {
+            // P of keys 64 hv .. 64 hv + 63 sits in columns 64 hv .. 64 hv + 31
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ts(tmem + Lay::kColO, a_tm + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_o,
-                    (j > 0 || kk > 0));
+            for (int kk = 0; kk < kTile / 32; ++kk)
+              umma_ts(tmem + (hv ? Lay::kColO1 : Lay::kColO), a_tm + 64 * hv + kk * 8,
+                      vd + static_cast<uint64_t>(((4 * hv + kk) * 2048) >> 4), idesc_o, (j > 0 || kk > 0));
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_ts(tmem + Lay::kColO, a_tm + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_o,
+                      (j > 0 || kk > 0));
+          }
           umma_commit(s_free + b);
           umma_commit(v_empty + vs);
-          umma_commit(pv_done + (g & 1));
+          umma_commit(pv_done + 2 * hv + (g & 1));
         }
         if (ok) umma_commit(o_final);
       }
@@ -308,7 +332,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int never = 0;
       mbar_wait(drain, 0, &never);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax
     const int half = (warp - 4) / 4;  // key columns [64 * half, 64 * half + 64)
     const int quad = warp & 3;
@@ -344,13 +368,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
           for (int t = 0; t < 4; ++t) mx[t] = max3(mx[t], x[i + 2 * t], x[i + 2 * t + 1]);
         }
-        // exchange the partial row max with the other half (double-buffered by phase)
-        float* xm = xmax + ((xp & 1) * 2) * kTile;
-        xm[half * kTile + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        mbar_arrive(xchg);
-        if (!(ok = mbar_wait(xchg, xp & 1, abort_flag))) break;
-        ++xp;
-        const float mt = fmaxf(xm[r], xm[kTile + r]) * c;
+        float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        if constexpr (!Lay::kSplit) {
+          // exchange the partial row max with the other half (double-buffered by phase)
+          float* xm = xmax + ((xp & 1) * 2) * kTile;
+          xm[half * kTile + r] = mt;
+          mbar_arrive(xchg);
+          if (!(ok = mbar_wait(xchg, xp & 1, abort_flag))) break;
+          ++xp;
+          mt = fmaxf(xm[r], xm[kTile + r]);
+        }
+        mt *= c;
         // move the reference only when the row max grows past the slack
         const bool bump = mt > m + kRescaleSlack;
         const float m_new = bump ? mt : m;
@@ -369,9 +397,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             sum2[t & 3] = add2(sum2[t & 3], pv);
             pk[t] = pack_bf16x2(pv.x, pv.y);
           }
-          // P for keys [64 half + 32 cc, +32) goes to columns [32 half + 16 cc, +16);
-          // every thread of both halves read its scores before the exchange above.
-          tmem_st_x16(tmem_addr(tS, lane_base, half * 32 + cc * 16), pk);
+          // P for keys [64 half + 32 cc, +32) goes to columns [32 half + 16 cc, +16)
+          // (every thread of both halves read its scores before the exchange
+          // above), or, split, to [64 half + 16 cc, +16): columns this
+          // thread has read itself.
+          tmem_st_x16(tmem_addr(tS, lane_base, (Lay::kSplit ? 64 : 32) * half + cc * 16), pk);
         }
         const float2 s01 = add2(sum2[0], sum2[1]), s23 = add2(sum2[2], sum2[3]);
         l = l * alpha + ((s01.x + s01.y) + (s23.x + s23.y));
@@ -380,12 +410,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           // O may only be rescaled once P V of the previous key tile has landed
           // (P V of tile g-NB is done, so the barrier of tile g-1's parity is at
           // most one phase behind: its parity identifies the phase)
-          if (!(ok = mbar_wait(pv_done + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag))) break;
+          const int ph = Lay::kSplit ? half : 0;
+          if (!(ok = mbar_wait(pv_done + 2 * ph + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag))) break;
           tc_fence_after();
+          // this half's columns of O, or, split, all of this half's O
 #pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc) {
+          for (int cc = 0; cc < (Lay::kSplit ? D / 32 : D / 64); ++cc) {
             uint32_t ov[32];
-            const uint32_t ta = tmem_addr(tmem + Lay::kColO, lane_base, half * (D / 2) + cc * 32);
+            const uint32_t ta = Lay::kSplit
+                                    ? tmem_addr(tmem + (half ? Lay::kColO1 : Lay::kColO), lane_base, cc * 32)
+                                    : tmem_addr(tmem + Lay::kColO, lane_base, half * (D / 2) + cc * 32);
             tmem_ld_x32(ta, ov);
 #pragma unroll
             for (int t = 0; t < 32; ++t) ov[t] = __float_as_uint(__uint_as_float(ov[t]) * alpha);
@@ -394,23 +428,46 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full + b);
+        mbar_arrive(p_full + (Lay::kSplit ? half * NB : 0) + b);
       }
       if (!ok) break;
       // ---- epilogue of this unit
       if (!(ok = mbar_wait(o_final, uc & 1, abort_flag))) break;
       ++uc;
-      // combine the two halves' row sums
+      // combine the two halves' row sums (split: and reference maxima)
       xsum[(xp & 1) * kTile * 2 + half * kTile + r] = l;
+      if constexpr (Lay::kSplit) xmax[(xp & 1) * kTile * 2 + half * kTile + r] = m;
       mbar_arrive(xchg);
       if (!(ok = mbar_wait(xchg, xp & 1, abort_flag))) break;
-      const float lt = xsum[(xp & 1) * kTile * 2 + r] + xsum[(xp & 1) * kTile * 2 + kTile + r];
+      const float l0 = xsum[(xp & 1) * kTile * 2 + r], l1 = xsum[(xp & 1) * kTile * 2 + kTile + r];
+      float lt, a0 = 1.f, a1 = 1.f;
+      if constexpr (Lay::kSplit) {
+        // O = (2^(m0 - m) O0 + 2^(m1 - m) O1) / (2^(m0 - m) l0 + 2^(m1 - m) l1)
+        const float m0 = xmax[(xp & 1) * kTile * 2 + r], m1 = xmax[(xp & 1) * kTile * 2 + kTile + r];
+        const float mm = fmaxf(m0, m1);
+        a0 = mm == -INFINITY ? 0.f : ex2_approx(m0 - mm);
+        a1 = mm == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+        lt = a0 * l0 + a1 * l1;
+        m = mm;
+      } else {
+        lt = l0 + l1;
+      }
       ++xp;
       tc_fence_after();
       uint32_t ov[D / 2];
+      if constexpr (Lay::kSplit) {
+        // this thread writes output columns [D/2 half, D/2 half + D/2) of its row
+        uint32_t ov1[D / 2];
+        tmem_ld_x32(tmem_addr(tmem + Lay::kColO, lane_base, half * (D / 2)), ov);
+        tmem_ld_x32(tmem_addr(tmem + Lay::kColO1, lane_base, half * (D / 2)), ov1);
 #pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc)
-        tmem_ld_x32(tmem_addr(tmem + Lay::kColO, lane_base, half * (D / 2) + cc * 32), ov + 32 * cc);
+        for (int t = 0; t < D / 2; ++t)
+          ov[t] = __float_as_uint(__uint_as_float(ov[t]) * a0 + __uint_as_float(ov1[t]) * a1);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc)
+          tmem_ld_x32(tmem_addr(tmem + Lay::kColO, lane_base, half * (D / 2) + cc * 32), ov + 32 * cc);
+      }
       // O is in registers: the next unit's P V may start overwriting it
       tc_fence_before();
       mbar_arrive(o_free);
@@ -517,7 +574,7 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   const int grid = static_cast<int>(units < sms ? units : sms);  // one CTA per SM, persistent
   FwdParams q = p;
   q.group_pairs = choose_group_pairs(p, grid, D);
-  fa_fwd_kernel<D><<<grid, 384, Lay::kBytes, stream>>>(tq, tk, tv, q);
+  fa_fwd_kernel<D><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tq, tk, tv, q);
   return cudaGetLastError();
 }
 
