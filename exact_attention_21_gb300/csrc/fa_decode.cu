@@ -113,48 +113,41 @@ __device__ __forceinline__ long long decode_row(const DecodeParams& p, int b, lo
 }
 
 // TMA loads of the K and V tile of logical keys k0 .. k0 + 127 of sequence b
-// (K/V head g): CHUNKS boxes of 64 (16-bit) or 128 (8-bit) columns per tile,
-// each CHUNK_BYTES apart in shared memory; paged caches take one box of
-// page_size rows per page (1 KB-aligned in shared memory for page_size >= 8,
-// so the 128-byte swizzle pattern continues across boxes).
+// (K/V head g), issued by the 32 lanes of the calling warp: CHUNKS boxes of
+// 64 (16-bit) or 128 (8-bit) columns per tile, each CHUNK_BYTES apart in
+// shared memory; paged caches take one box of page_size rows per page (1
+// KB-aligned in shared memory for page_size >= 8, so the 128-byte swizzle
+// pattern continues across boxes), lane j copying page j: a tile of small
+// pages is many copies, and one warp instruction issues one per lane.
+// Returns false for a table entry outside the pool (page 0 is read instead,
+// and the status bit is set).
 template <int CHUNKS, int CHUNK_BYTES, int COLS>
 __device__ __forceinline__ void load_kv_tile(const DecodeParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                              uint8_t* dst_k, uint8_t* dst_v, uint64_t* bar, int b, int g,
-                                             long long seq0, int k0, int L) {
+                                             long long seq0, int k0, int L, int lane) {
   if (p.block_table == nullptr) {
-    const int row = static_cast<int>(seq0 + k0);
-    for (int c = 0; c < CHUNKS; ++c) {
-      tma_load_3d(dst_k + c * CHUNK_BYTES, tm_k, bar, c * COLS, g, row);
-      tma_load_3d(dst_v + c * CHUNK_BYTES, tm_v, bar, c * COLS, g, row);
+    // lane c: K box c; lane CHUNKS + c: V box c
+    if (lane < 2 * CHUNKS) {
+      const int c = lane % CHUNKS;
+      const bool is_v = lane >= CHUNKS;
+      tma_load_3d((is_v ? dst_v : dst_k) + c * CHUNK_BYTES, is_v ? tm_v : tm_k, bar, c * COLS, g,
+                  static_cast<int>(seq0 + k0));
     }
     return;
   }
-  // the tile's table entries are read together first: the copies below are
-  // ordered memory operations, and reading each entry right before its copy
-  // would pay one load latency per page
   const int ps = p.page_size;
-  const int np = kTile / ps;
-  const int* entries = p.block_table + static_cast<long long>(b) * p.max_pages + k0 / ps;
-  int phys[kTile / 8];
-#pragma unroll
-  for (int j = 0; j < kTile / 8; ++j)  // plain loads only, so they can all be in flight at once
-    phys[j] = (j < np && (k0 / ps + j) * ps < L) ? __ldg(entries + j) : 0;
-  bool bad = false;
-#pragma unroll
-  for (int j = 0; j < kTile / 8; ++j) {
-    const bool out = phys[j] < 0 || phys[j] >= p.num_pages;  // see decode_page
-    bad |= out;
-    phys[j] = out ? 0 : phys[j];
-  }
-  if (bad) atomicOr(p.status, kStatusBadOffsets);
-#pragma unroll
-  for (int j = 0; j < kTile / 8; ++j) {
-    if (j < np) {
-      const int row = phys[j] * ps;
-      for (int c = 0; c < CHUNKS; ++c) {
-        tma_load_3d(dst_k + c * CHUNK_BYTES + j * ps * 128, tm_k, bar, c * COLS, g, row);
-        tma_load_3d(dst_v + c * CHUNK_BYTES + j * ps * 128, tm_v, bar, c * COLS, g, row);
-      }
+  const int j = lane;  // page of the tile
+  if (j < kTile / ps) {
+    const int lp = k0 / ps + j;
+    int phys = lp * ps < L ? __ldg(p.block_table + static_cast<long long>(b) * p.max_pages + lp) : 0;
+    if (phys < 0 || phys >= p.num_pages) {  // see decode_page
+      atomicOr(p.status, kStatusBadOffsets);
+      phys = 0;
+    }
+    const int row = phys * ps;
+    for (int c = 0; c < CHUNKS; ++c) {
+      tma_load_3d(dst_k + c * CHUNK_BYTES + j * ps * 128, tm_k, bar, c * COLS, g, row);
+      tma_load_3d(dst_v + c * CHUNK_BYTES + j * ps * 128, tm_v, bar, c * COLS, g, row);
     }
   }
 }
@@ -199,20 +192,26 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (one warp)
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int issued = 0;
-      bool ok = true;
-      for (int i = 0; i < nt; ++i) {
-        const int st = i % NS;
-        if (i >= NS && !(ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag))) break;
-        mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
-        load_kv_tile<D / 64, Lay::kChunkBytes, 64>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTileBytes, full + st,
-                                                   b, g, seq0, (t0 + i) * kTile, L);
-        ++issued;
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int i = 0; i < nt; ++i) {
+      const int st = i % NS;
+      // lane 0 waits for the stage and posts the byte count before any copy
+      if (lane == 0) {
+        if (i >= NS) ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag);
+        if (ok) mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
       }
+      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+      load_kv_tile<D / 64, Lay::kChunkBytes, 64>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTileBytes, full + st,
+                                                 b, g, seq0, (t0 + i) * kTile, L, lane);
+      ++issued;
+    }
+    if (lane == 0) {
       if (!ok) give_up();
       // no TMA write may still be in flight when the CTA exits
       int never = 0;
@@ -571,25 +570,31 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (one warp)
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int issued = 0;
-      bool ok = true;
-      for (int i = 0; i < nt; ++i) {
-        const int st = i % NS;
-        if (i >= NS && !(ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag))) break;
-        mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
-        if constexpr (FP8) {
-          load_kv_tile<1, Lay::kTile8Bytes, 128>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTile8Bytes, full + st, b,
-                                                  g, seq0, (t0 + i) * kTile, L);
-        } else {
-          load_kv_tile<2, Lay::kChunkBytes, 64>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTileBytes, full + st, b,
-                                                 g, seq0, (t0 + i) * kTile, L);
-        }
-        ++issued;
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int i = 0; i < nt; ++i) {
+      const int st = i % NS;
+      // lane 0 waits for the stage and posts the byte count before any copy
+      if (lane == 0) {
+        if (i >= NS) ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag);
+        if (ok) mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
       }
+      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+      if constexpr (FP8) {
+        load_kv_tile<1, Lay::kTile8Bytes, 128>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTile8Bytes, full + st, b,
+                                                g, seq0, (t0 + i) * kTile, L, lane);
+      } else {
+        load_kv_tile<2, Lay::kChunkBytes, 64>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTileBytes, full + st, b,
+                                               g, seq0, (t0 + i) * kTile, L, lane);
+      }
+      ++issued;
+    }
+    if (lane == 0) {
       if (!ok) give_up();
       // no TMA write may still be in flight when the CTA exits
       int never = 0;
