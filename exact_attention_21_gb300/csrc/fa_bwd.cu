@@ -277,16 +277,18 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         umma_commit(sdp_full + (m & 1));
       };
       // S^T_m needs the Q stage of step m and the step region of m-2: its dQ
-      // read out, or (no dQ) its dV and dK products done.  dP^T_m needs the
+      // read out and its dV and dK products done.  dP^T_m needs the
       // dO stage and the dP^T region, which the score warpgroups of step m-1
       // release (dp_free) once their dP^T loads are done.
       auto issue_next = [&](int m) -> bool {
         if (!mbar_wait(qdo_full + m % NS, (m / NS) & 1, abort_flag)) return false;
         if (role == 2 && m >= 2) {
           const int r = m - 2;
-          if (DQ ? !mbar_wait(dq_free + (r & 1), (r >> 1) & 1, abort_flag)
-                 : !mbar_wait(qdo_empty + r % NS, (r / NS) & 1, abort_flag))
-            return false;
+          if (DQ && !mbar_wait(dq_free + (r & 1), (r >> 1) & 1, abort_flag)) return false;
+          // dV and dK of step m-2 are done with the region too (thread B's dK
+          // has no order with respect to thread A's dQ, so dq_free alone does
+          // not cover it)
+          if (!mbar_wait(qdo_empty + r % NS, (r / NS) & 1, abort_flag)) return false;
         }
         if (role == 1 && m >= 1 && !mbar_wait(dp_free, (m - 1) & 1, abort_flag)) return false;
         tc_fence_after();
