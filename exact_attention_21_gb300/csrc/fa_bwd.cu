@@ -17,18 +17,24 @@
 // below for d = 64, fa_bwd128_kernel in fa_bwd128.cu for d = 128),
 // fa_bwd_dq_kernel (dQ accumulator -> bf16).
 //
-// fa_bwd_kernel: one CTA per (key tile j, K/V head, sequence); it walks the
-// query heads of the group and their query tiles ("steps"), so dK and dV of
-// the group accumulate in TMEM with no atomics.  Warp roles:
-//   warp 0       producer: K_j, V_j once (TMA); per step Q_i, dO_i (TMA) and
-//                the LSE / D values of the tile (plain loads) into a 3-stage ring.
+// fa_bwd_kernel: persistent, one CTA per SM walking work units (key tile j,
+// K/V head, sequence), heaviest first; per unit it walks the query heads of
+// the group and their query tiles ("steps"), so dK and dV of the group
+// accumulate in TMEM with no atomics.  Steps are counted across units, so
+// the rings and the step-parity barriers run on from one unit to the next
+// and the next unit's first products start while the last one drains.
+// Warp roles:
+//   warp 0       producer: per step Q_i, dO_i (TMA) and the LSE / D values of
+//                the tile (plain loads) into a 3-stage ring.
 //   warp 1       TMEM allocator; MMA issuer A (one thread): dV and dQ.
 //   warp 14      MMA issuer B (one thread): dP^T and dK.
-//   warp 15      MMA issuer C (one thread): S^T.
+//   warp 15      MMA issuer C (one thread): K_j, V_j of each unit (TMA, once
+//                every product of the previous unit that reads them is done)
+//                and S^T.
 //   warps 2..9   two score warpgroups: thread = key row (TMEM lane); the
 //                first takes query columns 0..63, the second 64..127; P^T to
-//                TMEM (bf16), dS^T to TMEM and (for dQ) shared memory; dV / dK
-//                epilogue.
+//                TMEM (bf16), dS^T to TMEM and (for dQ) shared memory; the
+//                unit's dV / dK epilogue.
 //   warps 10..13 dQ warpgroup: dQ tile TMEM -> swizzled shared memory (the
 //                step's dS^T buffer, free once the dQ product has read it) ->
 //                two TMA bulk reduce-adds (f32) into the global accumulator.
@@ -36,16 +42,17 @@
 // (A) and dK += dS^T_n Q_n (B) run side by side, both taking queries 64..127
 // first, then dQ_n = dS_n K (A, once dK_n has read those queries, whose
 // columns dQ_n overwrites); S^T_{n+2} (C) follows as soon as the dQ of step n
-// has been read out, and dP^T_{n+2} (B) as soon as the score warpgroups of
-// step n+1 have read their dP^T.  The scores of the next step are thus
-// computed while the score warpgroups still work on the current one.
+// has been read out and dV_n, dK_n are done, and dP^T_{n+2} (B) as soon as
+// the score warpgroups of step n+1 have read their dP^T.  The scores of the
+// next step are thus computed while the score warpgroups still work on the
+// current one.
 // TMEM (d = 64, 512 columns): two step regions of 128 columns (S^T f32; each
-// 32-column chunk of S^T, once read, takes the bf16 P^T of its 32 queries in
-// its first 16 columns and their bf16 dS^T in the last 16, so dV and dK both
+// 16-column chunk of S^T, once read, takes the bf16 P^T of its 16 queries in
+// its first 8 columns and their bf16 dS^T in the last 8, so dV and dK both
 // take their A operand from TMEM; dQ f32 over columns 64..127, written by an
 // MMA issued after the dV and dK products that read them),
 // dP^T [256, 384), dV [384, 448), dK [448, 512).  dS^T also goes to shared
-// memory (double-buffered) as the MN-major A operand of dQ (rows = queries).
+// memory (three buffers) as the MN-major A operand of dQ (rows = queries).
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
@@ -73,8 +80,8 @@ struct BwdLayout {
   static constexpr int kStatBytes = 2 * kTile * 4;
   static constexpr int kOffBar = kOffStats + 2 * kStatBytes;
   // kv_full, qdo_full[], qdo_empty[], sdp_full[2], ps_ready[2], dp_free, dq_full[2], dq_free[2],
-  // dq_staged, ds_free[3], epi, drain, dk_hi[2]
-  static constexpr int kNumBars = 1 + 2 * kStages + 18;
+  // dq_staged, ds_free[3], epi, drain, dk_hi[2], kv_free, acc_free
+  static constexpr int kNumBars = 1 + 2 * kStages + 20;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // no room to round the dynamic shared memory base up to the 1 KB alignment
   // of the 128-byte swizzle: the kernel requires an aligned base (it is, with
@@ -100,20 +107,38 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using Lay = BwdLayout<D>;
   constexpr int NS = Lay::kStages;
-
-  const int g = blockIdx.x;  // K/V head
-  const int kt = blockIdx.y;
-  const int s = blockIdx.z;
-  long long seq0;
-  int L;
-  if (!sequence_bounds(p.cu, s, p.N, p.T, seq0, L, p.status)) return;
-  const int k0 = kt * kTile;
-  if (k0 >= L) return;
   const bool causal = p.causal != 0;
-  const int nqt = (L + kTile - 1) / kTile;
-  const int i0 = first_q_tile_for(kt, causal);
-  const int per_head = nqt - i0;
-  const int nsteps = p.group * per_head;
+
+  // Persistent: work units (128-key tile, K/V head, sequence), key tile
+  // outermost so the causal work goes heaviest first; CTA i takes the units
+  // i, 2G-1-i, 2G+i, ... (G = grid size).  Every role walks the same units
+  // and counts steps globally, so the step-indexed barriers and buffers run
+  // on across units; units past the end of their sequence are skipped by
+  // every role alike.
+  const int n_units = p.n_kvtiles * p.B * p.Hkv;
+  const int G = static_cast<int>(gridDim.x);
+  auto unit_of = [&](int k) {
+    return k * G + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+  };
+  struct Unit {
+    long long seq0;
+    int L, g, k0, i0, per_head, nsteps;
+  };
+  auto unit_at = [&](int u, Unit& w) -> bool {
+    w.g = u % p.Hkv;
+    const int rest = u / p.Hkv;
+    const int kt = rest / p.B;
+    if (!sequence_bounds(p.cu, rest % p.B, p.N, p.T, w.seq0, w.L, p.status)) return false;
+    w.k0 = kt * kTile;
+    if (w.k0 >= w.L) return false;
+    w.i0 = first_q_tile_for(kt, causal);
+    w.per_head = (w.L + kTile - 1) / kTile - w.i0;
+    w.nsteps = p.group * w.per_head;
+    return true;
+  };
+  // local step nl of unit w -> (query head, query tile)
+  auto step_head = [&](const Unit& w, int nl) { return w.g * p.group + nl / w.per_head; };
+  auto step_qtile = [&](const Unit& w, int nl) { return w.i0 + nl % w.per_head; };
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
@@ -139,6 +164,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* epi = ds_free + Lay::kDSBufs;
   uint64_t* drain = epi + 1;
   uint64_t* dk_hi = drain + 1;  // dk_hi[n & 1]: dK_n has read queries 64..127
+  uint64_t* kv_free = dk_hi + 2;   // the unit's K / V tiles have been read by every product
+  uint64_t* acc_free = kv_free + 1;  // the unit's dV / dK have been read out of TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
 
@@ -168,6 +195,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(drain, 3);
     mbar_init(dk_hi, 1);
     mbar_init(dk_hi + 1, 1);
+    mbar_init(kv_free, 3);   // the three MMA threads, once per unit
+    mbar_init(acc_free, 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -183,70 +212,70 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     atomicOr(p.status, kStatusTimeout);
     *abort_flag = 1;
   };
-  // step n -> (query head, query tile)
-  auto step_head = [&](int n) { return g * p.group + n / per_head; };
-  auto step_qtile = [&](int n) { return i0 + n % per_head; };
   auto region = [&](int n) { return tmem + Lay::kColStep + static_cast<uint32_t>(n & 1) * 128; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Q_i, dO_i (TMA) and the LSE / D values of every step; K_j, V_j are
+    // loaded by thread C, the first to need them.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_dq);
-      mbar_arrive_expect_tx(kv_full, 2 * Lay::kTileBytes);
-      for (int c = 0; c < Lay::kChunks; ++c) {
-        tma_load_3d(sK + c * Lay::kChunkBytes, &tm_k, kv_full, c * 64, g, static_cast<int>(seq0 + k0));
-        tma_load_3d(sV + c * Lay::kChunkBytes, &tm_v, kv_full, c * 64, g, static_cast<int>(seq0 + k0));
-      }
     }
     int uses[NS] = {};
     bool ok = true;
-    for (int n = 0; n < nsteps; ++n) {
-      const int st = n % NS;
-      if (n >= NS && !(ok = mbar_wait(qdo_empty + st, ((n / NS) - 1) & 1, abort_flag))) break;
-      const int h = step_head(n), q0 = step_qtile(n) * kTile;
-      if (lane == 0) {
-        mbar_expect_tx(qdo_full + st, 2 * Lay::kTileBytes);
-        const int row = static_cast<int>(seq0 + q0);
-        for (int c = 0; c < Lay::kChunks; ++c) {
-          tma_load_3d(stage_q(st) + c * Lay::kChunkBytes, &tm_q, qdo_full + st, c * 64, h, row);
-          tma_load_3d(stage_do(st) + c * Lay::kChunkBytes, &tm_do, qdo_full + st, c * 64, h, row);
+    int n = 0;  // steps so far
+    for (int k = 0, un = unit_of(0); un < n_units && ok; un = unit_of(++k)) {
+      Unit w;
+      if (!unit_at(un, w)) continue;
+      for (int nl = 0; nl < w.nsteps; ++nl, ++n) {
+        const int st = n % NS;
+        if (n >= NS &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(qdo_empty + st, ((n / NS) - 1) & 1, abort_flag))))
+          break;
+        const int h = step_head(w, nl), q0 = step_qtile(w, nl) * kTile;
+        if (lane == 0) {
+          mbar_expect_tx(qdo_full + st, 2 * Lay::kTileBytes);
+          const int row = static_cast<int>(w.seq0 + q0);
+          for (int c = 0; c < Lay::kChunks; ++c) {
+            tma_load_3d(stage_q(st) + c * Lay::kChunkBytes, &tm_q, qdo_full + st, c * 64, h, row);
+            tma_load_3d(stage_do(st) + c * Lay::kChunkBytes, &tm_do, qdo_full + st, c * 64, h, row);
+          }
         }
-      }
-      const long long lrow = static_cast<long long>(h) * p.T + seq0 + q0;
-      float lv[kTile / 32], dv[kTile / 32];
-#pragma unroll
-      for (int t = 0; t < kTile / 32; ++t) {
-        const int idx = lane + 32 * t;
-        const bool valid = q0 + idx < L;
-        lv[t] = valid ? __ldg(p.lse + lrow + idx) : INFINITY;
-        dv[t] = valid ? __ldg(p.rowdot + lrow + idx) : 0.f;
-      }
-      // the stats slot of this step parity: the score warpgroups are done
-      // with step n - 2 (on a failed wait the stage still completes, so the
-      // drain below covers the loads already issued)
-      if (n >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(ps_ready + (n & 1), ((n - 2) >> 1) & 1, abort_flag));
-      if (ok) {
-        float* stats = step_stats(n);
+        const long long lrow = static_cast<long long>(h) * p.T + w.seq0 + q0;
+        float lv[kTile / 32], dv[kTile / 32];
 #pragma unroll
         for (int t = 0; t < kTile / 32; ++t) {
-          // stored negated: -LSE * log2 e and -D (queries past the end: P = 0)
-          stats[lane + 32 * t] = -lv[t] * kLog2e;
-          stats[kTile + lane + 32 * t] = -dv[t];
+          const int idx = lane + 32 * t;
+          const bool valid = q0 + idx < w.L;
+          lv[t] = valid ? __ldg(p.lse + lrow + idx) : INFINITY;
+          dv[t] = valid ? __ldg(p.rowdot + lrow + idx) : 0.f;
         }
+        // the stats slot of this step parity: the score warpgroups are done
+        // with step n - 2 (on a failed wait the stage still completes, so the
+        // drain below covers the loads already issued)
+        if (n >= 2)
+          ok = __all_sync(0xffffffffu, mbar_wait(ps_ready + (n & 1), ((n - 2) >> 1) & 1, abort_flag));
+        if (ok) {
+          float* stats = step_stats(n);
+#pragma unroll
+          for (int t = 0; t < kTile / 32; ++t) {
+            // stored negated: -LSE * log2 e and -D (queries past the end: P = 0)
+            stats[lane + 32 * t] = -lv[t] * kLog2e;
+            stats[kTile + lane + 32 * t] = -dv[t];
+          }
+        }
+        mbar_arrive(qdo_full + st);
+        ++uses[st];
+        if (!ok) break;
       }
-      mbar_arrive(qdo_full + st);
-      ++uses[st];
-      if (!ok) break;
     }
     if (!ok && lane == 0) give_up();
     if (lane == 0) {
       int never = 0;
-      mbar_wait(kv_full, 0, &never);
       for (int i = 0; i < NS; ++i)
         if (uses[i]) mbar_wait(qdo_full + i, (uses[i] - 1) & 1, &never);
     }
@@ -295,53 +324,82 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         issue_score(m);
         return true;
       };
-      bool ok = mbar_wait(kv_full, 0, abort_flag);
-      tc_fence_after();
-      if (role == 2) {
-        for (int m = 0; m < nsteps && ok; ++m) ok = issue_next(m);
-      } else {
-        if (ok && role == 1) ok = issue_next(0);
-        if (ok && role == 1 && nsteps > 1) ok = issue_next(1);
-        for (int n = 0; n < nsteps && ok; ++n) {
-          const int st = n % NS;
-          // Score warpgroups may finish step n + 1 before this thread looks at
-          // step n, so each step parity has its own barrier: step n + 2 cannot
-          // start before its S^T and dP^T are issued.
-          if (!(ok = mbar_wait(ps_ready + (n & 1), (n >> 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          // dV += P^T dO (A) or dK += dS^T Q (B)  (A operand: P^T or dS^T in
-          // TMEM, queries 16 kk .. 16 kk + 15 at the columns the score
-          // warpgroups chose; B operand: dO or Q, rows = queries = K, MN-major)
-          const uint32_t ya = smem_u32(role == 0 ? stage_do(st) : stage_q(st));
-          const uint32_t acc = tmem + (role == 0 ? Lay::kColDV : Lay::kColDK);
-          const uint32_t a0 = region(n) + (role == 0 ? 0 : 16);
-          // queries 64..127 first: their columns are where dQ_n goes
-#pragma unroll
-          for (int j = 0; j < kTile / 16; ++j) {
-            const int kk = (j + 4) % 8;
-            umma_ts(acc, a0 + 64 * (kk / 4) + 32 * ((kk % 4) / 2) + 8 * (kk % 2),
-                    sdesc_sw128(ya + kk * 2048, Lay::kChunkBytes, 1024), id_dvk, (n > 0 || j > 0));
-            if (role == 1 && j == 3) umma_commit(dk_hi + (n & 1));  // dK has read queries 64..127
+      bool ok = true;
+      int n0 = 0, uc = 0, kv_loads = 0;  // steps and units so far, K / V loads issued (C)
+      for (int k = 0, un = unit_of(0); un < n_units && ok; un = unit_of(++k)) {
+        Unit w;
+        if (!unit_at(un, w)) continue;
+        if (role == 2) {
+          // K_j, V_j of this unit, once every product of the previous unit
+          // that reads them is done
+          if (uc >= 1 && !(ok = mbar_wait(kv_free, (uc - 1) & 1, abort_flag))) break;
+          mbar_arrive_expect_tx(kv_full, 2 * Lay::kTileBytes);
+          for (int c = 0; c < Lay::kChunks; ++c) {
+            tma_load_3d(sK + c * Lay::kChunkBytes, &tm_k, kv_full, c * 64, w.g, static_cast<int>(w.seq0 + w.k0));
+            tma_load_3d(sV + c * Lay::kChunkBytes, &tm_v, kv_full, c * 64, w.g, static_cast<int>(w.seq0 + w.k0));
           }
-          umma_commit(qdo_empty + st);
-          if (role == 0 && DQ) {
-            // dQ_n = dS K into columns 64..127 of the step region of n, once
-            // dV_n (above, this thread) and the first half of dK_n (thread B)
-            // have read the P^T / dS^T there; its dQ_{n-2} was read before
-            // S^T_n was issued  (A: the dS^T tile read query-major, MN-major;
-            // B: K, MN-major)
-            if (!(ok = mbar_wait(dk_hi + (n & 1), (n >> 1) & 1, abort_flag))) break;
-            tc_fence_after();
-            const uint32_t dsb = sDSa + (n % Lay::kDSBufs) * Lay::kDSBytes;
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
-                      sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
-            umma_commit(dq_full + (n & 1));
-          }
-          if (role == 1 && n + 2 < nsteps && !(ok = issue_next(n + 2))) break;
+          ++kv_loads;
         }
-        if (ok) umma_commit(epi);
+        if ((role != 0 || DQ) && !(ok = mbar_wait(kv_full, uc & 1, abort_flag))) break;
+        tc_fence_after();
+        if (role == 2) {
+          for (int nl = 0; nl < w.nsteps && ok; ++nl) ok = issue_next(n0 + nl);
+        } else {
+          if (ok && role == 1) ok = issue_next(n0);
+          if (ok && role == 1 && w.nsteps > 1) ok = issue_next(n0 + 1);
+          for (int nl = 0; nl < w.nsteps && ok; ++nl) {
+            const int n = n0 + nl;
+            const int st = n % NS;
+            // Score warpgroups may finish step n + 1 before this thread looks at
+            // step n, so each step parity has its own barrier: step n + 2 cannot
+            // start before its S^T and dP^T are issued.
+            if (!(ok = mbar_wait(ps_ready + (n & 1), (n >> 1) & 1, abort_flag))) break;
+            // dV and dK of the previous unit have been read out before this
+            // unit's first products overwrite them
+            if (nl == 0 && uc >= 1 && !(ok = mbar_wait(acc_free, (uc - 1) & 1, abort_flag))) break;
+            tc_fence_after();
+            // dV += P^T dO (A) or dK += dS^T Q (B)  (A operand: P^T or dS^T in
+            // TMEM, queries 16 kk .. 16 kk + 15 at the columns the score
+            // warpgroups chose; B operand: dO or Q, rows = queries = K, MN-major)
+            const uint32_t ya = smem_u32(role == 0 ? stage_do(st) : stage_q(st));
+            const uint32_t acc = tmem + (role == 0 ? Lay::kColDV : Lay::kColDK);
+            const uint32_t a0 = region(n) + (role == 0 ? 0 : 8);
+            // queries 64..127 first: their columns are where dQ_n goes
+#pragma unroll
+            for (int j = 0; j < kTile / 16; ++j) {
+              const int kk = (j + 4) % 8;
+              umma_ts(acc, a0 + 16 * kk, sdesc_sw128(ya + kk * 2048, Lay::kChunkBytes, 1024), id_dvk,
+                      (nl > 0 || j > 0));
+              if (role == 1 && j == 3) umma_commit(dk_hi + (n & 1));  // dK has read queries 64..127
+            }
+            umma_commit(qdo_empty + st);
+            if (role == 0 && DQ) {
+              // dQ_n = dS K into columns 64..127 of the step region of n, once
+              // dV_n (above, this thread) and the first half of dK_n (thread B)
+              // have read the P^T / dS^T there; its dQ_{n-2} was read before
+              // S^T_n was issued  (A: the dS^T tile read query-major, MN-major;
+              // B: K, MN-major)
+              if (!(ok = mbar_wait(dk_hi + (n & 1), (n >> 1) & 1, abort_flag))) break;
+              tc_fence_after();
+              const uint32_t dsb = sDSa + (n % Lay::kDSBufs) * Lay::kDSBytes;
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                umma_ss(region(n) + Lay::kColDQ, sdesc_sw128(dsb + kk * 2048, Lay::kChunkBytes, 1024),
+                        sdesc_sw128(sKa + kk * 2048, Lay::kChunkBytes, 1024), id_dq, kk > 0);
+              umma_commit(dq_full + (n & 1));
+            }
+            if (role == 1 && nl + 2 < w.nsteps && !(ok = issue_next(n + 2))) break;
+          }
+          if (ok) umma_commit(epi);  // this unit's dV / dK are complete
+        }
+        if (ok) umma_commit(kv_free);  // this thread's products of the unit are done with K, V
+        n0 += w.nsteps;
+        ++uc;
+      }
+      if (role == 2 && kv_loads > 0) {
+        // no K / V copy may still be in flight when the CTA exits
+        int never = 0;
+        mbar_wait(kv_full, (kv_loads - 1) & 1, &never);
       }
       if (!ok) give_up();
       umma_commit(drain);
@@ -353,18 +411,24 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int half = (warp - 2) / 4;  // query columns [64 * half, 64 * half + 64)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // key row within the tile
-    const int kpos = k0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
-    const bool key_ok = kpos < L;
     bool ok = true;
-    for (int n = 0; n < nsteps; ++n) {
+    int n = 0, uc = 0;  // steps and units so far
+    for (int k = 0, un = unit_of(0); un < n_units && ok; un = unit_of(++k)) {
+    Unit w;
+    if (!unit_at(un, w)) continue;
+    const int k0 = w.k0, L = w.L;
+    const long long seq0 = w.seq0;
+    const int kpos = k0 + r;
+    const bool key_ok = kpos < L;
+    for (int nl = 0; nl < w.nsteps; ++nl, ++n) {
       const int st = n % NS;
       if (!(ok = mbar_wait(sdp_full + (n & 1), (n >> 1) & 1, abort_flag))) break;
       if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
       tc_fence_after();
-      const int q0 = step_qtile(n) * kTile;
+      const int q0 = step_qtile(w, nl) * kTile;
       const float2* nlse2 = reinterpret_cast<const float2*>(step_stats(n)) + half * 32;
       const float2* ndot2 = nlse2 + kTile / 2;
       // Keys past the sequence end and keys after the query (diagonal tile,
@@ -374,21 +438,21 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       uint8_t* ds_row = sDS + (n % Lay::kDSBufs) * Lay::kDSBytes + half * Lay::kChunkBytes + r * 128;
       const uint32_t reg = region(n);
 #pragma unroll
-      for (int cl = 0; cl < 2; ++cl) {
-        const int col0 = half * 64 + cl * 32;  // first query column of this chunk
-        uint32_t sv[32], dpv[32];
-        tmem_ld_x32_pair(tmem_addr(reg, lane_base, col0), sv, tmem_addr(tmem, lane_base, Lay::kColDP + col0), dpv);
-        if (cl == 1) {
+      for (int cl = 0; cl < 4; ++cl) {
+        const int col0 = half * 64 + cl * 16;  // first query column of this chunk
+        uint32_t sv[16], dpv[16];
+        tmem_ld_x16_pair(tmem_addr(reg, lane_base, col0), sv, tmem_addr(tmem, lane_base, Lay::kColDP + col0), dpv);
+        if (cl == 3) {
           // dP^T fully read: the next step's dP^T may overwrite it
           tc_fence_before();
           mbar_arrive(dp_free);
         }
-        uint32_t pk[16], dsk[16];
+        uint32_t pk[8], dsk[8];
         const bool mask_chunk = zero_below > col0;
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float2 nl = nlse2[cl * 16 + t], nd = ndot2[cl * 16 + t];
-          const float2 x = fma2(make_float2(__uint_as_float(sv[2 * t]), __uint_as_float(sv[2 * t + 1])), c2, nl);
+        for (int t = 0; t < 8; ++t) {
+          const float2 nl2 = nlse2[cl * 8 + t], nd = ndot2[cl * 8 + t];
+          const float2 x = fma2(make_float2(__uint_as_float(sv[2 * t]), __uint_as_float(sv[2 * t + 1])), c2, nl2);
           float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (mask_chunk) {
             if (col0 + 2 * t < zero_below) pv.x = 0.f;
@@ -399,21 +463,22 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           pk[t] = pack_bf16x2(pv.x, pv.y);
           dsk[t] = pack_bf16x2(dd.x, dd.y);
         }
-        // P^T and dS^T (bf16) overwrite the 32 S^T columns this chunk has
-        // just read: P^T in the first 16, dS^T in the last 16.
-        tmem_st_x16(tmem_addr(reg, lane_base, col0), pk);
-        tmem_st_x16(tmem_addr(reg, lane_base, col0 + 16), dsk);
+        // P^T and dS^T (bf16) overwrite the 16 S^T columns this chunk has
+        // just read: P^T in the first 8, dS^T in the last 8.
+        tmem_st_x8(tmem_addr(reg, lane_base, col0), pk);
+        tmem_st_x8(tmem_addr(reg, lane_base, col0 + 8), dsk);
         // The dS^T buffer of this step (n % 3) is free once the bulk reduces
         // of dQ_{n-3}, staged there, have read it (one vote per warp, so the
         // warp stays together for the TMEM loads that follow).
         if (DQ && cl == 0 && n >= Lay::kDSBufs)
           ok = __all_sync(0xffffffffu, mbar_wait(ds_free + n % Lay::kDSBufs, (n / Lay::kDSBufs - 1) & 1, abort_flag));
-        // dS^T row r into the 128B-swizzled tile (query-contiguous rows).
+        // dS^T row r into the 128B-swizzled tile (query-contiguous rows; the
+        // 16-byte unit u holds queries 8 u .. 8 u + 7 of this 64-query half).
 #pragma unroll
-        for (int u4 = 0; u4 < 4 && DQ && ok; ++u4) {
-          const int u = cl * 4 + u4;
-          *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
-              make_uint4(dsk[4 * u4], dsk[4 * u4 + 1], dsk[4 * u4 + 2], dsk[4 * u4 + 3]);
+        for (int u2 = 0; u2 < 2 && DQ && ok; ++u2) {
+          const int uu = cl * 2 + u2;
+          *reinterpret_cast<uint4*>(ds_row + ((uu ^ (r & 7)) << 4)) =
+              make_uint4(dsk[4 * u2], dsk[4 * u2 + 1], dsk[4 * u2 + 2], dsk[4 * u2 + 3]);
         }
       }
       if (!ok) break;
@@ -422,17 +487,16 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(ps_ready + (n & 1));
     }
-    if (ok) ok = mbar_wait(epi, 0, abort_flag);
-    if (!ok) {
-      give_up();
-    } else {
+    if (ok) ok = mbar_wait(epi, uc & 1, abort_flag);
+    if (!ok) break;
+    {
       tc_fence_after();
       // first warpgroup stores dV, second stores dK (scaled)
       const bool row_ok = kpos < L;
       const long long tok = seq0 + kpos;
       const uint32_t col = half == 0 ? Lay::kColDV : Lay::kColDK;
       const float mul = half == 0 ? 1.f : p.scale;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? p.dv : p.dk) + (tok * p.Hkv + g) * D;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? p.dv : p.dk) + (tok * p.Hkv + w.g) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t v[32];
@@ -448,6 +512,12 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
     }
+    // dV and dK are in registers and stored: the next unit may restart them
+    tc_fence_before();
+    mbar_arrive(acc_free);
+    ++uc;
+    }
+    if (!ok) give_up();
   } else if (DQ) {
     // ------------------------------------------------------------ dQ warpgroup
     const int quad = warp & 3;
@@ -455,7 +525,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
     const bool issuer = (warp == 10 && lane == 0);
     bool ok = true;
-    for (int n = 0; n < nsteps && ok; ++n) {
+    int n = 0;  // steps so far
+    for (int k = 0, un = unit_of(0); un < n_units && ok; un = unit_of(++k)) {
+    Unit w;
+    if (!unit_at(un, w)) continue;
+    for (int nl = 0; nl < w.nsteps && ok; ++nl, ++n) {
       if (!(ok = mbar_wait(dq_full + (n & 1), (n >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       uint32_t v[D];
@@ -463,7 +537,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int cc = 0; cc < D / 32; ++cc) tmem_ld_x32(tmem_addr(region(n), lane_base, Lay::kColDQ + cc * 32), v + 32 * cc);
       tc_fence_before();
       mbar_arrive(dq_free + (n & 1));
-      const int h = step_head(n), q0 = step_qtile(n) * kTile;
+      const int h = step_head(w, nl), q0 = step_qtile(w, nl) * kTile;
       // Stage dQ_n in the dS^T buffer of step n, which the dQ product has
       // finished reading: two f32 boxes of 32 columns x 128 rows, 128-byte
       // swizzle, added to the accumulator by two bulk reduces in flight at once.
@@ -484,7 +558,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // whole tile can be added; rows past T are clipped by the TMA unit.
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc)
-          tma_reduce_add_3d(&tm_dq, buf + cc * kTile * 128, cc * 32, h, static_cast<int>(seq0 + q0));
+          tma_reduce_add_3d(&tm_dq, buf + cc * kTile * 128, cc * 32, h, static_cast<int>(w.seq0 + q0));
         bulk_commit_group();
         // The buffer of step n - 1 goes back to the score warpgroups (dS^T of
         // step n + 2) once its reduces have read it; those of step n stay in
@@ -492,6 +566,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         bulk_wait_group_read1();
         if (n >= 1) mbar_arrive(ds_free + (n - 1) % Lay::kDSBufs);
       }
+    }
     }
     if (issuer) bulk_wait_group0();
     if (!ok) give_up();
@@ -575,7 +650,12 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     auto kern = deterministic ? fa_bwd_kernel<D, false> : fa_bwd_kernel<D, true>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.Hkv, p.n_kvtiles, p.B);
+    // persistent: one CTA per SM, or one per unit when there are fewer
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long units = static_cast<long long>(p.n_kvtiles) * p.B * p.Hkv;
+    const int grid = static_cast<int>(units < sms ? units : sms);
     kern<<<grid, kBwdThreads, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     e = cudaGetLastError();
   } else {
