@@ -339,6 +339,17 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tma_load_3d(sV + c * Lay::kChunkBytes, &tm_v, kv_full, c * 64, w.g, static_cast<int>(w.seq0 + w.k0));
           }
           ++kv_loads;
+          // and the next unit's K_j, V_j into L2, so that their load at the
+          // unit boundary does not wait for DRAM
+          for (int k2 = k + 1, un2 = unit_of(k2); un2 < n_units; un2 = unit_of(++k2)) {
+            Unit w2;
+            if (!unit_at(un2, w2)) continue;
+            for (int c = 0; c < Lay::kChunks; ++c) {
+              tma_prefetch_l2_3d(&tm_k, c * 64, w2.g, static_cast<int>(w2.seq0 + w2.k0));
+              tma_prefetch_l2_3d(&tm_v, c * 64, w2.g, static_cast<int>(w2.seq0 + w2.k0));
+            }
+            break;
+          }
         }
         if ((role != 0 || DQ) && !(ok = mbar_wait(kv_full, uc & 1, abort_flag))) break;
         tc_fence_after();
