@@ -734,17 +734,27 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // results of waits are made warp-uniform (the shuffles and TMEM accesses
     // need whole warps) and the loop ends only on a vote of all 128 threads.
     bool ok = true;
-    for (int i = 0; i < nt; ++i) {
-      const int kpos = (t0 + i) * kTile + r;
-      const bool valid = kpos < L;
-      float sk = 1.f, sv = 1.f;  // per-token scales of this key (FP8 cache)
+    // per-token scales of this thread's key (FP8 cache), loaded a tile ahead:
+    // through a page table they are two dependent loads from memory
+    auto load_scales = [&](int i, float& sk, float& sv) {
+      sk = 1.f;
+      sv = 1.f;
       if constexpr (FP8) {
-        if (valid) {
+        const int kpos = (t0 + i) * kTile + r;
+        if (i < nt && kpos < L) {
           const long long si = decode_row(p, b, seq0, kpos, L) * p.Hkv + g;
           sk = __ldg(p.k_scale + si);
           sv = __ldg(p.v_scale + si);
         }
       }
+    };
+    float sk_next, sv_next;
+    load_scales(0, sk_next, sv_next);
+    for (int i = 0; i < nt; ++i) {
+      const int kpos = (t0 + i) * kTile + r;
+      const bool valid = kpos < L;
+      const float sk = sk_next, sv = sv_next;
+      load_scales(i + 1, sk_next, sv_next);
       bool w = __all_sync(0xffffffffu, mbar_wait(s_full + (i & 1), (i >> 1) & 1, abort_flag));
       float x[H];
       bool over = false;  // a score above its head's reference by more than the slack
