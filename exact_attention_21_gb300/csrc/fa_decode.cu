@@ -493,7 +493,10 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
-template <bool FP8>
+// HS: query heads the softmax threads work on (8 when the GQA group has at
+// most 8, else 16): the MMA's N is 16 either way, and the rows of P^T and
+// columns of O^T past the group are never read.
+template <bool FP8, int HS>
 __global__ void __launch_bounds__(DecTcLayout<FP8>::kThreads, 1)
 fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const DecodeParams p) {
@@ -656,7 +659,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const int hq0 = g * group;
     const float c = p.scale_log2;
     // Q, K-major with the 128-byte swizzle; padded heads are 0
-    float inv_sq[H];  // FP8: 1 / s_q of each head
+    float inv_sq[HS];  // FP8: 1 / s_q of each head
     if constexpr (FP8) {
       // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h; thread r
       // takes dims 16 (r % 8) .. +15 of head r / 8 (one 16-byte unit per row)
@@ -708,7 +711,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       mbar_arrive(q_ready);
       asm volatile("bar.sync 1, 128;" ::: "memory");  // every head's 1 / s_q written
 #pragma unroll
-      for (int hh = 0; hh < H; ++hh) inv_sq[hh] = sInvSq[hh];
+      for (int hh = 0; hh < HS; ++hh) inv_sq[hh] = sInvSq[hh];
     } else {
       const int h = r / 8, u2 = (r % 8) * 2;  // 8 threads per head row, two 16-byte units each
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
@@ -722,11 +725,11 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       fence_proxy_async_smem();
       mbar_arrive(q_ready);
 #pragma unroll
-      for (int hh = 0; hh < H; ++hh) inv_sq[hh] = 1.f;
+      for (int hh = 0; hh < HS; ++hh) inv_sq[hh] = 1.f;
     }
-    float m[H], lt[H];
+    float m[HS], lt[HS];
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
+    for (int h = 0; h < HS; ++h) {
       m[h] = -INFINITY;
       lt[h] = 0.f;
     }
@@ -756,34 +759,34 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const float sk = sk_next, sv = sv_next;
       load_scales(i + 1, sk_next, sv_next);
       bool w = __all_sync(0xffffffffu, mbar_wait(s_full + (i & 1), (i >> 1) & 1, abort_flag));
-      float x[H];
+      float x[HS];
       bool over = false;  // a score above its head's reference by more than the slack
       if (w) {
         tc_fence_after();
         uint32_t svv[Lay::kSCols];
-        float sc[H];
+        float sc[HS];
         if constexpr (FP8) {
           const uint32_t ts = tmem + Lay::kColS + (i & 1) * Lay::kSCols;
           tmem_ld_x16_x32_pair(tmem_addr(ts, lane_base, 2 * H), svv + 2 * H, tmem_addr(ts, lane_base, 0), svv);
 #pragma unroll
-          for (int h = 0; h < H; ++h)
+          for (int h = 0; h < HS; ++h)
             sc[h] = (__uint_as_float(svv[h]) + __uint_as_float(svv[H + h]) + __uint_as_float(svv[2 * H + h])) * inv_sq[h];
         } else {
           tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (i & 1) * Lay::kSCols, lane_base, 0), svv);
 #pragma unroll
-          for (int h = 0; h < H; ++h) sc[h] = __uint_as_float(svv[h]);
+          for (int h = 0; h < HS; ++h) sc[h] = __uint_as_float(svv[h]);
         }
         const float ck = c * sk;
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
+        for (int h = 0; h < HS; ++h) {
           x[h] = valid ? sc[h] * ck : -INFINITY;
           over |= x[h] > m[h] + kDecRescaleSlack;  // always for a valid key on the first tile (m = -inf)
         }
       }
       bool bump = false;
-      float alpha[H];
+      float alpha[HS];
 #pragma unroll
-      for (int h = 0; h < H; ++h) alpha[h] = 1.f;
+      for (int h = 0; h < HS; ++h) alpha[h] = 1.f;
       // One vote per tile: in the common case no reference moves and the
       // probabilities are taken against the current m.  Otherwise (the first
       // tile, a score jump, or a wait that gave up) the tile max of every
@@ -791,7 +794,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (softmax_sync_or(over || !w)) {
         if (!(ok = softmax_sync_and(w))) break;
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
+        for (int h = 0; h < HS; ++h) {
           float mx = x[h];
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -799,7 +802,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
+        for (int h = 0; h < HS; ++h) {
           const float tm = fmaxf(fmaxf(sRed[h], sRed[H + h]), fmaxf(sRed[2 * H + h], sRed[3 * H + h]));
           // the tile's key 0 is valid, so tm is finite
           const bool up = tm > m[h] + kDecRescaleSlack;
@@ -816,7 +819,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         uint8_t* pb = pbuf(i) + (r / 64) * Lay::kHChunkBytes + (r % 8) * 2;
         const int pu = (r % 64) / 8;
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
+        for (int h = 0; h < HS; ++h) {
           const float pv = ex2_approx(x[h] - m[h]);  // masked keys: 0
           lt[h] = fmaf(lt[h], alpha[h], pv);
           uint16_t bits;
@@ -839,7 +842,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           uint32_t ov[H];
           tmem_ld_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
 #pragma unroll
-          for (int h = 0; h < H; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+          for (int h = 0; h < HS; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
           tmem_st_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
           tmem_st_wait();
         }
@@ -856,7 +859,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     ok = softmax_sync_and(ok);
     // ---- the split's output: O^T / l, and its LSE
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
+    for (int h = 0; h < HS; ++h) {
       float x = lt[h];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
@@ -872,7 +875,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       tmem_ld_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
       const long long row0 = static_cast<long long>(b) * p.Hq + hq0;
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
+      for (int h = 0; h < HS; ++h) {
         if (h < group) {
           const float l = sRed[h] + sRed[H + h] + sRed[2 * H + h] + sRed[3 * H + h];
           p.o_part[((row0 + h) * p.n_splits + split) * D + r] = __uint_as_float(ov[h]) / l;
@@ -999,11 +1002,11 @@ template <bool FP8>
 int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
   using Lay = DecTcLayout<FP8>;
   if (p.group > kDecHeads) return -1;
-  cudaError_t e =
-      cudaFuncSetAttribute(fa_decode_tc_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+  auto kern = p.group <= 8 ? fa_decode_tc_kernel<FP8, 8> : fa_decode_tc_kernel<FP8, kDecHeads>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_splits, p.Hkv, p.B);
-  fa_decode_tc_kernel<FP8><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tk, tv, p);
+  kern<<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(p.B) * p.Hq;
