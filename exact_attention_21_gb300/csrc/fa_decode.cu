@@ -454,7 +454,11 @@ struct DecTcLayout {
   static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
-  static constexpr int kThreads = FP8 ? 320 : 192;
+  // warp 0 loads, warp 1 issues P V, warps 2-5 run the softmax, warps 6-9
+  // dequantise V (FP8), and the last warp issues S^T: a single thread
+  // issuing both would start one of these narrow MMAs only every ~100 cycles
+  static constexpr int kWarpS = FP8 ? 10 : 6;
+  static constexpr int kThreads = 32 * (kWarpS + 1);
   // S^T buffers of kSCols columns at 0 and kSCols (FP8: a column per head and term), O^T after them
   static constexpr int kSCols = FP8 ? 3 * kDecHeads : kDecHeads;
   static constexpr uint32_t kTmemCols = FP8 ? 128 : 64;
@@ -555,7 +559,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       mbar_init(pv_done + i, 1);
       mbar_init(v_ready + i, 128);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);  // both MMA-issuing threads commit
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -604,11 +608,38 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       for (int i = issued > NS ? issued - NS : 0; i < issued; ++i) mbar_wait(full + i % NS, (i / NS) & 1, &never);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; i < nt && ok; ++i) {
+        // P^T of tile i written, S^T buffer i & 1 read, O^T rescaled
+        if (!(ok = mbar_wait(p_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
+        if (FP8 && !(ok = mbar_wait(v_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t sVa = smem_u32(v16(i)), sPa = smem_u32(pbuf(i));
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_ss(tmem + Lay::kColO, sdesc_sw128(sVa + kk * 2048, Lay::kChunkBytes, 1024),
+                  sdesc_sw128(sPa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_o, (i > 0 || kk > 0));
+        // the stage's K was read by S^T of tile i, complete before the softmax
+        // released P^T of tile i
+        if constexpr (!FP8) umma_commit(empty + i % NS);
+        umma_commit(pv_done + (i & 1));
+      }
+      if (!ok) give_up();
+      umma_commit(drain);
+      int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+  } else if (warp == Lay::kWarpS) {
+    // ------------------------------------------------------------ S^T issuer
     if (lane == 0) {
       const uint32_t sQa = smem_u32(sQ);
-      auto issue_s = [&](int i) -> bool {
-        if (!mbar_wait(full + i % NS, (i / NS) & 1, abort_flag)) return false;
+      bool ok = mbar_wait(q_ready, 0, abort_flag);
+      for (int i = 0; i < nt && ok; ++i) {
+        // S^T buffer i & 1 was read by the softmax of tile i - 2 once it released P^T
+        if (i >= 2 && !(ok = mbar_wait(p_ready + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(full + i % NS, (i / NS) & 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t sKa = smem_u32(ktile(i));
         if constexpr (FP8) {
@@ -626,24 +657,6 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         umma_commit(s_full + (i & 1));
         if constexpr (FP8) umma_commit(empty + i % NS);  // the K half of the stage has been read
-        return true;
-      };
-      bool ok = mbar_wait(q_ready, 0, abort_flag);
-      if (ok) ok = issue_s(0);
-      if (ok && nt > 1) ok = issue_s(1);
-      for (int i = 0; i < nt && ok; ++i) {
-        // P^T of tile i written, S^T buffer i & 1 read, O^T rescaled
-        if (!(ok = mbar_wait(p_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
-        if (FP8 && !(ok = mbar_wait(v_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t sVa = smem_u32(v16(i)), sPa = smem_u32(pbuf(i));
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(tmem + Lay::kColO, sdesc_sw128(sVa + kk * 2048, Lay::kChunkBytes, 1024),
-                  sdesc_sw128(sPa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_o, (i > 0 || kk > 0));
-        if constexpr (!FP8) umma_commit(empty + i % NS);
-        umma_commit(pv_done + (i & 1));
-        if (i + 2 < nt && !(ok = issue_s(i + 2))) break;
       }
       if (!ok) give_up();
       umma_commit(drain);
