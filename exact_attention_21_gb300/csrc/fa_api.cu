@@ -409,6 +409,7 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   p.group = Hq / Hkv;
   p.split_tiles = decode_split_tiles(B, Hkv, s.n_tiles, T, !paged && cu_seqlens_k != nullptr, dev->sms);
   p.n_splits = (s.n_tiles + p.split_tiles - 1) / p.split_tiles;
+  p.sms = dev->sms;
   const size_t rows = static_cast<size_t>(B) * Hq * p.n_splits;
   p.o_part = static_cast<float*>(workspace);
   p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * d * 4 + 255) / 256 * 256);

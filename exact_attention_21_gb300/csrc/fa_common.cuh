@@ -94,6 +94,7 @@ struct DecodeParams {
   int B, Hq, Hkv, N, group;
   int n_splits;       // splits per (sequence, K/V head) in the grid
   int split_tiles;    // 128-key tiles per split
+  int sms;            // multiprocessors: CTAs of the persistent decode kernel
   float scale_log2;   // scale * log2(e)
 };
 

@@ -497,6 +497,34 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// One work item of the persistent kernel: split w % n_splits of K/V head
+// (w / n_splits) % Hkv of sequence w / (n_splits Hkv).  False for a split past
+// the end of its sequence's cache (the combine skips it) and for a sequence
+// with bad offsets or length (a status bit).
+struct DecItem {
+  long long seq0;
+  int split, g, b, L, t0, nt;
+};
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, long long w, DecItem& it) {
+  it.split = static_cast<int>(w % p.n_splits);
+  const long long rest = w / p.n_splits;
+  it.g = static_cast<int>(rest % p.Hkv);
+  it.b = static_cast<int>(rest / p.Hkv);
+  if (!decode_bounds(p, it.b, it.seq0, it.L)) return false;
+  const int seq_tiles = (it.L + kTile - 1) / kTile;
+  it.t0 = it.split * p.split_tiles;
+  if (it.t0 >= seq_tiles) return false;
+  it.nt = min(p.split_tiles, seq_tiles - it.t0);
+  return true;
+}
+// This CTA's first item at or after w (its items are blockIdx.x + j gridDim.x)
+// that has work, or n_items.
+__device__ __forceinline__ long long next_item(const DecodeParams& p, long long w, long long n_items, DecItem& it) {
+  for (; w < n_items; w += gridDim.x)
+    if (decode_item(p, w, it)) return w;
+  return n_items;
+}
+
 // HS: query heads the softmax threads work on (8 when the GQA group has at
 // most 8, else 16): the MMA's N is 16 either way, and the rows of P^T and
 // columns of O^T past the group are never read.
@@ -513,14 +541,10 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   constexpr uint32_t id_s = FP8 ? idesc_e4m3_f32(kTile, 3 * H) : idesc_bf16_f32(kTile, H, false, false);
   constexpr uint32_t id_o = FP8 ? idesc_f16_f32(D, H, true, false) : idesc_bf16_f32(D, H, true, false);
 
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  long long seq0;
-  int L;
-  if (!decode_bounds(p, b, seq0, L)) return;
-  const int seq_tiles = (L + kTile - 1) / kTile;
-  const int t0 = split * p.split_tiles;
-  if (t0 >= seq_tiles) return;  // past the end of this sequence's cache: the combine skips it
-  const int nt = min(p.split_tiles, seq_tiles - t0);
+  // persistent: the CTA runs its items back to back; the barrier rings and
+  // the S^T / P^T / V buffers run on a tile count over all of them (gt), so
+  // the loads and S^T of an item overlap the previous item's epilogue
+  const long long n_items = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -535,13 +559,14 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint64_t* pv_done = p_ready + 2;  // FP8: also frees dequantised V buffer i & 1
   uint64_t* drain = pv_done + 2;
   uint64_t* v_ready = drain + 1;     // FP8 only: dequantised V of tile i in buffer i & 1
+  uint64_t* o_free = v_ready + 2;    // O^T buffer j read by the epilogue of an item
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
-  auto stage = [&](int st) { return smem + st * Lay::kStageBytes; };
-  auto pbuf = [&](int i) { return smem + Lay::kOffP + (i & 1) * Lay::kPBytes; };
+  auto stage = [&](uint32_t st) { return smem + st * Lay::kStageBytes; };
+  auto pbuf = [&](uint32_t i) { return smem + Lay::kOffP + (i & 1) * Lay::kPBytes; };
   // the K tile S^T of tile i reads (E4M3 for an FP8 cache) and the 16-bit V tile of P V
-  auto ktile = [&](int i) { return stage(i % NS); };
-  auto v16 = [&](int i) {
+  auto ktile = [&](uint32_t i) { return stage(i % NS); };
+  auto v16 = [&](uint32_t i) {
     return FP8 ? smem + Lay::kOffCvt + (i & 1) * Lay::kTileBytes : stage(i % NS) + Lay::kTileBytes;
   };
 
@@ -558,6 +583,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       mbar_init(p_ready + i, 128);
       mbar_init(pv_done + i, 1);
       mbar_init(v_ready + i, 128);
+      mbar_init(o_free + i, 128);
     }
     mbar_init(drain, 2);  // both MMA-issuing threads commit
     *abort_flag = 0;
@@ -582,49 +608,61 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
-    int issued = 0;
+    uint32_t gt = 0;  // tiles issued
     bool ok = true;
-    for (int i = 0; i < nt; ++i) {
-      const int st = i % NS;
-      // lane 0 waits for the stage and posts the byte count before any copy
-      if (lane == 0) {
-        if (i >= NS) ok = mbar_wait(empty + st, ((i / NS) - 1) & 1, abort_flag);
-        if (ok) mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
+    DecItem it;
+    for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
+         w = next_item(p, w + gridDim.x, n_items, it)) {
+      for (int i = 0; i < it.nt; ++i, ++gt) {
+        const uint32_t st = gt % NS;
+        // lane 0 waits for the stage and posts the byte count before any copy
+        if (lane == 0) {
+          if (gt >= NS) ok = mbar_wait(empty + st, ((gt / NS) - 1) & 1, abort_flag);
+          if (ok) mbar_arrive_expect_tx(full + st, Lay::kStageBytes);
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        if constexpr (FP8) {
+          load_kv_tile<1, Lay::kTile8Bytes, 128>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTile8Bytes, full + st,
+                                                  it.b, it.g, it.seq0, (it.t0 + i) * kTile, it.L, lane);
+        } else {
+          load_kv_tile<2, Lay::kChunkBytes, 64>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTileBytes, full + st,
+                                                 it.b, it.g, it.seq0, (it.t0 + i) * kTile, it.L, lane);
+        }
       }
-      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
-      if constexpr (FP8) {
-        load_kv_tile<1, Lay::kTile8Bytes, 128>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTile8Bytes, full + st, b,
-                                                g, seq0, (t0 + i) * kTile, L, lane);
-      } else {
-        load_kv_tile<2, Lay::kChunkBytes, 64>(p, &tm_k, &tm_v, stage(st), stage(st) + Lay::kTileBytes, full + st, b,
-                                               g, seq0, (t0 + i) * kTile, L, lane);
-      }
-      ++issued;
     }
     if (lane == 0) {
       if (!ok) give_up();
       // no TMA write may still be in flight when the CTA exits
       int never = 0;
-      for (int i = issued > NS ? issued - NS : 0; i < issued; ++i) mbar_wait(full + i % NS, (i / NS) & 1, &never);
+      for (uint32_t j = gt > NS ? gt - NS : 0; j < gt; ++j) mbar_wait(full + j % NS, (j / NS) & 1, &never);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ P V issuer
     if (lane == 0) {
       bool ok = true;
-      for (int i = 0; i < nt && ok; ++i) {
-        // P^T of tile i written, S^T buffer i & 1 read, O^T rescaled
-        if (!(ok = mbar_wait(p_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
-        if (FP8 && !(ok = mbar_wait(v_ready + (i & 1), (i >> 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t sVa = smem_u32(v16(i)), sPa = smem_u32(pbuf(i));
+      uint32_t gt = 0, kq = 0;  // tiles and items so far
+      DecItem it;
+      for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
+           w = next_item(p, w + gridDim.x, n_items, it), ++kq) {
+        // O^T buffer kq & 1 was last read by the epilogue of item kq - 2
+        if (kq >= 2 && !(ok = mbar_wait(o_free + (kq & 1), ((kq - 2) >> 1) & 1, abort_flag))) break;
+        const uint32_t tO = tmem + Lay::kColO + (kq & 1) * H;
+        for (int i = 0; i < it.nt; ++i, ++gt) {
+          // P^T of tile gt written, S^T buffer gt & 1 read, O^T rescaled
+          if (!(ok = mbar_wait(p_ready + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
+          if (FP8 && !(ok = mbar_wait(v_ready + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t sVa = smem_u32(v16(gt)), sPa = smem_u32(pbuf(gt));
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_ss(tmem + Lay::kColO, sdesc_sw128(sVa + kk * 2048, Lay::kChunkBytes, 1024),
-                  sdesc_sw128(sPa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_o, (i > 0 || kk > 0));
-        // the stage's K was read by S^T of tile i, complete before the softmax
-        // released P^T of tile i
-        if constexpr (!FP8) umma_commit(empty + i % NS);
-        umma_commit(pv_done + (i & 1));
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_ss(tO, sdesc_sw128(sVa + kk * 2048, Lay::kChunkBytes, 1024),
+                    sdesc_sw128(sPa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_o,
+                    (i > 0 || kk > 0));
+          // the stage's K was read by S^T of tile gt, complete before the
+          // softmax released P^T of tile gt
+          if constexpr (!FP8) umma_commit(empty + gt % NS);
+          umma_commit(pv_done + (gt & 1));
+        }
       }
       if (!ok) give_up();
       umma_commit(drain);
@@ -635,28 +673,35 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // ------------------------------------------------------------ S^T issuer
     if (lane == 0) {
       const uint32_t sQa = smem_u32(sQ);
-      bool ok = mbar_wait(q_ready, 0, abort_flag);
-      for (int i = 0; i < nt && ok; ++i) {
-        // S^T buffer i & 1 was read by the softmax of tile i - 2 once it released P^T
-        if (i >= 2 && !(ok = mbar_wait(p_ready + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(full + i % NS, (i / NS) & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t sKa = smem_u32(ktile(i));
-        if constexpr (FP8) {
-          // E4M3 K (one 128-byte row per key) x the 48 E4M3 query rows, 32 elements per step
+      bool ok = true;
+      uint32_t gt = 0, kq = 0;  // tiles and items so far
+      DecItem it;
+      for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
+           w = next_item(p, w + gridDim.x, n_items, it), ++kq) {
+        // the item's query (written once S^T of the previous item completed)
+        if (!(ok = mbar_wait(q_ready, kq & 1, abort_flag))) break;
+        for (int i = 0; i < it.nt; ++i, ++gt) {
+          // S^T buffer gt & 1 was read by the softmax of tile gt - 2 once it released P^T
+          if (gt >= 2 && !(ok = mbar_wait(p_ready + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(full + gt % NS, (gt / NS) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t sKa = smem_u32(ktile(gt));
+          const uint32_t tS = tmem + Lay::kColS + (gt & 1) * Lay::kSCols;
+          if constexpr (FP8) {
+            // E4M3 K (one 128-byte row per key) x the 48 E4M3 query rows, 32 elements per step
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk)
-            umma_ss_f8(tmem + Lay::kColS + (i & 1) * Lay::kSCols, sdesc_sw128(sKa + kk * 32, 16, 1024),
-                       sdesc_sw128(sQa + kk * 32, 16, 1024), id_s, kk > 0);
-        } else {
+            for (int kk = 0; kk < D / 32; ++kk)
+              umma_ss_f8(tS, sdesc_sw128(sKa + kk * 32, 16, 1024), sdesc_sw128(sQa + kk * 32, 16, 1024), id_s,
+                         kk > 0);
+          } else {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + Lay::kColS + (i & 1) * Lay::kSCols,
-                    sdesc_sw128(sKa + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
-                    sdesc_sw128(sQa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_s, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_ss(tS, sdesc_sw128(sKa + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
+                      sdesc_sw128(sQa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_s, kk > 0);
+          }
+          umma_commit(s_full + (gt & 1));
+          if constexpr (FP8) umma_commit(empty + gt % NS);  // the K half of the stage has been read
         }
-        umma_commit(s_full + (i & 1));
-        if constexpr (FP8) umma_commit(empty + i % NS);  // the K half of the stage has been read
       }
       if (!ok) give_up();
       umma_commit(drain);
@@ -669,232 +714,270 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const int r = quad * 32 + lane;  // key row of S^T, dimension row of O^T
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
     const int group = p.group;
-    const int hq0 = g * group;
     const float c = p.scale_log2;
-    // Q, K-major with the 128-byte swizzle; padded heads are 0
-    float inv_sq[HS];  // FP8: 1 / s_q of each head
-    if constexpr (FP8) {
-      // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h; thread r
-      // takes dims 16 (r % 8) .. +15 of head r / 8 (one 16-byte unit per row)
-      const int h = r / 8, sub = r % 8;
-      float v[16];
-      if (h < group) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                          (static_cast<long long>(b) * p.Hq + hq0 + h) * D + 16 * sub);
-        const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
-        const uint32_t wq[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    // The item's query into sQ (K-major, 128-byte swizzle, padded heads 0) and,
+    // FP8, 1 / s_q of each head into isq; then q_ready.
+    auto write_q = [&](const DecItem& it, float (&isq)[HS]) {
+      const int hq0 = it.g * group;
+      if constexpr (FP8) {
+        // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h; thread r
+        // takes dims 16 (r % 8) .. +15 of head r / 8 (one 16-byte unit per row)
+        const int h = r / 8, sub = r % 8;
+        float v[16];
+        if (h < group) {
+          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                            (static_cast<long long>(it.b) * p.Hq + hq0 + h) * D +
+                                                            16 * sub);
+          const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
+          const uint32_t wq[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          v[2 * e] = bf16_lo(wq[e]);
-          v[2 * e + 1] = bf16_hi(wq[e]);
+          for (int e = 0; e < 8; ++e) {
+            v[2 * e] = bf16_lo(wq[e]);
+            v[2 * e + 1] = bf16_hi(wq[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0.f;
         }
-      } else {
+        float amax = 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = 0.f;
-      }
-      float amax = 0.f;
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        // the 8 threads of a head are 8 consecutive lanes
 #pragma unroll
-      for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
-      // the 8 threads of a head are 8 consecutive lanes
+        for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float sq = amax > 0.f ? 448.f / amax : 1.f;
+        uint32_t term[3][4] = {};
 #pragma unroll
-      for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const float sq = amax > 0.f ? 448.f / amax : 1.f;
-      uint32_t term[3][4] = {};
+        for (int e = 0; e < 16; e += 2) {
+          float2 y = make_float2(v[e] * sq, v[e + 1] * sq);  // remainder still to represent
 #pragma unroll
-      for (int e = 0; e < 16; e += 2) {
-        float2 y = make_float2(v[e] * sq, v[e + 1] * sq);  // remainder still to represent
+          for (int t = 0; t < 3; ++t) {
+            const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+            const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(c2, __NV_E4M3);
+            y.x -= __half2float(*reinterpret_cast<const __half*>(&hb.x));  // exact in f32
+            y.y -= __half2float(*reinterpret_cast<const __half*>(&hb.y));
+            term[t][e / 4] |= static_cast<uint32_t>(c2) << (16 * ((e / 2) & 1));
+          }
+        }
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
-          const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
-          const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(c2, __NV_E4M3);
-          y.x -= __half2float(*reinterpret_cast<const __half*>(&hb.x));  // exact in f32
-          y.y -= __half2float(*reinterpret_cast<const __half*>(&hb.y));
-          term[t][e / 4] |= static_cast<uint32_t>(c2) << (16 * ((e / 2) & 1));
+          const int row = t * kDecHeads + h;
+          *reinterpret_cast<uint4*>(sQ + row * 128 + ((sub ^ (row & 7)) << 4)) =
+              make_uint4(term[t][0], term[t][1], term[t][2], term[t][3]);
         }
+        float* sInvSq = reinterpret_cast<float*>(smem + Lay::kOffInvSq);
+        if (sub == 0) sInvSq[h] = 1.f / sq;
+        fence_proxy_async_smem();
+        mbar_arrive(q_ready);
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // every head's 1 / s_q written
+#pragma unroll
+        for (int hh = 0; hh < HS; ++hh) isq[hh] = sInvSq[hh];
+      } else {
+        const int h = r / 8, u2 = (r % 8) * 2;  // 8 threads per head row, two 16-byte units each
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                          (static_cast<long long>(it.b) * p.Hq + hq0 + h) * D);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int u = u2 + j;  // unit of the 256-byte row: chunk u / 8, unit u % 8
+          const uint4 val = h < group ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(sQ + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = val;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(q_ready);
+#pragma unroll
+        for (int hh = 0; hh < HS; ++hh) isq[hh] = 1.f;
       }
-#pragma unroll
-      for (int t = 0; t < 3; ++t) {
-        const int row = t * kDecHeads + h;
-        *reinterpret_cast<uint4*>(sQ + row * 128 + ((sub ^ (row & 7)) << 4)) =
-            make_uint4(term[t][0], term[t][1], term[t][2], term[t][3]);
-      }
-      float* sInvSq = reinterpret_cast<float*>(smem + Lay::kOffInvSq);
-      if (sub == 0) sInvSq[h] = 1.f / sq;
-      fence_proxy_async_smem();
-      mbar_arrive(q_ready);
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // every head's 1 / s_q written
-#pragma unroll
-      for (int hh = 0; hh < HS; ++hh) inv_sq[hh] = sInvSq[hh];
-    } else {
-      const int h = r / 8, u2 = (r % 8) * 2;  // 8 threads per head row, two 16-byte units each
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                        (static_cast<long long>(b) * p.Hq + hq0 + h) * D);
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int u = u2 + j;  // unit of the 256-byte row: chunk u / 8, unit u % 8
-        const uint4 val = h < group ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sQ + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = val;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(q_ready);
-#pragma unroll
-      for (int hh = 0; hh < HS; ++hh) inv_sq[hh] = 1.f;
-    }
-    float m[HS], lt[HS];
-#pragma unroll
-    for (int h = 0; h < HS; ++h) {
-      m[h] = -INFINITY;
-      lt[h] = 0.f;
-    }
-    // A wait that gives up must not leave the other threads at a barrier:
-    // results of waits are made warp-uniform (the shuffles and TMEM accesses
-    // need whole warps) and the loop ends only on a vote of all 128 threads.
-    bool ok = true;
-    // per-token scales of this thread's key (FP8 cache), loaded a tile ahead:
-    // through a page table they are two dependent loads from memory
-    auto load_scales = [&](int i, float& sk, float& sv) {
+    };
+    // per-token scales of this thread's key in tile i of an item (FP8 cache),
+    // loaded a tile ahead: through a page table they are two dependent loads
+    auto load_scales = [&](const DecItem& it, int i, float& sk, float& sv) {
       sk = 1.f;
       sv = 1.f;
       if constexpr (FP8) {
-        const int kpos = (t0 + i) * kTile + r;
-        if (i < nt && kpos < L) {
-          const long long si = decode_row(p, b, seq0, kpos, L) * p.Hkv + g;
+        const int kpos = (it.t0 + i) * kTile + r;
+        if (i < it.nt && kpos < it.L) {
+          const long long si = decode_row(p, it.b, it.seq0, kpos, it.L) * p.Hkv + it.g;
           sk = __ldg(p.k_scale + si);
           sv = __ldg(p.v_scale + si);
         }
       }
     };
-    float sk_next, sv_next;
-    load_scales(0, sk_next, sv_next);
-    for (int i = 0; i < nt; ++i) {
-      const int kpos = (t0 + i) * kTile + r;
-      const bool valid = kpos < L;
-      const float sk = sk_next, sv = sv_next;
-      load_scales(i + 1, sk_next, sv_next);
-      bool w = __all_sync(0xffffffffu, mbar_wait(s_full + (i & 1), (i >> 1) & 1, abort_flag));
-      float x[HS];
-      bool over = false;  // a score above its head's reference by more than the slack
-      if (w) {
-        tc_fence_after();
-        uint32_t svv[Lay::kSCols];
-        float sc[HS];
-        if constexpr (FP8) {
-          const uint32_t ts = tmem + Lay::kColS + (i & 1) * Lay::kSCols;
-          tmem_ld_x16_x32_pair(tmem_addr(ts, lane_base, 2 * H), svv + 2 * H, tmem_addr(ts, lane_base, 0), svv);
+    // A wait that gives up must not leave the other threads at a barrier:
+    // results of waits are made warp-uniform (the shuffles and TMEM accesses
+    // need whole warps) and the loops end only on a vote of all 128 threads.
+    bool ok = true;
+    uint32_t gt = 0, kq = 0;  // tiles and items so far
+    DecItem it;
+    long long w = next_item(p, blockIdx.x, n_items, it);
+    float inv_sq[HS];  // FP8: 1 / s_q of each head
+    float sk_next = 1.f, sv_next = 1.f;
+    if (w < n_items) {
+      write_q(it, inv_sq);
+      load_scales(it, 0, sk_next, sv_next);
+    }
+    while (w < n_items && ok) {
+      const uint32_t tO = tmem + Lay::kColO + (kq & 1) * H;
+      float m[HS], lt[HS];
 #pragma unroll
-          for (int h = 0; h < HS; ++h)
-            sc[h] = (__uint_as_float(svv[h]) + __uint_as_float(svv[H + h]) + __uint_as_float(svv[2 * H + h])) * inv_sq[h];
-        } else {
-          tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (i & 1) * Lay::kSCols, lane_base, 0), svv);
-#pragma unroll
-          for (int h = 0; h < HS; ++h) sc[h] = __uint_as_float(svv[h]);
-        }
-        const float ck = c * sk;
-#pragma unroll
-        for (int h = 0; h < HS; ++h) {
-          x[h] = valid ? sc[h] * ck : -INFINITY;
-          over |= x[h] > m[h] + kDecRescaleSlack;  // always for a valid key on the first tile (m = -inf)
-        }
+      for (int h = 0; h < HS; ++h) {
+        m[h] = -INFINITY;
+        lt[h] = 0.f;
       }
-      bool bump = false;
-      float alpha[HS];
-#pragma unroll
-      for (int h = 0; h < HS; ++h) alpha[h] = 1.f;
-      // One vote per tile: in the common case no reference moves and the
-      // probabilities are taken against the current m.  Otherwise (the first
-      // tile, a score jump, or a wait that gave up) the tile max of every
-      // head is reduced over the 128 keys.
-      if (softmax_sync_or(over || !w)) {
-        if (!(ok = softmax_sync_and(w))) break;
-#pragma unroll
-        for (int h = 0; h < HS; ++h) {
-          float mx = x[h];
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          if (lane == 0) sRed[quad * H + h] = mx;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-#pragma unroll
-        for (int h = 0; h < HS; ++h) {
-          const float tm = fmaxf(fmaxf(sRed[h], sRed[H + h]), fmaxf(sRed[2 * H + h], sRed[3 * H + h]));
-          // the tile's key 0 is valid, so tm is finite
-          const bool up = tm > m[h] + kDecRescaleSlack;
-          const float mn = up ? tm : m[h];
-          alpha[h] = up ? ex2_approx(m[h] - mn) : 1.f;
-          bump |= up;
-          m[h] = mn;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // sRed is rewritten by the next reduction
-      }
-      // P^T buffer i & 1 was last read by P V of tile i - 2
-      w = i < 2 || __all_sync(0xffffffffu, mbar_wait(pv_done + (i & 1), ((i - 2) >> 1) & 1, abort_flag));
-      if (w) {
-        uint8_t* pb = pbuf(i) + (r / 64) * Lay::kHChunkBytes + (r % 8) * 2;
-        const int pu = (r % 64) / 8;
-#pragma unroll
-        for (int h = 0; h < HS; ++h) {
-          const float pv = ex2_approx(x[h] - m[h]);  // masked keys: 0
-          lt[h] = fmaf(lt[h], alpha[h], pv);
-          uint16_t bits;
-          if constexpr (FP8) {
-            const __half ph = __float2half_rn(pv * sv);
-            bits = *reinterpret_cast<const uint16_t*>(&ph);
-          } else {
-            const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
-            bits = *reinterpret_cast<const uint16_t*>(&pb16);
-          }
-          sts_u16(pb + h * 128 + ((pu ^ (h & 7)) << 4), bits);
-        }
-      }
-      // m is the same in every thread, so bump is uniform
-      if (w && i > 0 && bump) {
-        // O^T may only be touched once P V of tile i - 1 has completed
-        w = __all_sync(0xffffffffu, mbar_wait(pv_done + ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag));
-        if (w) {
+      for (int i = 0; i < it.nt; ++i, ++gt) {
+        const int kpos = (it.t0 + i) * kTile + r;
+        const bool valid = kpos < it.L;
+        const float sk = sk_next, sv = sv_next;
+        load_scales(it, i + 1, sk_next, sv_next);
+        bool wt = __all_sync(0xffffffffu, mbar_wait(s_full + (gt & 1), (gt >> 1) & 1, abort_flag));
+        float x[HS];
+        bool over = false;  // a score above its head's reference by more than the slack
+        if (wt) {
           tc_fence_after();
-          uint32_t ov[H];
-          tmem_ld_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
+          uint32_t svv[Lay::kSCols];
+          float sc[HS];
+          if constexpr (FP8) {
+            const uint32_t ts = tmem + Lay::kColS + (gt & 1) * Lay::kSCols;
+            tmem_ld_x16_x32_pair(tmem_addr(ts, lane_base, 2 * H), svv + 2 * H, tmem_addr(ts, lane_base, 0), svv);
 #pragma unroll
-          for (int h = 0; h < HS; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-          tmem_st_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
-          tmem_st_wait();
+            for (int h = 0; h < HS; ++h)
+              sc[h] = (__uint_as_float(svv[h]) + __uint_as_float(svv[H + h]) + __uint_as_float(svv[2 * H + h])) *
+                      inv_sq[h];
+          } else {
+            tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (gt & 1) * Lay::kSCols, lane_base, 0), svv);
+#pragma unroll
+            for (int h = 0; h < HS; ++h) sc[h] = __uint_as_float(svv[h]);
+          }
+          const float ck = c * sk;
+#pragma unroll
+          for (int h = 0; h < HS; ++h) {
+            x[h] = valid ? sc[h] * ck : -INFINITY;
+            over |= x[h] > m[h] + kDecRescaleSlack;  // always for a valid key on the first tile (m = -inf)
+          }
         }
-      }
-      if (w) {
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(p_ready + (i & 1));
-      }
-      // a warp that gave up here stops arriving; the vote of the next tile
-      // (or the final wait below) ends the loop for everyone
-      ok = w;
-    }
-    ok = softmax_sync_and(ok);
-    // ---- the split's output: O^T / l, and its LSE
+        bool bump = false;
+        float alpha[HS];
 #pragma unroll
-    for (int h = 0; h < HS; ++h) {
-      float x = lt[h];
+        for (int h = 0; h < HS; ++h) alpha[h] = 1.f;
+        // One vote per tile: in the common case no reference moves and the
+        // probabilities are taken against the current m.  Otherwise (the first
+        // tile, a score jump, or a wait that gave up) the tile max of every
+        // head is reduced over the 128 keys.
+        if (softmax_sync_or(over || !wt)) {
+          if (!(ok = softmax_sync_and(wt))) break;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-      if (lane == 0) sRed[quad * H + h] = x;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(pv_done + ((nt - 1) & 1), ((nt - 1) >> 1) & 1, abort_flag));
-    if (!ok) {
-      if (lane == 0) give_up();
-    } else {
+          for (int h = 0; h < HS; ++h) {
+            float mx = x[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (lane == 0) sRed[quad * H + h] = mx;
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+          for (int h = 0; h < HS; ++h) {
+            const float tm = fmaxf(fmaxf(sRed[h], sRed[H + h]), fmaxf(sRed[2 * H + h], sRed[3 * H + h]));
+            // the tile's key 0 is valid, so tm is finite
+            const bool up = tm > m[h] + kDecRescaleSlack;
+            const float mn = up ? tm : m[h];
+            alpha[h] = up ? ex2_approx(m[h] - mn) : 1.f;
+            bump |= up;
+            m[h] = mn;
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");  // sRed is rewritten by the next reduction
+        }
+        // P^T buffer gt & 1 was last read by P V of tile gt - 2
+        wt = gt < 2 || __all_sync(0xffffffffu, mbar_wait(pv_done + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag));
+        if (wt) {
+          uint8_t* pb = pbuf(gt) + (r / 64) * Lay::kHChunkBytes + (r % 8) * 2;
+          const int pu = (r % 64) / 8;
+#pragma unroll
+          for (int h = 0; h < HS; ++h) {
+            const float pv = ex2_approx(x[h] - m[h]);  // masked keys: 0
+            lt[h] = fmaf(lt[h], alpha[h], pv);
+            uint16_t bits;
+            if constexpr (FP8) {
+              const __half ph = __float2half_rn(pv * sv);
+              bits = *reinterpret_cast<const uint16_t*>(&ph);
+            } else {
+              const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
+              bits = *reinterpret_cast<const uint16_t*>(&pb16);
+            }
+            sts_u16(pb + h * 128 + ((pu ^ (h & 7)) << 4), bits);
+          }
+        }
+        // m is the same in every thread, so bump is uniform
+        if (wt && i > 0 && bump) {
+          // O^T may only be touched once P V of tile gt - 1 has completed
+          wt = __all_sync(0xffffffffu, mbar_wait(pv_done + ((gt - 1) & 1), ((gt - 1) >> 1) & 1, abort_flag));
+          if (wt) {
+            tc_fence_after();
+            uint32_t ov[H];
+            tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
+#pragma unroll
+            for (int h = 0; h < HS; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+            tmem_st_x16(tmem_addr(tO, lane_base, 0), ov);
+            tmem_st_wait();
+          }
+        }
+        if (wt) {
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(p_ready + (gt & 1));
+        }
+        // a warp that gave up here stops arriving; the vote of the next tile
+        // (or the vote below) ends the loop for everyone
+        ok = wt;
+      }
+      if (!(ok = softmax_sync_and(ok))) {
+        if (lane == 0) give_up();
+        break;
+      }
+      // the next item's query: S^T of its first tiles runs during this epilogue
+      // (S^T of this item completed: its last scores were read above)
+      DecItem nx;
+      const long long w2 = next_item(p, w + gridDim.x, n_items, nx);
+      float inv_next[HS];
+#pragma unroll
+      for (int hh = 0; hh < HS; ++hh) inv_next[hh] = 1.f;
+      if (w2 < n_items) {
+        write_q(nx, inv_next);
+        load_scales(nx, 0, sk_next, sv_next);
+      }
+      // ---- the split's output: O^T / l, and its LSE
+#pragma unroll
+      for (int h = 0; h < HS; ++h) {
+        float xs = lt[h];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, off);
+        if (lane == 0) sRed[quad * H + h] = xs;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      // all four warps take the same way out: the next item has barriers
+      ok = softmax_sync_and(
+          __all_sync(0xffffffffu, mbar_wait(pv_done + ((gt - 1) & 1), ((gt - 1) >> 1) & 1, abort_flag)));
+      if (!ok) {
+        if (lane == 0) give_up();
+        break;
+      }
       tc_fence_after();
       uint32_t ov[H];
-      tmem_ld_x16(tmem_addr(tmem + Lay::kColO, lane_base, 0), ov);
-      const long long row0 = static_cast<long long>(b) * p.Hq + hq0;
+      tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
+      const long long row0 = static_cast<long long>(it.b) * p.Hq + static_cast<long long>(it.g) * group;
 #pragma unroll
       for (int h = 0; h < HS; ++h) {
         if (h < group) {
           const float l = sRed[h] + sRed[H + h] + sRed[2 * H + h] + sRed[3 * H + h];
-          p.o_part[((row0 + h) * p.n_splits + split) * D + r] = __uint_as_float(ov[h]) / l;
-          if (r == 0) p.lse_part[(row0 + h) * p.n_splits + split] = (m[h] + log2f(l)) * 0.6931471805599453f;
+          p.o_part[((row0 + h) * p.n_splits + it.split) * D + r] = __uint_as_float(ov[h]) / l;
+          if (r == 0) p.lse_part[(row0 + h) * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
         }
       }
+      // O^T buffer kq & 1 read: P V of item kq + 2 may write it
+      tc_fence_before();
+      mbar_arrive(o_free + (kq & 1));
+      it = nx;
+      w = w2;
+#pragma unroll
+      for (int hh = 0; hh < HS; ++hh) inv_sq[hh] = inv_next[hh];
+      ++kq;
     }
   } else if constexpr (FP8) {
     // ------------------------------------------------------------ converter warpgroup
@@ -904,12 +987,16 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // scales are applied elsewhere.
     const int r = (warp - 6) * 32 + lane;
     bool ok = true;
-    for (int i = 0; i < nt && ok; ++i) {
-      const int st = i % NS;
-      if (!(ok = mbar_wait(full + st, (i / NS) & 1, abort_flag))) break;
-      if (i >= 2 && !(ok = mbar_wait(pv_done + (i & 1), ((i - 2) >> 1) & 1, abort_flag))) break;
+    uint32_t gt = 0;  // tiles so far
+    DecItem it;
+    for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
+         w = next_item(p, w + gridDim.x, n_items, it))
+    for (int i = 0; i < it.nt && ok; ++i, ++gt) {
+      const uint32_t st = gt % NS;
+      if (!(ok = mbar_wait(full + st, (gt / NS) & 1, abort_flag))) break;
+      if (gt >= 2 && !(ok = mbar_wait(pv_done + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag))) break;
       const uint8_t* src = stage(st) + Lay::kTile8Bytes + r * 128;
-      uint8_t* dst = v16(i) + r * 128;
+      uint8_t* dst = v16(gt) + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint4 e = *reinterpret_cast<const uint4*>(src + ((u ^ (r & 7)) << 4));  // dims 16u .. 16u+15
@@ -926,7 +1013,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         *reinterpret_cast<uint4*>(chunk + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(v_ready + (i & 1));
+      mbar_arrive(v_ready + (gt & 1));
       mbar_arrive(empty + st);  // the V half of the E4M3 stage has been read
     }
     if (!ok) give_up();
@@ -1018,7 +1105,9 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
   auto kern = p.group <= 8 ? fa_decode_tc_kernel<FP8, 8> : fa_decode_tc_kernel<FP8, kDecHeads>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_splits, p.Hkv, p.B);
+  // persistent: one CTA per multiprocessor (or per item, if fewer)
+  const long long items = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(items, std::max(p.sms, 1)));
   kern<<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
