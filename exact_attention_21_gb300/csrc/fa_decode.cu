@@ -402,32 +402,44 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 //     O^T += V_tile^T P^T    M = d = 128,   N = 16 heads, K = 128 keys
 // so the threads only turn 16 scores per key into probabilities.  Roles:
 //   warp 0     TMA producer of the K / V stages.
-//   warp 1     TMEM allocator and MMA issuer (one thread).
+//   warp 1     TMEM allocator and P V issuer (one thread).
 //   warps 2-5  softmax warpgroup: thread = key row of S^T (TMEM lane) for the
 //              probabilities, and = dimension row of O^T for the rescale and
 //              the split's output.
-//   warps 6-9  (FP8 cache only) converter warpgroup: dequantises each E4M3
-//              V tile into a 16-bit tile in shared memory ("Attention 算子优化…",
-//              section 六: the cache stays FP8 in HBM, dequantisation happens
-//              on chip, softmax and accumulation in f32).
+//   warp 6     S^T issuer (one thread).
 // S^T is double-buffered in TMEM, so S^T of tile i+1 runs while the softmax
-// works on tile i; P^T (16-bit, K-major: 16 head rows x 128 keys) is
-// double-buffered in shared memory.  The running max of a head only moves
-// when a tile's max exceeds it by more than kDecRescaleSlack (log2 units);
-// any common reference gives the same merge, so this is exact and O^T is
-// rarely rescaled.
+// works on tile i; P^T (K-major: 16 head rows x 128 keys) is double-buffered
+// in shared memory.  The running max of a head only moves when a tile's max
+// exceeds it by more than a slack (log2 units); any common reference gives
+// the same merge, so this is exact and O^T is rarely rescaled.
 //
 // With the FP8 cache S^T reads the E4M3 K tile as it arrived, in a
 // kind::f8f6f4 MMA: each head's query is scaled by s_q = 448 / max|q| and
 // written as three E4M3 rows, q1 = e4m3(s_q q), q2 = e4m3(s_q q - q1) and
 // q3 = e4m3(s_q q - q1 - q2), which carry s_q q to about 2^-12 relative, so
 // S^T (N = 48: 16 columns per term) loses nothing a bf16 query would keep;
-// the softmax threads add the three columns of a head and divide by s_q.  P V runs in f16 over V dequantised to f16 (exact) with P
-// in f16.  The per-token scales fold into the per-key work of the softmax
-// threads: s_k multiplies the key's scores, s_v its probabilities before the
-// P V product (the row sum keeps the unscaled probabilities).
+// the softmax threads add the three columns of a head and divide by s_q.
+// P V reads the E4M3 V tile as it arrived too ("Attention 算子优化…", section
+// 六: the cache stays FP8 in HBM, softmax and accumulation in f32): a
+// kind::f8f6f4 MMA of V^T (MN-major) with P^T written as three E4M3 terms in
+// the same way, so the stage is the only copy of the tile on chip.  The
+// per-token scales fold into the per-key work of the softmax threads: s_k
+// multiplies the key's scores, s_v its probabilities before they are split
+// into terms (the row sum keeps the unscaled probabilities).  To keep the
+// terms in E4M3's normal range, s_v is taken relative to 2^E, E the largest
+// binary exponent of the scales seen so far (O^T is rescaled when E grows),
+// the probabilities are bounded by a slack of 2 instead of 8, and the
+// product is scaled by 2^6: the terms stay below 256 and the weights that
+// carry O at or above 2^-6, where three terms hold them to about 2^-12.
 constexpr int kDecHeads = 16;               // MMA N: query heads per CTA, padded
 constexpr float kDecRescaleSlack = 8.f;
+constexpr float kDecRescaleSlackFp8 = 2.f;
+constexpr int kDecPScaleLog2 = 6;           // FP8: P^T terms carry p s_v 2^(6 - e), e relative to 2^E
+
+// 2^e as a float for an integer e; 0 below -126.
+__device__ __forceinline__ float exp2i(int e) {
+  return e < -126 ? 0.f : __uint_as_float(static_cast<uint32_t>(min(e, 127) + 127) << 23);
+}
 
 template <bool FP8>
 struct DecTcLayout {
@@ -437,32 +449,34 @@ struct DecTcLayout {
   static constexpr int kTile8Bytes = kTile * 128;      // E4M3 128 x 128 tile (one 128-byte row per key)
   // TMA stages: 16-bit K and V tiles, or E4M3 K and V tiles
   static constexpr int kStageBytes = FP8 ? 2 * kTile8Bytes : 2 * kTileBytes;
-  static constexpr int kStages = FP8 ? 4 : 3;
-  // FP8: dequantised V, two buffers (freed when P V completes)
-  static constexpr int kCvtBytes = FP8 ? 2 * kTileBytes : 0;
-  static constexpr int kHChunkBytes = kDecHeads * 128;  // 16 rows x 64 16-bit elements
+  static constexpr int kStages = FP8 ? 6 : 3;
+  static constexpr int kHChunkBytes = kDecHeads * 128;  // 16 rows x 128 bytes
   // Q: 16 heads x 128 dims, K-major, bf16; FP8: 48 E4M3 rows (three terms per head) x 128 dims
   static constexpr int kQBytes = (FP8 ? 3 : 2) * kHChunkBytes;
-  static constexpr int kPBytes = 2 * kHChunkBytes;      // P^T: 16 heads x 128 keys, K-major
-  static constexpr int kOffCvt = kStages * kStageBytes;
-  static constexpr int kOffQ = kOffCvt + kCvtBytes;
+  // P^T: 16 heads x 128 keys, K-major, 16-bit; FP8: 48 E4M3 rows (three terms per head)
+  static constexpr int kPBytes = (FP8 ? 3 : 2) * kHChunkBytes;
+  static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffP = kOffQ + kQBytes;          // two buffers
   static constexpr int kOffRed = kOffP + 2 * kPBytes;    // f32 [4 warps][16 heads]
   static constexpr int kOffInvSq = kOffRed + 4 * kDecHeads * 4;  // FP8: f32 1 / s_q [16 heads]
-  static constexpr int kOffBar = kOffInvSq + kDecHeads * 4;
-  // full[], empty[], q_ready, s_full[2], p_ready[2], pv_done[2], drain, k_ready[2], v_ready[2]
-  static constexpr int kNumBars = 2 * kStages + 12;
+  static constexpr int kOffRedE = kOffInvSq + kDecHeads * 4;     // FP8: int [4 warps], scale exponents
+  static constexpr int kOffBar = kOffRedE + 16;
+  // full[], empty[], q_ready, s_full[2], p_ready[2], pv_done[2], drain, o_free[2]
+  static constexpr int kNumBars = 2 * kStages + 10;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
-  // warp 0 loads, warp 1 issues P V, warps 2-5 run the softmax, warps 6-9
-  // dequantise V (FP8), and the last warp issues S^T: a single thread
-  // issuing both would start one of these narrow MMAs only every ~100 cycles
-  static constexpr int kWarpS = FP8 ? 10 : 6;
+  // warp 0 loads, warp 1 issues P V, warps 2-5 run the softmax and warp 6
+  // issues S^T: a single thread issuing both would start one of these narrow
+  // MMAs only every ~100 cycles
+  static constexpr int kWarpS = 6;
   static constexpr int kThreads = 32 * (kWarpS + 1);
   // S^T buffers of kSCols columns at 0 and kSCols (FP8: a column per head and term), O^T after them
   static constexpr int kSCols = FP8 ? 3 * kDecHeads : kDecHeads;
-  static constexpr uint32_t kTmemCols = FP8 ? 128 : 64;
+  // O^T: a column per head (FP8: per head and term), two buffers
+  static constexpr int kOCols = kSCols;
+  static constexpr uint32_t kTmemCols = FP8 ? 256 : 64;
   static constexpr uint32_t kColS = 0, kColO = 2 * kSCols;
+  static_assert(kColO + 2 * kOCols <= kTmemCols, "TMEM budget");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -536,10 +550,10 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   constexpr int NS = Lay::kStages;
   constexpr int D = Lay::D;
   constexpr int H = kDecHeads;
-  // the MMAs read 16-bit operands: bf16 for a bf16 cache, f16 for an E4M3 one
-  // S^T: E4M3 K x the E4M3 query terms for an FP8 cache, bf16 otherwise; P V: 16-bit
+  // bf16 cache: bf16 MMAs; E4M3 cache: E4M3 K x the query's E4M3 terms, and
+  // E4M3 V^T (MN-major) x the E4M3 terms of P^T
   constexpr uint32_t id_s = FP8 ? idesc_e4m3_f32(kTile, 3 * H) : idesc_bf16_f32(kTile, H, false, false);
-  constexpr uint32_t id_o = FP8 ? idesc_f16_f32(D, H, true, false) : idesc_bf16_f32(D, H, true, false);
+  constexpr uint32_t id_o = FP8 ? idesc_e4m3_f32(D, 3 * H, true) : idesc_bf16_f32(D, H, true, false);
 
   // persistent: the CTA runs its items back to back; the barrier rings and
   // the S^T / P^T / V buffers run on a tile count over all of them (gt), so
@@ -558,31 +572,26 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint64_t* p_ready = s_full + 2;
   uint64_t* pv_done = p_ready + 2;  // FP8: also frees dequantised V buffer i & 1
   uint64_t* drain = pv_done + 2;
-  uint64_t* v_ready = drain + 1;     // FP8 only: dequantised V of tile i in buffer i & 1
-  uint64_t* o_free = v_ready + 2;    // O^T buffer j read by the epilogue of an item
+  uint64_t* o_free = drain + 1;      // O^T buffer j read by the epilogue of an item
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
   auto stage = [&](uint32_t st) { return smem + st * Lay::kStageBytes; };
   auto pbuf = [&](uint32_t i) { return smem + Lay::kOffP + (i & 1) * Lay::kPBytes; };
-  // the K tile S^T of tile i reads (E4M3 for an FP8 cache) and the 16-bit V tile of P V
+  // the K and V tiles of tile i (E4M3 for an FP8 cache)
   auto ktile = [&](uint32_t i) { return stage(i % NS); };
-  auto v16 = [&](uint32_t i) {
-    return FP8 ? smem + Lay::kOffCvt + (i & 1) * Lay::kTileBytes : stage(i % NS) + Lay::kTileBytes;
-  };
+  auto vtile = [&](uint32_t i) { return stage(i % NS) + (FP8 ? Lay::kTile8Bytes : Lay::kTileBytes); };
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full + i, 1);
-      // FP8: released by S^T's commit (K) and the converter warpgroup (V)
-      mbar_init(empty + i, FP8 ? 129 : 1);
+      mbar_init(empty + i, 1);  // P V of the tile completed (after its S^T)
     }
     mbar_init(q_ready, 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_ready + i, 128);
       mbar_init(pv_done + i, 1);
-      mbar_init(v_ready + i, 128);
       mbar_init(o_free + i, 128);
     }
     mbar_init(drain, 2);  // both MMA-issuing threads commit
@@ -646,21 +655,29 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
            w = next_item(p, w + gridDim.x, n_items, it), ++kq) {
         // O^T buffer kq & 1 was last read by the epilogue of item kq - 2
         if (kq >= 2 && !(ok = mbar_wait(o_free + (kq & 1), ((kq - 2) >> 1) & 1, abort_flag))) break;
-        const uint32_t tO = tmem + Lay::kColO + (kq & 1) * H;
+        const uint32_t tO = tmem + Lay::kColO + (kq & 1) * Lay::kOCols;
         for (int i = 0; i < it.nt; ++i, ++gt) {
           // P^T of tile gt written, S^T buffer gt & 1 read, O^T rescaled
           if (!(ok = mbar_wait(p_ready + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
-          if (FP8 && !(ok = mbar_wait(v_ready + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
           tc_fence_after();
-          const uint32_t sVa = smem_u32(v16(gt)), sPa = smem_u32(pbuf(gt));
+          const uint32_t sVa = smem_u32(vtile(gt)), sPa = smem_u32(pbuf(gt));
+          if constexpr (FP8) {
+            // V^T: one 128-byte row of dimensions per key, 8-key groups 1 KB
+            // apart; P^T: 48 rows of 128 keys; 32 keys per step
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_ss(tO, sdesc_sw128(sVa + kk * 2048, Lay::kChunkBytes, 1024),
-                    sdesc_sw128(sPa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_o,
-                    (i > 0 || kk > 0));
+            for (int kk = 0; kk < kTile / 32; ++kk)
+              umma_ss_f8(tO, sdesc_sw128(sVa + kk * 4096, 16, 1024), sdesc_sw128(sPa + kk * 32, 16, 1024), id_o,
+                         (i > 0 || kk > 0));
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_ss(tO, sdesc_sw128(sVa + kk * 2048, Lay::kChunkBytes, 1024),
+                      sdesc_sw128(sPa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_o,
+                      (i > 0 || kk > 0));
+          }
           // the stage's K was read by S^T of tile gt, complete before the
           // softmax released P^T of tile gt
-          if constexpr (!FP8) umma_commit(empty + gt % NS);
+          umma_commit(empty + gt % NS);
           umma_commit(pv_done + (gt & 1));
         }
       }
@@ -700,7 +717,6 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                       sdesc_sw128(sQa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_s, kk > 0);
           }
           umma_commit(s_full + (gt & 1));
-          if constexpr (FP8) umma_commit(empty + gt % NS);  // the K half of the stage has been read
         }
       }
       if (!ok) give_up();
@@ -715,6 +731,13 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
     const int group = p.group;
     const float c = p.scale_log2;
+    constexpr float kSlack = FP8 ? kDecRescaleSlackFp8 : kDecRescaleSlack;
+    int* sRedE = reinterpret_cast<int*>(smem + Lay::kOffRedE);
+    // P^T rows of the padded heads are read by the MMA but never used: zero
+    // them once (all of both buffers)
+    for (int j = r; j < 2 * Lay::kPBytes / 16; j += 128)
+      reinterpret_cast<uint4*>(smem + Lay::kOffP)[j] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     // The item's query into sQ (K-major, 128-byte swizzle, padded heads 0) and,
     // FP8, 1 / s_q of each head into isq; then q_ready.
     auto write_q = [&](const DecItem& it, float (&isq)[HS]) {
@@ -816,7 +839,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       load_scales(it, 0, sk_next, sv_next);
     }
     while (w < n_items && ok) {
-      const uint32_t tO = tmem + Lay::kColO + (kq & 1) * H;
+      const uint32_t tO = tmem + Lay::kColO + (kq & 1) * Lay::kOCols;
+      int E = 0;  // FP8: largest biased exponent of the item's V scales so far
       float m[HS], lt[HS];
 #pragma unroll
       for (int h = 0; h < HS; ++h) {
@@ -828,6 +852,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const bool valid = kpos < it.L;
         const float sk = sk_next, sv = sv_next;
         load_scales(it, i + 1, sk_next, sv_next);
+        const uint32_t svb = __float_as_uint(sv);
+        const int ei = (FP8 && valid) ? static_cast<int>((svb >> 23) & 0xffu) : 0;  // masked keys: none
         bool wt = __all_sync(0xffffffffu, mbar_wait(s_full + (gt & 1), (gt >> 1) & 1, abort_flag));
         float x[HS];
         bool over = false;  // a score above its head's reference by more than the slack
@@ -851,10 +877,12 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
           for (int h = 0; h < HS; ++h) {
             x[h] = valid ? sc[h] * ck : -INFINITY;
-            over |= x[h] > m[h] + kDecRescaleSlack;  // always for a valid key on the first tile (m = -inf)
+            over |= x[h] > m[h] + kSlack;  // always for a valid key on the first tile (m = -inf)
           }
+          over |= ei > E;
         }
         bool bump = false;
+        float beta = 1.f;  // FP8: O^T's factor for a larger E
         float alpha[HS];
 #pragma unroll
         for (int h = 0; h < HS; ++h) alpha[h] = 1.f;
@@ -871,37 +899,71 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             if (lane == 0) sRed[quad * H + h] = mx;
           }
+          if constexpr (FP8) {
+            const int em = __reduce_max_sync(0xffffffffu, ei);
+            if (lane == 0) sRedE[quad] = em;
+          }
           asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
           for (int h = 0; h < HS; ++h) {
             const float tm = fmaxf(fmaxf(sRed[h], sRed[H + h]), fmaxf(sRed[2 * H + h], sRed[3 * H + h]));
             // the tile's key 0 is valid, so tm is finite
-            const bool up = tm > m[h] + kDecRescaleSlack;
+            const bool up = tm > m[h] + kSlack;
             const float mn = up ? tm : m[h];
             alpha[h] = up ? ex2_approx(m[h] - mn) : 1.f;
             bump |= up;
             m[h] = mn;
+          }
+          if constexpr (FP8) {
+            const int te = max(max(sRedE[0], sRedE[1]), max(sRedE[2], sRedE[3]));
+            if (te > E) {
+              beta = exp2i(E - te);
+              bump = true;
+              E = te;
+            }
           }
           asm volatile("bar.sync 1, 128;" ::: "memory");  // sRed is rewritten by the next reduction
         }
         // P^T buffer gt & 1 was last read by P V of tile gt - 2
         wt = gt < 2 || __all_sync(0xffffffffu, mbar_wait(pv_done + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag));
         if (wt) {
-          uint8_t* pb = pbuf(gt) + (r / 64) * Lay::kHChunkBytes + (r % 8) * 2;
-          const int pu = (r % 64) / 8;
+          if constexpr (FP8) {
+            // s_v 2^(6 + 126 - E): the scale's exponent moved relative to 2^E
+            // (below 64); 0 for a masked key or one 2^126 below the largest
+            const int ne = ei + kDecPScaleLog2 + 126 - E;
+            const float svs = (ei > 0 && ne > 0) ? __uint_as_float((static_cast<uint32_t>(ne) << 23) | (svb & 0x7fffffu))
+                                                 : 0.f;
+            // P^T row t * 16 + h, key r: 16-byte unit r / 16 of the row, swizzled
+            uint8_t* pb = pbuf(gt) + (r & 15);
 #pragma unroll
-          for (int h = 0; h < HS; ++h) {
-            const float pv = ex2_approx(x[h] - m[h]);  // masked keys: 0
-            lt[h] = fmaf(lt[h], alpha[h], pv);
-            uint16_t bits;
-            if constexpr (FP8) {
-              const __half ph = __float2half_rn(pv * sv);
-              bits = *reinterpret_cast<const uint16_t*>(&ph);
-            } else {
-              const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
-              bits = *reinterpret_cast<const uint16_t*>(&pb16);
+            for (int h = 0; h < HS; h += 2) {
+              const float p0 = ex2_approx(x[h] - m[h]), p1 = ex2_approx(x[h + 1] - m[h + 1]);  // masked keys: 0
+              lt[h] = fmaf(lt[h], alpha[h], p0);
+              lt[h + 1] = fmaf(lt[h + 1], alpha[h + 1], p1);
+              float2 y = make_float2(p0 * svs, p1 * svs);  // below 256: no saturation
+#pragma unroll
+              for (int t = 0; t < 3; ++t) {
+                const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+                if (t < 2) {
+                  const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(c2, __NV_E4M3);
+                  y.x -= __half2float(*reinterpret_cast<const __half*>(&hb.x));  // exact in f32
+                  y.y -= __half2float(*reinterpret_cast<const __half*>(&hb.y));
+                }
+                const int row0 = t * kDecHeads + h;
+                pb[row0 * 128 + ((((r >> 4) ^ (row0 & 7))) << 4)] = static_cast<uint8_t>(c2 & 0xffu);
+                pb[(row0 + 1) * 128 + ((((r >> 4) ^ ((row0 + 1) & 7))) << 4)] = static_cast<uint8_t>(c2 >> 8);
+              }
             }
-            sts_u16(pb + h * 128 + ((pu ^ (h & 7)) << 4), bits);
+          } else {
+            uint8_t* pb = pbuf(gt) + (r / 64) * Lay::kHChunkBytes + (r % 8) * 2;
+            const int pu = (r % 64) / 8;
+#pragma unroll
+            for (int h = 0; h < HS; ++h) {
+              const float pv = ex2_approx(x[h] - m[h]);  // masked keys: 0
+              lt[h] = fmaf(lt[h], alpha[h], pv);
+              const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
+              sts_u16(pb + h * 128 + ((pu ^ (h & 7)) << 4), *reinterpret_cast<const uint16_t*>(&pb16));
+            }
           }
         }
         // m is the same in every thread, so bump is uniform
@@ -910,11 +972,22 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           wt = __all_sync(0xffffffffu, mbar_wait(pv_done + ((gt - 1) & 1), ((gt - 1) >> 1) & 1, abort_flag));
           if (wt) {
             tc_fence_after();
-            uint32_t ov[H];
-            tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
+            uint32_t ov[Lay::kOCols];
+            if constexpr (FP8) {
+              tmem_ld_x16_x32_pair(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H, tmem_addr(tO, lane_base, 0), ov);
 #pragma unroll
-            for (int h = 0; h < HS; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-            tmem_st_x16(tmem_addr(tO, lane_base, 0), ov);
+              for (int t = 0; t < 3; ++t)
+#pragma unroll
+                for (int h = 0; h < HS; ++h)
+                  ov[t * H + h] = __float_as_uint(__uint_as_float(ov[t * H + h]) * (alpha[h] * beta));
+              tmem_st_x32(tmem_addr(tO, lane_base, 0), ov);
+              tmem_st_x16(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H);
+            } else {
+              tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
+#pragma unroll
+              for (int h = 0; h < HS; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+              tmem_st_x16(tmem_addr(tO, lane_base, 0), ov);
+            }
             tmem_st_wait();
           }
         }
@@ -959,14 +1032,27 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         break;
       }
       tc_fence_after();
-      uint32_t ov[H];
-      tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
+      uint32_t ov[Lay::kOCols];
+      float osum[HS];
+      if constexpr (FP8) {
+        tmem_ld_x16_x32_pair(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H, tmem_addr(tO, lane_base, 0), ov);
+        // the terms' sum times 2^(E - 126 - 6), in two exact steps
+        const int e = E - 126 - kDecPScaleLog2, e1 = e / 2;
+        const float f1 = exp2i(e1), f2 = exp2i(e - e1);
+#pragma unroll
+        for (int h = 0; h < HS; ++h)
+          osum[h] = ((__uint_as_float(ov[h]) + __uint_as_float(ov[H + h]) + __uint_as_float(ov[2 * H + h])) * f1) * f2;
+      } else {
+        tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
+#pragma unroll
+        for (int h = 0; h < HS; ++h) osum[h] = __uint_as_float(ov[h]);
+      }
       const long long row0 = static_cast<long long>(it.b) * p.Hq + static_cast<long long>(it.g) * group;
 #pragma unroll
       for (int h = 0; h < HS; ++h) {
         if (h < group) {
           const float l = sRed[h] + sRed[H + h] + sRed[2 * H + h] + sRed[3 * H + h];
-          p.o_part[((row0 + h) * p.n_splits + it.split) * D + r] = __uint_as_float(ov[h]) / l;
+          p.o_part[((row0 + h) * p.n_splits + it.split) * D + r] = osum[h] / l;
           if (r == 0) p.lse_part[(row0 + h) * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
         }
       }
@@ -979,44 +1065,6 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       for (int hh = 0; hh < HS; ++hh) inv_sq[hh] = inv_next[hh];
       ++kq;
     }
-  } else if constexpr (FP8) {
-    // ------------------------------------------------------------ converter warpgroup
-    // Thread r dequantises key row r of the tile's V: 8 units of 16 E4M3 codes
-    // each, into 16 f16 units of the 128-byte-swizzled 16-bit tile P V reads
-    // (buffer i & 1, once P V of tile i - 2 is done with it).  The per-token
-    // scales are applied elsewhere.
-    const int r = (warp - 6) * 32 + lane;
-    bool ok = true;
-    uint32_t gt = 0;  // tiles so far
-    DecItem it;
-    for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
-         w = next_item(p, w + gridDim.x, n_items, it))
-    for (int i = 0; i < it.nt && ok; ++i, ++gt) {
-      const uint32_t st = gt % NS;
-      if (!(ok = mbar_wait(full + st, (gt / NS) & 1, abort_flag))) break;
-      if (gt >= 2 && !(ok = mbar_wait(pv_done + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag))) break;
-      const uint8_t* src = stage(st) + Lay::kTile8Bytes + r * 128;
-      uint8_t* dst = v16(gt) + r * 128;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 e = *reinterpret_cast<const uint4*>(src + ((u ^ (r & 7)) << 4));  // dims 16u .. 16u+15
-        const uint32_t w[4] = {e.x, e.y, e.z, e.w};
-        uint32_t h16[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          h16[2 * j] = e4m3x2_to_f16x2(w[j]);
-          h16[2 * j + 1] = e4m3x2_to_f16x2(w[j] >> 16);
-        }
-        uint8_t* chunk = dst + (u / 4) * Lay::kChunkBytes;
-        const int u0 = 2 * (u % 4);
-        *reinterpret_cast<uint4*>(chunk + ((u0 ^ (r & 7)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-        *reinterpret_cast<uint4*>(chunk + (((u0 + 1) ^ (r & 7)) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(v_ready + (gt & 1));
-      mbar_arrive(empty + st);  // the V half of the E4M3 stage has been read
-    }
-    if (!ok) give_up();
   }
 
   tc_fence_before();

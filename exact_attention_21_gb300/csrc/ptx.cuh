@@ -225,9 +225,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 }
 
 // kind::f8f6f4 with E4M3 A and B (format value 0 in bits 7-9 and 10-12),
-// both K-major, f32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// B K-major, A K-major or MN-major, f32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major = false) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // The same for f16 A and B (format value 0 in bits 7-9 and 10-12).
