@@ -456,13 +456,18 @@ struct DecTcLayout {
   // P^T: 16 heads x 128 keys, K-major, 16-bit; FP8: 48 E4M3 rows (three terms per head)
   static constexpr int kPBytes = (FP8 ? 3 : 2) * kHChunkBytes;
   static constexpr int kOffQ = kStages * kStageBytes;
-  static constexpr int kOffP = kOffQ + kQBytes;          // two buffers
-  static constexpr int kOffRed = kOffP + 2 * kPBytes;    // f32 [4 warps][16 heads]
-  static constexpr int kOffInvSq = kOffRed + 4 * kDecHeads * 4;  // FP8: f32 1 / s_q [16 heads]
-  static constexpr int kOffRedE = kOffInvSq + kDecHeads * 4;     // FP8: int [4 warps], scale exponents
-  static constexpr int kOffBar = kOffRedE + 16;
-  // full[], empty[], q_ready, s_full[2], p_ready[2], pv_done[2], drain, o_free[2]
-  static constexpr int kNumBars = 2 * kStages + 10;
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;      // Q: two buffers (this item's, the next one's)
+  static constexpr int kOffRed = kOffP + 2 * kPBytes;    // P^T: two buffers; f32 [4 warps][16 heads]
+  static constexpr int kOffInvSq = kOffRed + 4 * kDecHeads * 4;  // FP8: f32 1 / s_q [2 buffers][16 heads]
+  static constexpr int kOffRedE = kOffInvSq + 2 * kDecHeads * 4;  // FP8: int [4 warps], scale exponents
+  // FP8: per-token scales (s_k, s_v) of the 128 keys of the next kScaleAhead tiles
+  static constexpr int kScaleAhead = 4;
+  static constexpr int kOffScale = kOffRedE + 16;
+  static constexpr int kOffBar = kOffScale + (FP8 ? kScaleAhead * kTile * 8 : 0);
+  // S^T buffers in TMEM: S^T runs up to three tiles ahead of the softmax
+  static constexpr int kSBufs = 3;
+  // full[], empty[], q_ready, s_full[3], p_ready[3], pv_done[2], drain, o_free[2]
+  static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
   // warp 0 loads, warp 1 issues P V, warps 2-5 run the softmax and warp 6
@@ -470,12 +475,12 @@ struct DecTcLayout {
   // MMAs only every ~100 cycles
   static constexpr int kWarpS = 6;
   static constexpr int kThreads = 32 * (kWarpS + 1);
-  // S^T buffers of kSCols columns at 0 and kSCols (FP8: a column per head and term), O^T after them
+  // S^T buffers of kSCols columns from 0 (FP8: a column per head and term), O^T after them
   static constexpr int kSCols = FP8 ? 3 * kDecHeads : kDecHeads;
   // O^T: a column per head (FP8: per head and term), two buffers
   static constexpr int kOCols = kSCols;
-  static constexpr uint32_t kTmemCols = FP8 ? 256 : 64;
-  static constexpr uint32_t kColS = 0, kColO = 2 * kSCols;
+  static constexpr uint32_t kTmemCols = FP8 ? 256 : 128;
+  static constexpr uint32_t kColS = 0, kColO = kSBufs * kSCols;
   static_assert(kColO + 2 * kOCols <= kTmemCols, "TMEM budget");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
@@ -569,8 +574,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint64_t* empty = full + NS;
   uint64_t* q_ready = empty + NS;
   uint64_t* s_full = q_ready + 1;
-  uint64_t* p_ready = s_full + 2;
-  uint64_t* pv_done = p_ready + 2;  // FP8: also frees dequantised V buffer i & 1
+  uint64_t* p_ready = s_full + Lay::kSBufs;
+  uint64_t* pv_done = p_ready + Lay::kSBufs;
   uint64_t* drain = pv_done + 2;
   uint64_t* o_free = drain + 1;      // O^T buffer j read by the epilogue of an item
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
@@ -588,9 +593,11 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       mbar_init(empty + i, 1);  // P V of the tile completed (after its S^T)
     }
     mbar_init(q_ready, 128);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < Lay::kSBufs; ++i) {
       mbar_init(s_full + i, 1);
       mbar_init(p_ready + i, 128);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(pv_done + i, 1);
       mbar_init(o_free + i, 128);
     }
@@ -657,8 +664,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (kq >= 2 && !(ok = mbar_wait(o_free + (kq & 1), ((kq - 2) >> 1) & 1, abort_flag))) break;
         const uint32_t tO = tmem + Lay::kColO + (kq & 1) * Lay::kOCols;
         for (int i = 0; i < it.nt; ++i, ++gt) {
-          // P^T of tile gt written, S^T buffer gt & 1 read, O^T rescaled
-          if (!(ok = mbar_wait(p_ready + (gt & 1), (gt >> 1) & 1, abort_flag))) break;
+          // P^T of tile gt written, S^T buffer gt % 3 read, O^T rescaled
+          if (!(ok = mbar_wait(p_ready + gt % Lay::kSBufs, (gt / Lay::kSBufs) & 1, abort_flag))) break;
           tc_fence_after();
           const uint32_t sVa = smem_u32(vtile(gt)), sPa = smem_u32(pbuf(gt));
           if constexpr (FP8) {
@@ -689,21 +696,23 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   } else if (warp == Lay::kWarpS) {
     // ------------------------------------------------------------ S^T issuer
     if (lane == 0) {
-      const uint32_t sQa = smem_u32(sQ);
       bool ok = true;
       uint32_t gt = 0, kq = 0;  // tiles and items so far
       DecItem it;
       for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
            w = next_item(p, w + gridDim.x, n_items, it), ++kq) {
-        // the item's query (written once S^T of the previous item completed)
+        // the item's query, in buffer kq & 1
         if (!(ok = mbar_wait(q_ready, kq & 1, abort_flag))) break;
+        const uint32_t sQa = smem_u32(sQ + (kq & 1) * Lay::kQBytes);
         for (int i = 0; i < it.nt; ++i, ++gt) {
-          // S^T buffer gt & 1 was read by the softmax of tile gt - 2 once it released P^T
-          if (gt >= 2 && !(ok = mbar_wait(p_ready + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag))) break;
+          // S^T buffer gt % 3 was read by the softmax of tile gt - 3 once it released P^T
+          if (gt >= Lay::kSBufs && !(ok = mbar_wait(p_ready + gt % Lay::kSBufs, ((gt - Lay::kSBufs) / Lay::kSBufs) & 1,
+                                                    abort_flag)))
+            break;
           if (!(ok = mbar_wait(full + gt % NS, (gt / NS) & 1, abort_flag))) break;
           tc_fence_after();
           const uint32_t sKa = smem_u32(ktile(gt));
-          const uint32_t tS = tmem + Lay::kColS + (gt & 1) * Lay::kSCols;
+          const uint32_t tS = tmem + Lay::kColS + (gt % Lay::kSBufs) * Lay::kSCols;
           if constexpr (FP8) {
             // E4M3 K (one 128-byte row per key) x the 48 E4M3 query rows, 32 elements per step
 #pragma unroll
@@ -716,7 +725,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
               umma_ss(tS, sdesc_sw128(sKa + (kk / 4) * Lay::kChunkBytes + (kk % 4) * 32, 16, 1024),
                       sdesc_sw128(sQa + (kk / 4) * Lay::kHChunkBytes + (kk % 4) * 32, 16, 1024), id_s, kk > 0);
           }
-          umma_commit(s_full + (gt & 1));
+          umma_commit(s_full + gt % Lay::kSBufs);
         }
       }
       if (!ok) give_up();
@@ -738,29 +747,34 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     for (int j = r; j < 2 * Lay::kPBytes / 16; j += 128)
       reinterpret_cast<uint4*>(smem + Lay::kOffP)[j] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
-    // The item's query into sQ (K-major, 128-byte swizzle, padded heads 0) and,
-    // FP8, 1 / s_q of each head into isq; then q_ready.
-    auto write_q = [&](const DecItem& it, float (&isq)[HS]) {
-      const int hq0 = it.g * group;
+    // An item's query: thread r holds dims 16 (r % 8) .. +15 of head r / 8
+    // (two 16-byte units; 0 past the group), fetched an item ahead.
+    auto fetch_q = [&](const DecItem& it, uint4 (&qa)[2]) {
+      const int h = r / 8;
+      if (h < group) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                          (static_cast<long long>(it.b) * p.Hq + it.g * group + h) * D +
+                                                          16 * (r % 8));
+        qa[0] = __ldg(src);
+        qa[1] = __ldg(src + 1);
+      } else {
+        qa[0] = qa[1] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    // ... written into Q buffer qb (K-major, 128-byte swizzle), FP8 with
+    // 1 / s_q of each head, then q_ready.  Buffer qb was last read by S^T of
+    // the item before the previous one.
+    auto store_q = [&](int qb, const uint4 (&qa)[2]) {
+      uint8_t* q = sQ + qb * Lay::kQBytes;
+      const int h = r / 8, sub = r % 8;
       if constexpr (FP8) {
-        // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h; thread r
-        // takes dims 16 (r % 8) .. +15 of head r / 8 (one 16-byte unit per row)
-        const int h = r / 8, sub = r % 8;
+        // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h
+        const uint32_t wq[8] = {qa[0].x, qa[0].y, qa[0].z, qa[0].w, qa[1].x, qa[1].y, qa[1].z, qa[1].w};
         float v[16];
-        if (h < group) {
-          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                            (static_cast<long long>(it.b) * p.Hq + hq0 + h) * D +
-                                                            16 * sub);
-          const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
-          const uint32_t wq[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            v[2 * e] = bf16_lo(wq[e]);
-            v[2 * e + 1] = bf16_hi(wq[e]);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = 0.f;
+        for (int e = 0; e < 8; ++e) {
+          v[2 * e] = bf16_lo(wq[e]);
+          v[2 * e + 1] = bf16_hi(wq[e]);
         }
         float amax = 0.f;
 #pragma unroll
@@ -785,45 +799,39 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
           const int row = t * kDecHeads + h;
-          *reinterpret_cast<uint4*>(sQ + row * 128 + ((sub ^ (row & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(q + row * 128 + ((sub ^ (row & 7)) << 4)) =
               make_uint4(term[t][0], term[t][1], term[t][2], term[t][3]);
         }
-        float* sInvSq = reinterpret_cast<float*>(smem + Lay::kOffInvSq);
-        if (sub == 0) sInvSq[h] = 1.f / sq;
-        fence_proxy_async_smem();
-        mbar_arrive(q_ready);
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // every head's 1 / s_q written
-#pragma unroll
-        for (int hh = 0; hh < HS; ++hh) isq[hh] = sInvSq[hh];
+        if (sub == 0) reinterpret_cast<float*>(smem + Lay::kOffInvSq)[qb * kDecHeads + h] = 1.f / sq;
       } else {
-        const int h = r / 8, u2 = (r % 8) * 2;  // 8 threads per head row, two 16-byte units each
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                          (static_cast<long long>(it.b) * p.Hq + hq0 + h) * D);
+        // units 2 sub, 2 sub + 1 of the 256-byte row: chunk u / 8, unit u % 8
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int u = u2 + j;  // unit of the 256-byte row: chunk u / 8, unit u % 8
-          const uint4 val = h < group ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(sQ + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = val;
+          const int u = 2 * sub + j;
+          *reinterpret_cast<uint4*>(q + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = qa[j];
         }
-        fence_proxy_async_smem();
-        mbar_arrive(q_ready);
-#pragma unroll
-        for (int hh = 0; hh < HS; ++hh) isq[hh] = 1.f;
       }
+      fence_proxy_async_smem();
+      mbar_arrive(q_ready);
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // FP8: every head's 1 / s_q written
     };
-    // per-token scales of this thread's key in tile i of an item (FP8 cache),
-    // loaded a tile ahead: through a page table they are two dependent loads
-    auto load_scales = [&](const DecItem& it, int i, float& sk, float& sv) {
-      sk = 1.f;
-      sv = 1.f;
-      if constexpr (FP8) {
-        const int kpos = (it.t0 + i) * kTile + r;
-        if (i < it.nt && kpos < it.L) {
-          const long long si = decode_row(p, it.b, it.seq0, kpos, it.L) * p.Hkv + it.g;
-          sk = __ldg(p.k_scale + si);
-          sv = __ldg(p.v_scale + si);
-        }
+    // FP8: per-token scales of this thread's key, copied (cp.async) into slot
+    // gt % kScaleAhead of a ring kScaleAhead tiles ahead of their use: in a
+    // saturated memory system a load takes several tiles' time.  One copy
+    // group per tile, empty or not; bit j of pf: slot j holds copies.
+    constexpr int kAhead = Lay::kScaleAhead;
+    float2* sScale = reinterpret_cast<float2*>(smem + Lay::kOffScale);
+    uint32_t pf = 0;
+    auto issue_scales = [&](const DecItem& t, int i, uint32_t slot) {
+      pf &= ~(1u << slot);
+      const int kpos = (t.t0 + i) * kTile + r;
+      if (i < t.nt && kpos < t.L) {
+        const long long si = decode_row(p, t.b, t.seq0, kpos, t.L) * p.Hkv + t.g;
+        cp_async_4(&sScale[slot * kTile + r].x, p.k_scale + si);
+        cp_async_4(&sScale[slot * kTile + r].y, p.v_scale + si);
+        pf |= 1u << slot;
       }
+      cp_async_commit();
     };
     // A wait that gives up must not leave the other threads at a barrier:
     // results of waits are made warp-uniform (the shuffles and TMEM accesses
@@ -832,13 +840,26 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     uint32_t gt = 0, kq = 0;  // tiles and items so far
     DecItem it;
     long long w = next_item(p, blockIdx.x, n_items, it);
-    float inv_sq[HS];  // FP8: 1 / s_q of each head
-    float sk_next = 1.f, sv_next = 1.f;
     if (w < n_items) {
-      write_q(it, inv_sq);
-      load_scales(it, 0, sk_next, sv_next);
+      uint4 qa[2];
+      fetch_q(it, qa);
+      store_q(0, qa);
+      if constexpr (FP8) {
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j) issue_scales(it, j, j);
+      }
     }
     while (w < n_items && ok) {
+      float inv_sq[HS];  // FP8: 1 / s_q of each head
+#pragma unroll
+      for (int hh = 0; hh < HS; ++hh)
+        inv_sq[hh] = FP8 ? reinterpret_cast<const float*>(smem + Lay::kOffInvSq)[(kq & 1) * kDecHeads + hh] : 1.f;
+      // the next item's query: fetched now, stored once this item's first tile
+      // is done, so that S^T can run into the next item ahead of the softmax
+      DecItem nx;
+      const long long w2 = next_item(p, w + gridDim.x, n_items, nx);
+      uint4 qn[2] = {};
+      if (w2 < n_items) fetch_q(nx, qn);
       const uint32_t tO = tmem + Lay::kColO + (kq & 1) * Lay::kOCols;
       int E = 0;  // FP8: largest biased exponent of the item's V scales so far
       float m[HS], lt[HS];
@@ -850,11 +871,36 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       for (int i = 0; i < it.nt; ++i, ++gt) {
         const int kpos = (it.t0 + i) * kTile + r;
         const bool valid = kpos < it.L;
-        const float sk = sk_next, sv = sv_next;
-        load_scales(it, i + 1, sk_next, sv_next);
+        float sk = 1.f, sv = 1.f;
+        if constexpr (FP8) {
+          const uint32_t slot = gt % kAhead;
+          cp_async_wait<kAhead - 1>();  // this tile's group
+          if (valid) {
+            if ((pf >> slot) & 1u) {
+              const float2 s2 = sScale[slot * kTile + r];
+              sk = s2.x;
+              sv = s2.y;
+            } else {  // a tile the ring did not reach (items shorter than the ring)
+              const long long si = decode_row(p, it.b, it.seq0, kpos, it.L) * p.Hkv + it.g;
+              sk = __ldg(p.k_scale + si);
+              sv = __ldg(p.v_scale + si);
+            }
+          }
+          // the slot's next tile, gt + kAhead: of this item or of the next
+          const int j = i + kAhead;
+          if (j < it.nt) {
+            issue_scales(it, j, slot);
+          } else if (w2 < n_items) {
+            issue_scales(nx, j - it.nt, slot);
+          } else {
+            pf &= ~(1u << slot);
+            cp_async_commit();
+          }
+        }
         const uint32_t svb = __float_as_uint(sv);
         const int ei = (FP8 && valid) ? static_cast<int>((svb >> 23) & 0xffu) : 0;  // masked keys: none
-        bool wt = __all_sync(0xffffffffu, mbar_wait(s_full + (gt & 1), (gt >> 1) & 1, abort_flag));
+        const uint32_t sb = gt % Lay::kSBufs;
+        bool wt = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (gt / Lay::kSBufs) & 1, abort_flag));
         float x[HS];
         bool over = false;  // a score above its head's reference by more than the slack
         if (wt) {
@@ -862,14 +908,14 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           uint32_t svv[Lay::kSCols];
           float sc[HS];
           if constexpr (FP8) {
-            const uint32_t ts = tmem + Lay::kColS + (gt & 1) * Lay::kSCols;
+            const uint32_t ts = tmem + Lay::kColS + sb * Lay::kSCols;
             tmem_ld_x16_x32_pair(tmem_addr(ts, lane_base, 2 * H), svv + 2 * H, tmem_addr(ts, lane_base, 0), svv);
 #pragma unroll
             for (int h = 0; h < HS; ++h)
               sc[h] = (__uint_as_float(svv[h]) + __uint_as_float(svv[H + h]) + __uint_as_float(svv[2 * H + h])) *
                       inv_sq[h];
           } else {
-            tmem_ld_x16(tmem_addr(tmem + Lay::kColS + (gt & 1) * Lay::kSCols, lane_base, 0), svv);
+            tmem_ld_x16(tmem_addr(tmem + Lay::kColS + sb * Lay::kSCols, lane_base, 0), svv);
 #pragma unroll
             for (int h = 0; h < HS; ++h) sc[h] = __uint_as_float(svv[h]);
           }
@@ -994,26 +1040,17 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (wt) {
           fence_proxy_async_smem();
           tc_fence_before();
-          mbar_arrive(p_ready + (gt & 1));
+          mbar_arrive(p_ready + sb);
         }
         // a warp that gave up here stops arriving; the vote of the next tile
         // (or the vote below) ends the loop for everyone
         ok = wt;
+        // (every thread, so that the barrier in store_q is met)
+        if (i == 0 && w2 < n_items) store_q((kq + 1) & 1, qn);
       }
       if (!(ok = softmax_sync_and(ok))) {
         if (lane == 0) give_up();
         break;
-      }
-      // the next item's query: S^T of its first tiles runs during this epilogue
-      // (S^T of this item completed: its last scores were read above)
-      DecItem nx;
-      const long long w2 = next_item(p, w + gridDim.x, n_items, nx);
-      float inv_next[HS];
-#pragma unroll
-      for (int hh = 0; hh < HS; ++hh) inv_next[hh] = 1.f;
-      if (w2 < n_items) {
-        write_q(nx, inv_next);
-        load_scales(nx, 0, sk_next, sv_next);
       }
       // ---- the split's output: O^T / l, and its LSE
 #pragma unroll
@@ -1061,10 +1098,10 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       mbar_arrive(o_free + (kq & 1));
       it = nx;
       w = w2;
-#pragma unroll
-      for (int hh = 0; hh < HS; ++hh) inv_sq[hh] = inv_next[hh];
       ++kq;
     }
+    // no copy into shared memory may still be in flight when the CTA exits
+    if constexpr (FP8) cp_async_wait<0>();
   }
 
   tc_fence_before();
