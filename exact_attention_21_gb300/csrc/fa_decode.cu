@@ -422,15 +422,16 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 // P V reads the E4M3 V tile as it arrived too ("Attention 算子优化…", section
 // 六: the cache stays FP8 in HBM, softmax and accumulation in f32): a
 // kind::f8f6f4 MMA of V^T (MN-major) with P^T written as three E4M3 terms in
-// the same way, so the stage is the only copy of the tile on chip.  The
-// per-token scales fold into the per-key work of the softmax threads: s_k
-// multiplies the key's scores, s_v its probabilities before they are split
-// into terms (the row sum keeps the unscaled probabilities).  To keep the
-// terms in E4M3's normal range, s_v is taken relative to 2^E, E the largest
-// binary exponent of the scales seen so far (O^T is rescaled when E grows),
-// the probabilities are bounded by a slack of 2 instead of 8, and the
-// product is scaled by 2^6: the terms stay below 256 and the weights that
-// carry O at or above 2^-6, where three terms hold them to about 2^-12.
+// the same way, so the stage is the only copy of the tile on chip; the terms
+// carry a weight to about 2^-12 relative, as an f16 P would.  The per-token
+// scales fold into the per-key work of the softmax
+// threads: s_k multiplies the key's scores, s_v its probabilities before
+// they are split into terms (the row sum keeps the unscaled probabilities).
+// To keep the terms in E4M3's normal range, s_v is taken relative to 2^E, E
+// the largest binary exponent of the scales seen so far (O^T is rescaled
+// when E grows), the probabilities are bounded by a slack of 2 instead of 8,
+// and the product is scaled by 2^6: the weights stay below 256, and those
+// that carry O sit well above E4M3's smallest normal, 2^-6.
 constexpr int kDecHeads = 16;               // MMA N: query heads per CTA, padded
 constexpr float kDecRescaleSlack = 8.f;
 constexpr float kDecRescaleSlackFp8 = 2.f;
@@ -453,8 +454,11 @@ struct DecTcLayout {
   static constexpr int kHChunkBytes = kDecHeads * 128;  // 16 rows x 128 bytes
   // Q: 16 heads x 128 dims, K-major, bf16; FP8: 48 E4M3 rows (three terms per head) x 128 dims
   static constexpr int kQBytes = (FP8 ? 3 : 2) * kHChunkBytes;
-  // P^T: 16 heads x 128 keys, K-major, 16-bit; FP8: 48 E4M3 rows (three terms per head)
-  static constexpr int kPBytes = (FP8 ? 3 : 2) * kHChunkBytes;
+  // P^T: 16 heads x 128 keys, K-major, 16-bit; FP8: kPTerms E4M3 rows per head
+  // (two terms run about 6 % faster but hold a weight to 2^-8 only, which a
+  // single cached token with a large V row shows at the 1e-2 bar)
+  static constexpr int kPTerms = 3;
+  static constexpr int kPBytes = (FP8 ? kPTerms : 2) * kHChunkBytes;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffP = kOffQ + 2 * kQBytes;      // Q: two buffers (this item's, the next one's)
   static constexpr int kOffRed = kOffP + 2 * kPBytes;    // P^T: two buffers; f32 [4 warps][16 heads]
@@ -478,7 +482,7 @@ struct DecTcLayout {
   // S^T buffers of kSCols columns from 0 (FP8: a column per head and term), O^T after them
   static constexpr int kSCols = FP8 ? 3 * kDecHeads : kDecHeads;
   // O^T: a column per head (FP8: per head and term), two buffers
-  static constexpr int kOCols = kSCols;
+  static constexpr int kOCols = FP8 ? kPTerms * kDecHeads : kDecHeads;
   static constexpr uint32_t kTmemCols = FP8 ? 256 : 128;
   static constexpr uint32_t kColS = 0, kColO = kSBufs * kSCols;
   static_assert(kColO + 2 * kOCols <= kTmemCols, "TMEM budget");
@@ -558,7 +562,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   // bf16 cache: bf16 MMAs; E4M3 cache: E4M3 K x the query's E4M3 terms, and
   // E4M3 V^T (MN-major) x the E4M3 terms of P^T
   constexpr uint32_t id_s = FP8 ? idesc_e4m3_f32(kTile, 3 * H) : idesc_bf16_f32(kTile, H, false, false);
-  constexpr uint32_t id_o = FP8 ? idesc_e4m3_f32(D, 3 * H, true) : idesc_bf16_f32(D, H, true, false);
+  constexpr uint32_t id_o = FP8 ? idesc_e4m3_f32(D, Lay::kPTerms * H, true) : idesc_bf16_f32(D, H, true, false);
 
   // persistent: the CTA runs its items back to back; the barrier rings and
   // the S^T / P^T / V buffers run on a tile count over all of them (gt), so
@@ -747,6 +751,13 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     for (int j = r; j < 2 * Lay::kPBytes / 16; j += 128)
       reinterpret_cast<uint4*>(smem + Lay::kOffP)[j] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
+    // FP8: this thread's row of an O^T buffer, kPTerms columns per head
+    auto ld_o = [&](uint32_t tO, uint32_t* ov) {
+      if constexpr (Lay::kPTerms == 3)
+        tmem_ld_x16_x32_pair(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H, tmem_addr(tO, lane_base, 0), ov);
+      else
+        tmem_ld_x32(tmem_addr(tO, lane_base, 0), ov);
+    };
     // An item's query: thread r holds dims 16 (r % 8) .. +15 of head r / 8
     // (two 16-byte units; 0 past the group), fetched an item ahead.
     auto fetch_q = [&](const DecItem& it, uint4 (&qa)[2]) {
@@ -988,9 +999,9 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
               lt[h + 1] = fmaf(lt[h + 1], alpha[h + 1], p1);
               float2 y = make_float2(p0 * svs, p1 * svs);  // below 256: no saturation
 #pragma unroll
-              for (int t = 0; t < 3; ++t) {
+              for (int t = 0; t < Lay::kPTerms; ++t) {
                 const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
-                if (t < 2) {
+                if (t + 1 < Lay::kPTerms) {
                   const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(c2, __NV_E4M3);
                   y.x -= __half2float(*reinterpret_cast<const __half*>(&hb.x));  // exact in f32
                   y.y -= __half2float(*reinterpret_cast<const __half*>(&hb.y));
@@ -1020,14 +1031,14 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             tc_fence_after();
             uint32_t ov[Lay::kOCols];
             if constexpr (FP8) {
-              tmem_ld_x16_x32_pair(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H, tmem_addr(tO, lane_base, 0), ov);
+              ld_o(tO, ov);
 #pragma unroll
-              for (int t = 0; t < 3; ++t)
+              for (int t = 0; t < Lay::kPTerms; ++t)
 #pragma unroll
                 for (int h = 0; h < HS; ++h)
                   ov[t * H + h] = __float_as_uint(__uint_as_float(ov[t * H + h]) * (alpha[h] * beta));
               tmem_st_x32(tmem_addr(tO, lane_base, 0), ov);
-              tmem_st_x16(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H);
+              if constexpr (Lay::kPTerms == 3) tmem_st_x16(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H);
             } else {
               tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
 #pragma unroll
@@ -1072,13 +1083,17 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       uint32_t ov[Lay::kOCols];
       float osum[HS];
       if constexpr (FP8) {
-        tmem_ld_x16_x32_pair(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H, tmem_addr(tO, lane_base, 0), ov);
+        ld_o(tO, ov);
         // the terms' sum times 2^(E - 126 - 6), in two exact steps
         const int e = E - 126 - kDecPScaleLog2, e1 = e / 2;
         const float f1 = exp2i(e1), f2 = exp2i(e - e1);
 #pragma unroll
-        for (int h = 0; h < HS; ++h)
-          osum[h] = ((__uint_as_float(ov[h]) + __uint_as_float(ov[H + h]) + __uint_as_float(ov[2 * H + h])) * f1) * f2;
+        for (int h = 0; h < HS; ++h) {
+          float s = 0.f;
+#pragma unroll
+          for (int t = 0; t < Lay::kPTerms; ++t) s += __uint_as_float(ov[t * H + h]);
+          osum[h] = (s * f1) * f2;
+        }
       } else {
         tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
 #pragma unroll
