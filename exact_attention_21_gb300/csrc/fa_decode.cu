@@ -548,6 +548,65 @@ __device__ __forceinline__ long long next_item(const DecodeParams& p, long long 
   return n_items;
 }
 
+// The softmax warpgroup writes an item's query (thread r: dims 16 (r % 8) ..
+// +15 of head r / 8, in qa) into a Q buffer q: K-major with the 128-byte
+// swizzle, FP8 as three E4M3 rows per head with 1 / s_q into inv_sq; then it
+// arrives on q_ready and meets the other 127 threads.  Out of line: it runs
+// once per item, and inlined it would sit in the hot loop's code.
+template <bool FP8>
+__device__ __noinline__ void dec_store_q(uint8_t* q, float* inv_sq, uint64_t* q_ready, int r, uint4 qa0, uint4 qa1) {
+  using Lay = DecTcLayout<FP8>;
+  const uint4 qa[2] = {qa0, qa1};
+  const int h = r / 8, sub = r % 8;
+  if constexpr (FP8) {
+    // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h
+    const uint32_t wq[8] = {qa[0].x, qa[0].y, qa[0].z, qa[0].w, qa[1].x, qa[1].y, qa[1].z, qa[1].w};
+    float v[16];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[2 * e] = bf16_lo(wq[e]);
+      v[2 * e + 1] = bf16_hi(wq[e]);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
+    // the 8 threads of a head are 8 consecutive lanes
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sq = amax > 0.f ? 448.f / amax : 1.f;
+    uint32_t term[3][4] = {};
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      float2 y = make_float2(v[e] * sq, v[e + 1] * sq);  // remainder still to represent
+#pragma unroll
+      for (int t = 0; t < 3; ++t) {
+        const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+        const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(c2, __NV_E4M3);
+        y.x -= __half2float(*reinterpret_cast<const __half*>(&hb.x));  // exact in f32
+        y.y -= __half2float(*reinterpret_cast<const __half*>(&hb.y));
+        term[t][e / 4] |= static_cast<uint32_t>(c2) << (16 * ((e / 2) & 1));
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+      const int row = t * kDecHeads + h;
+      *reinterpret_cast<uint4*>(q + row * 128 + ((sub ^ (row & 7)) << 4)) =
+          make_uint4(term[t][0], term[t][1], term[t][2], term[t][3]);
+    }
+    if (sub == 0) inv_sq[h] = 1.f / sq;
+  } else {
+    // units 2 sub, 2 sub + 1 of the 256-byte row: chunk u / 8, unit u % 8
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int u = 2 * sub + j;
+      *reinterpret_cast<uint4*>(q + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = qa[j];
+    }
+  }
+  fence_proxy_async_smem();
+  mbar_arrive(q_ready);
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // FP8: every head's 1 / s_q written
+}
+
 // HS: query heads the softmax threads work on (8 when the GQA group has at
 // most 8, else 16): the MMA's N is 16 either way, and the rows of P^T and
 // columns of O^T past the group are never read.
@@ -772,59 +831,9 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         qa[0] = qa[1] = make_uint4(0u, 0u, 0u, 0u);
       }
     };
-    // ... written into Q buffer qb (K-major, 128-byte swizzle), FP8 with
-    // 1 / s_q of each head, then q_ready.  Buffer qb was last read by S^T of
-    // the item before the previous one.
     auto store_q = [&](int qb, const uint4 (&qa)[2]) {
-      uint8_t* q = sQ + qb * Lay::kQBytes;
-      const int h = r / 8, sub = r % 8;
-      if constexpr (FP8) {
-        // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h
-        const uint32_t wq[8] = {qa[0].x, qa[0].y, qa[0].z, qa[0].w, qa[1].x, qa[1].y, qa[1].z, qa[1].w};
-        float v[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          v[2 * e] = bf16_lo(wq[e]);
-          v[2 * e + 1] = bf16_hi(wq[e]);
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
-        // the 8 threads of a head are 8 consecutive lanes
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float sq = amax > 0.f ? 448.f / amax : 1.f;
-        uint32_t term[3][4] = {};
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float2 y = make_float2(v[e] * sq, v[e + 1] * sq);  // remainder still to represent
-#pragma unroll
-          for (int t = 0; t < 3; ++t) {
-            const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
-            const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(c2, __NV_E4M3);
-            y.x -= __half2float(*reinterpret_cast<const __half*>(&hb.x));  // exact in f32
-            y.y -= __half2float(*reinterpret_cast<const __half*>(&hb.y));
-            term[t][e / 4] |= static_cast<uint32_t>(c2) << (16 * ((e / 2) & 1));
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < 3; ++t) {
-          const int row = t * kDecHeads + h;
-          *reinterpret_cast<uint4*>(q + row * 128 + ((sub ^ (row & 7)) << 4)) =
-              make_uint4(term[t][0], term[t][1], term[t][2], term[t][3]);
-        }
-        if (sub == 0) reinterpret_cast<float*>(smem + Lay::kOffInvSq)[qb * kDecHeads + h] = 1.f / sq;
-      } else {
-        // units 2 sub, 2 sub + 1 of the 256-byte row: chunk u / 8, unit u % 8
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int u = 2 * sub + j;
-          *reinterpret_cast<uint4*>(q + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = qa[j];
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(q_ready);
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // FP8: every head's 1 / s_q written
+      dec_store_q<FP8>(sQ + qb * Lay::kQBytes, reinterpret_cast<float*>(smem + Lay::kOffInvSq) + qb * kDecHeads,
+                       q_ready, r, qa[0], qa[1]);
     };
     // FP8: per-token scales of this thread's key, copied (cp.async) into slot
     // gt % kScaleAhead of a ring kScaleAhead tiles ahead of their use: in a
