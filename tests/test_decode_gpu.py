@@ -51,6 +51,16 @@ def test_decode_batched(cuda_device, d, N):
     check(3, 8, 2, d, [N] * 3, batched=True, seed=N)
 
 
+@pytest.mark.parametrize("heads", [(8, 2), (32, 2)])
+def test_decode_many_items_per_cta(cuda_device, heads):
+    """Many more (split, K/V head, sequence) items than SMs, of mixed and
+    empty lengths: each CTA of the persistent kernel runs a dozen items back
+    to back, carrying its rings, its S^T and O^T buffers and the next item's
+    query across them (GQA groups of 4 and 16)."""
+    lengths = [int(x) for x in np.random.default_rng(31).integers(0, 700, size=160)]
+    check(len(lengths), heads[0], heads[1], 128, lengths, seed=31)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_decode_packed_ragged_with_empty_caches(cuda_device, d):
     lengths = [5, 1, 300, 128, 129, 0, 640, 77, 2000]

@@ -101,6 +101,15 @@ def test_decode_fp8_gqa_groups(cuda_device, heads):
     check(2, heads[0], heads[1], [700, 1500], seed=sum(heads))
 
 
+@pytest.mark.parametrize("heads", [(8, 2), (32, 2)])
+def test_decode_fp8_many_items_per_cta(cuda_device, heads):
+    """A dozen items per CTA of mixed and empty lengths: the per-token scales
+    are copied ahead across items (and loaded directly for the tiles the
+    ring could not reach), and the scale exponent restarts with each item."""
+    lengths = [int(x) for x in np.random.default_rng(32).integers(0, 700, size=160)]
+    check(len(lengths), heads[0], heads[1], lengths, seed=32)
+
+
 def test_decode_fp8_long_cache_many_splits(cuda_device):
     check(1, 4, 1, [20000], batched=True, seed=7)
 
