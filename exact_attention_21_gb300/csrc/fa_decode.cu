@@ -461,24 +461,26 @@ struct DecTcLayout {
   static constexpr int kPBytes = (FP8 ? kPTerms : 2) * kHChunkBytes;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kOffP = kOffQ + 2 * kQBytes;      // Q: two buffers (this item's, the next one's)
-  static constexpr int kOffRed = kOffP + 2 * kPBytes;    // P^T: two buffers; f32 [4 warps][16 heads]
-  static constexpr int kOffInvSq = kOffRed + 4 * kDecHeads * 4;  // FP8: f32 1 / s_q [2 buffers][16 heads]
-  static constexpr int kOffRedE = kOffInvSq + 2 * kDecHeads * 4;  // FP8: int [4 warps], scale exponents
-  // FP8: per-token scales (s_k, s_v) of the 128 keys of the next kScaleAhead tiles
+  // P^T: two buffers; then f32 [2 warpgroups][4 warps][16 heads]
+  static constexpr int kOffRed = kOffP + 2 * kPBytes;
+  static constexpr int kOffInvSq = kOffRed + 2 * 4 * kDecHeads * 4;   // FP8: f32 1 / s_q [2 wg][2 buffers][16 heads]
+  static constexpr int kOffRedE = kOffInvSq + 2 * 2 * kDecHeads * 4;  // FP8: int [2 wg][4 warps], scale exponents
+  // FP8: per-token scales (s_k, s_v) of the 128 keys of the next kScaleAhead tiles, per warpgroup
   static constexpr int kScaleAhead = 4;
-  static constexpr int kOffScale = kOffRedE + 16;
-  static constexpr int kOffBar = kOffScale + (FP8 ? kScaleAhead * kTile * 8 : 0);
+  static constexpr int kOffScale = kOffRedE + 32;
+  static constexpr int kOffBar = kOffScale + (FP8 ? 2 * kScaleAhead * kTile * 8 : 0);
   // S^T buffers in TMEM: S^T runs up to three tiles ahead of the softmax
   static constexpr int kSBufs = 3;
   // full[], empty[], q_ready, s_full[3], p_ready[3], pv_done[2], drain, o_free[2]
   static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;
-  // warp 0 loads, warp 1 issues P V, warps 2-5 run the softmax and warp 6
-  // issues S^T: a single thread issuing both would start one of these narrow
-  // MMAs only every ~100 cycles
+  // warp 0 loads, warp 1 issues P V, warps 2-5 and 7-10 run the softmax
+  // (two warpgroups, half of the heads each) and warp 6 issues S^T: a single
+  // thread issuing both products would start one of these narrow MMAs only
+  // every ~100 cycles
   static constexpr int kWarpS = 6;
-  static constexpr int kThreads = 32 * (kWarpS + 1);
+  static constexpr int kThreads = 32 * 11;
   // S^T buffers of kSCols columns from 0 (FP8: a column per head and term), O^T after them
   static constexpr int kSCols = FP8 ? 3 * kDecHeads : kDecHeads;
   // O^T: a column per head (FP8: per head and term), two buffers
@@ -491,28 +493,29 @@ struct DecTcLayout {
 
 __device__ __forceinline__ void sts_u16(uint8_t* p, uint16_t v) { *reinterpret_cast<uint16_t*>(p) = v; }
 
-// Barrier among the 128 softmax threads (named barrier 1); returns whether
-// `v` held in all of them.
-__device__ __forceinline__ bool softmax_sync_and(bool v) {
+// Barrier among the 128 threads of a softmax warpgroup (named barrier id);
+// returns whether `v` held in all of them.
+__device__ __forceinline__ bool softmax_sync_and(bool v, int id) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
+      : "r"(static_cast<uint32_t>(v)), "r"(id)
       : "memory");
   return r != 0;
 }
 
-// Barrier among the 128 softmax threads; returns whether `v` held in any of them.
-__device__ __forceinline__ bool softmax_sync_or(bool v) {
+// The same; returns whether `v` held in any of them.
+__device__ __forceinline__ bool softmax_sync_or(bool v, int id) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
+      : "r"(static_cast<uint32_t>(v)), "r"(id)
       : "memory");
   return r != 0;
 }
+__device__ __forceinline__ void softmax_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
 // Two E4M3 codes (low byte first) -> two f16 (low half first), exactly.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
@@ -548,16 +551,20 @@ __device__ __forceinline__ long long next_item(const DecodeParams& p, long long 
   return n_items;
 }
 
-// The softmax warpgroup writes an item's query (thread r: dims 16 (r % 8) ..
-// +15 of head r / 8, in qa) into a Q buffer q: K-major with the 128-byte
-// swizzle, FP8 as three E4M3 rows per head with 1 / s_q into inv_sq; then it
-// arrives on q_ready and meets the other 127 threads.  Out of line: it runs
-// once per item, and inlined it would sit in the hot loop's code.
+// A softmax warpgroup's part in an item's query (thread r: dims 16 (r % 8) ..
+// +15 of head r / 8, in qa).  The first warpgroup (write) writes it into a Q
+// buffer q, K-major with the 128-byte swizzle (FP8: three E4M3 rows per
+// head) and arrives on q_ready; with an FP8 cache each warpgroup puts
+// 1 / s_q of the 16 heads into its own inv_sq and meets its other 127
+// threads (barrier bar_id).  Out of line: it runs once per item, and inlined
+// it would sit in the hot loop's code.
 template <bool FP8>
-__device__ __noinline__ void dec_store_q(uint8_t* q, float* inv_sq, uint64_t* q_ready, int r, uint4 qa0, uint4 qa1) {
+__device__ __noinline__ void dec_store_q(uint8_t* q, float* inv_sq, uint64_t* q_ready, int r, uint4 qa0, uint4 qa1,
+                                         bool write, int bar_id) {
   using Lay = DecTcLayout<FP8>;
   const uint4 qa[2] = {qa0, qa1};
   const int h = r / 8, sub = r % 8;
+  if (!FP8 && !write) return;
   if constexpr (FP8) {
     // 48 E4M3 rows: the terms of head h in rows h, 16 + h, 32 + h
     const uint32_t wq[8] = {qa[0].x, qa[0].y, qa[0].z, qa[0].w, qa[1].x, qa[1].y, qa[1].z, qa[1].w};
@@ -587,11 +594,13 @@ __device__ __noinline__ void dec_store_q(uint8_t* q, float* inv_sq, uint64_t* q_
         term[t][e / 4] |= static_cast<uint32_t>(c2) << (16 * ((e / 2) & 1));
       }
     }
+    if (write) {
 #pragma unroll
-    for (int t = 0; t < 3; ++t) {
-      const int row = t * kDecHeads + h;
-      *reinterpret_cast<uint4*>(q + row * 128 + ((sub ^ (row & 7)) << 4)) =
-          make_uint4(term[t][0], term[t][1], term[t][2], term[t][3]);
+      for (int t = 0; t < 3; ++t) {
+        const int row = t * kDecHeads + h;
+        *reinterpret_cast<uint4*>(q + row * 128 + ((sub ^ (row & 7)) << 4)) =
+            make_uint4(term[t][0], term[t][1], term[t][2], term[t][3]);
+      }
     }
     if (sub == 0) inv_sq[h] = 1.f / sq;
   } else {
@@ -602,9 +611,11 @@ __device__ __noinline__ void dec_store_q(uint8_t* q, float* inv_sq, uint64_t* q_
       *reinterpret_cast<uint4*>(q + (u / 8) * Lay::kHChunkBytes + h * 128 + (((u % 8) ^ (h & 7)) << 4)) = qa[j];
     }
   }
-  fence_proxy_async_smem();
-  mbar_arrive(q_ready);
-  asm volatile("bar.sync 1, 128;" ::: "memory");  // FP8: every head's 1 / s_q written
+  if (write) {
+    fence_proxy_async_smem();
+    mbar_arrive(q_ready);
+  }
+  if constexpr (FP8) softmax_sync(bar_id);  // every head's 1 / s_q written
 }
 
 // HS: query heads the softmax threads work on (8 when the GQA group has at
@@ -658,11 +669,11 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     mbar_init(q_ready, 128);
     for (int i = 0; i < Lay::kSBufs; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_ready + i, 128);
+      mbar_init(p_ready + i, 256);  // both softmax warpgroups
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(pv_done + i, 1);
-      mbar_init(o_free + i, 128);
+      mbar_init(o_free + i, 256);
     }
     mbar_init(drain, 2);  // both MMA-issuing threads commit
     *abort_flag = 0;
@@ -796,32 +807,50 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       int never = 0;
       mbar_wait(drain, 0, &never);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ softmax warpgroup
+  } else if (warp < 6 || warp > Lay::kWarpS) {
+    // ------------------------------------------------------------ softmax warpgroups
+    // Warps 2-5 and 7-10: two warpgroups over the same keys, each taking half
+    // of the heads (HW of them from h0), so that two warps per scheduler
+    // share the per-key work.  Each has its own named barrier (1 + wg).
+    constexpr int HW = HS / 2;
+    const int wg = warp > Lay::kWarpS ? 1 : 0;
+    const int h0 = wg * HW;
+    const int bar_id = 1 + wg;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // key row of S^T, dimension row of O^T
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32);
     const int group = p.group;
     const float c = p.scale_log2;
     constexpr float kSlack = FP8 ? kDecRescaleSlackFp8 : kDecRescaleSlack;
-    int* sRedE = reinterpret_cast<int*>(smem + Lay::kOffRedE);
+    float* sRedW = sRed + wg * 4 * kDecHeads;
+    int* sRedE = reinterpret_cast<int*>(smem + Lay::kOffRedE) + wg * 4;
+    float* sInvSq = reinterpret_cast<float*>(smem + Lay::kOffInvSq) + wg * 2 * kDecHeads;
     // P^T rows of the padded heads are read by the MMA but never used: zero
-    // them once (all of both buffers)
-    for (int j = r; j < 2 * Lay::kPBytes / 16; j += 128)
-      reinterpret_cast<uint4*>(smem + Lay::kOffP)[j] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
-    // FP8: this thread's row of an O^T buffer, kPTerms columns per head
+    // them once (all of both buffers), before the first P^T is released
+    if (wg == 0) {
+      for (int j = r; j < 2 * Lay::kPBytes / 16; j += 128)
+        reinterpret_cast<uint4*>(smem + Lay::kOffP)[j] = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();
+    }
+    // this warpgroup's columns of an O^T buffer: kPTerms groups of HW (FP8)
     auto ld_o = [&](uint32_t tO, uint32_t* ov) {
-      if constexpr (Lay::kPTerms == 3)
-        tmem_ld_x16_x32_pair(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H, tmem_addr(tO, lane_base, 0), ov);
-      else
-        tmem_ld_x32(tmem_addr(tO, lane_base, 0), ov);
+      if constexpr (FP8) {
+        static_assert(Lay::kPTerms == 3, "three column groups");
+        tmem_ld_cols3<HW>(tmem_addr(tO, lane_base, h0), tmem_addr(tO, lane_base, H + h0),
+                          tmem_addr(tO, lane_base, 2 * H + h0), ov);
+      } else {
+        tmem_ld_cols<HW>(tmem_addr(tO, lane_base, h0), ov);
+      }
+    };
+    auto st_o = [&](uint32_t tO, const uint32_t* ov) {
+#pragma unroll
+      for (int t = 0; t < (FP8 ? Lay::kPTerms : 1); ++t) tmem_st_cols<HW>(tmem_addr(tO, lane_base, t * H + h0), ov + t * HW);
     };
     // An item's query: thread r holds dims 16 (r % 8) .. +15 of head r / 8
     // (two 16-byte units; 0 past the group), fetched an item ahead.
     auto fetch_q = [&](const DecItem& it, uint4 (&qa)[2]) {
       const int h = r / 8;
-      if (h < group) {
+      if (h < group && (FP8 || wg == 0)) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
                                                           (static_cast<long long>(it.b) * p.Hq + it.g * group + h) * D +
                                                           16 * (r % 8));
@@ -832,15 +861,15 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
     };
     auto store_q = [&](int qb, const uint4 (&qa)[2]) {
-      dec_store_q<FP8>(sQ + qb * Lay::kQBytes, reinterpret_cast<float*>(smem + Lay::kOffInvSq) + qb * kDecHeads,
-                       q_ready, r, qa[0], qa[1]);
+      dec_store_q<FP8>(sQ + qb * Lay::kQBytes, sInvSq + qb * kDecHeads, q_ready, r, qa[0], qa[1], wg == 0, bar_id);
     };
     // FP8: per-token scales of this thread's key, copied (cp.async) into slot
-    // gt % kScaleAhead of a ring kScaleAhead tiles ahead of their use: in a
-    // saturated memory system a load takes several tiles' time.  One copy
-    // group per tile, empty or not; bit j of pf: slot j holds copies.
+    // gt % kScaleAhead of this warpgroup's ring, kScaleAhead tiles ahead of
+    // their use: in a saturated memory system a load takes several tiles'
+    // time.  One copy group per tile, empty or not; bit j of pf: slot j holds
+    // copies.
     constexpr int kAhead = Lay::kScaleAhead;
-    float2* sScale = reinterpret_cast<float2*>(smem + Lay::kOffScale);
+    float2* sScale = reinterpret_cast<float2*>(smem + Lay::kOffScale) + wg * kAhead * kTile;
     uint32_t pf = 0;
     auto issue_scales = [&](const DecItem& t, int i, uint32_t slot) {
       pf &= ~(1u << slot);
@@ -855,7 +884,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     };
     // A wait that gives up must not leave the other threads at a barrier:
     // results of waits are made warp-uniform (the shuffles and TMEM accesses
-    // need whole warps) and the loops end only on a vote of all 128 threads.
+    // need whole warps) and the loops end only on a vote of all 128 threads
+    // of the warpgroup.
     bool ok = true;
     uint32_t gt = 0, kq = 0;  // tiles and items so far
     DecItem it;
@@ -870,10 +900,9 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       }
     }
     while (w < n_items && ok) {
-      float inv_sq[HS];  // FP8: 1 / s_q of each head
+      float inv_sq[HW];  // FP8: 1 / s_q of this warpgroup's heads
 #pragma unroll
-      for (int hh = 0; hh < HS; ++hh)
-        inv_sq[hh] = FP8 ? reinterpret_cast<const float*>(smem + Lay::kOffInvSq)[(kq & 1) * kDecHeads + hh] : 1.f;
+      for (int hh = 0; hh < HW; ++hh) inv_sq[hh] = FP8 ? sInvSq[(kq & 1) * kDecHeads + h0 + hh] : 1.f;
       // the next item's query: fetched now, stored once this item's first tile
       // is done, so that S^T can run into the next item ahead of the softmax
       DecItem nx;
@@ -882,9 +911,9 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (w2 < n_items) fetch_q(nx, qn);
       const uint32_t tO = tmem + Lay::kColO + (kq & 1) * Lay::kOCols;
       int E = 0;  // FP8: largest biased exponent of the item's V scales so far
-      float m[HS], lt[HS];
+      float m[HW], lt[HW];
 #pragma unroll
-      for (int h = 0; h < HS; ++h) {
+      for (int h = 0; h < HW; ++h) {
         m[h] = -INFINITY;
         lt[h] = 0.f;
       }
@@ -921,27 +950,29 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const int ei = (FP8 && valid) ? static_cast<int>((svb >> 23) & 0xffu) : 0;  // masked keys: none
         const uint32_t sb = gt % Lay::kSBufs;
         bool wt = __all_sync(0xffffffffu, mbar_wait(s_full + sb, (gt / Lay::kSBufs) & 1, abort_flag));
-        float x[HS];
+        float x[HW];
         bool over = false;  // a score above its head's reference by more than the slack
         if (wt) {
           tc_fence_after();
-          uint32_t svv[Lay::kSCols];
-          float sc[HS];
+          float sc[HW];
+          const uint32_t ts = tmem + Lay::kColS + sb * Lay::kSCols;
           if constexpr (FP8) {
-            const uint32_t ts = tmem + Lay::kColS + sb * Lay::kSCols;
-            tmem_ld_x16_x32_pair(tmem_addr(ts, lane_base, 2 * H), svv + 2 * H, tmem_addr(ts, lane_base, 0), svv);
+            uint32_t svv[3 * HW];
+            tmem_ld_cols3<HW>(tmem_addr(ts, lane_base, h0), tmem_addr(ts, lane_base, H + h0),
+                              tmem_addr(ts, lane_base, 2 * H + h0), svv);
 #pragma unroll
-            for (int h = 0; h < HS; ++h)
-              sc[h] = (__uint_as_float(svv[h]) + __uint_as_float(svv[H + h]) + __uint_as_float(svv[2 * H + h])) *
+            for (int h = 0; h < HW; ++h)
+              sc[h] = (__uint_as_float(svv[h]) + __uint_as_float(svv[HW + h]) + __uint_as_float(svv[2 * HW + h])) *
                       inv_sq[h];
           } else {
-            tmem_ld_x16(tmem_addr(tmem + Lay::kColS + sb * Lay::kSCols, lane_base, 0), svv);
+            uint32_t svv[HW];
+            tmem_ld_cols<HW>(tmem_addr(ts, lane_base, h0), svv);
 #pragma unroll
-            for (int h = 0; h < HS; ++h) sc[h] = __uint_as_float(svv[h]);
+            for (int h = 0; h < HW; ++h) sc[h] = __uint_as_float(svv[h]);
           }
           const float ck = c * sk;
 #pragma unroll
-          for (int h = 0; h < HS; ++h) {
+          for (int h = 0; h < HW; ++h) {
             x[h] = valid ? sc[h] * ck : -INFINITY;
             over |= x[h] > m[h] + kSlack;  // always for a valid key on the first tile (m = -inf)
           }
@@ -949,30 +980,30 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         bool bump = false;
         float beta = 1.f;  // FP8: O^T's factor for a larger E
-        float alpha[HS];
+        float alpha[HW];
 #pragma unroll
-        for (int h = 0; h < HS; ++h) alpha[h] = 1.f;
+        for (int h = 0; h < HW; ++h) alpha[h] = 1.f;
         // One vote per tile: in the common case no reference moves and the
         // probabilities are taken against the current m.  Otherwise (the first
         // tile, a score jump, or a wait that gave up) the tile max of every
         // head is reduced over the 128 keys.
-        if (softmax_sync_or(over || !wt)) {
-          if (!(ok = softmax_sync_and(wt))) break;
+        if (softmax_sync_or(over || !wt, bar_id)) {
+          if (!(ok = softmax_sync_and(wt, bar_id))) break;
 #pragma unroll
-          for (int h = 0; h < HS; ++h) {
+          for (int h = 0; h < HW; ++h) {
             float mx = x[h];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            if (lane == 0) sRed[quad * H + h] = mx;
+            if (lane == 0) sRedW[quad * H + h] = mx;
           }
           if constexpr (FP8) {
             const int em = __reduce_max_sync(0xffffffffu, ei);
             if (lane == 0) sRedE[quad] = em;
           }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          softmax_sync(bar_id);
 #pragma unroll
-          for (int h = 0; h < HS; ++h) {
-            const float tm = fmaxf(fmaxf(sRed[h], sRed[H + h]), fmaxf(sRed[2 * H + h], sRed[3 * H + h]));
+          for (int h = 0; h < HW; ++h) {
+            const float tm = fmaxf(fmaxf(sRedW[h], sRedW[H + h]), fmaxf(sRedW[2 * H + h], sRedW[3 * H + h]));
             // the tile's key 0 is valid, so tm is finite
             const bool up = tm > m[h] + kSlack;
             const float mn = up ? tm : m[h];
@@ -988,7 +1019,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
               E = te;
             }
           }
-          asm volatile("bar.sync 1, 128;" ::: "memory");  // sRed is rewritten by the next reduction
+          softmax_sync(bar_id);  // sRedW is rewritten by the next reduction
         }
         // P^T buffer gt & 1 was last read by P V of tile gt - 2
         wt = gt < 2 || __all_sync(0xffffffffu, mbar_wait(pv_done + (gt & 1), ((gt - 2) >> 1) & 1, abort_flag));
@@ -1002,7 +1033,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             // P^T row t * 16 + h, key r: 16-byte unit r / 16 of the row, swizzled
             uint8_t* pb = pbuf(gt) + (r & 15);
 #pragma unroll
-            for (int h = 0; h < HS; h += 2) {
+            for (int h = 0; h < HW; h += 2) {
               const float p0 = ex2_approx(x[h] - m[h]), p1 = ex2_approx(x[h + 1] - m[h + 1]);  // masked keys: 0
               lt[h] = fmaf(lt[h], alpha[h], p0);
               lt[h + 1] = fmaf(lt[h + 1], alpha[h + 1], p1);
@@ -1015,7 +1046,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                   y.x -= __half2float(*reinterpret_cast<const __half*>(&hb.x));  // exact in f32
                   y.y -= __half2float(*reinterpret_cast<const __half*>(&hb.y));
                 }
-                const int row0 = t * kDecHeads + h;
+                const int row0 = t * kDecHeads + h0 + h;
                 pb[row0 * 128 + ((((r >> 4) ^ (row0 & 7))) << 4)] = static_cast<uint8_t>(c2 & 0xffu);
                 pb[(row0 + 1) * 128 + ((((r >> 4) ^ ((row0 + 1) & 7))) << 4)] = static_cast<uint8_t>(c2 >> 8);
               }
@@ -1024,36 +1055,30 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             uint8_t* pb = pbuf(gt) + (r / 64) * Lay::kHChunkBytes + (r % 8) * 2;
             const int pu = (r % 64) / 8;
 #pragma unroll
-            for (int h = 0; h < HS; ++h) {
+            for (int h = 0; h < HW; ++h) {
               const float pv = ex2_approx(x[h] - m[h]);  // masked keys: 0
               lt[h] = fmaf(lt[h], alpha[h], pv);
               const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
-              sts_u16(pb + h * 128 + ((pu ^ (h & 7)) << 4), *reinterpret_cast<const uint16_t*>(&pb16));
+              const int hr = h0 + h;
+              sts_u16(pb + hr * 128 + ((pu ^ (hr & 7)) << 4), *reinterpret_cast<const uint16_t*>(&pb16));
             }
           }
         }
-        // m is the same in every thread, so bump is uniform
+        // m is the same in every thread of the warpgroup, so bump is uniform
         if (wt && i > 0 && bump) {
           // O^T may only be touched once P V of tile gt - 1 has completed
           wt = __all_sync(0xffffffffu, mbar_wait(pv_done + ((gt - 1) & 1), ((gt - 1) >> 1) & 1, abort_flag));
           if (wt) {
             tc_fence_after();
-            uint32_t ov[Lay::kOCols];
-            if constexpr (FP8) {
-              ld_o(tO, ov);
+            constexpr int NT = FP8 ? Lay::kPTerms : 1;
+            uint32_t ov[NT * HW];
+            ld_o(tO, ov);
 #pragma unroll
-              for (int t = 0; t < Lay::kPTerms; ++t)
+            for (int t = 0; t < NT; ++t)
 #pragma unroll
-                for (int h = 0; h < HS; ++h)
-                  ov[t * H + h] = __float_as_uint(__uint_as_float(ov[t * H + h]) * (alpha[h] * beta));
-              tmem_st_x32(tmem_addr(tO, lane_base, 0), ov);
-              if constexpr (Lay::kPTerms == 3) tmem_st_x16(tmem_addr(tO, lane_base, 2 * H), ov + 2 * H);
-            } else {
-              tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
-#pragma unroll
-              for (int h = 0; h < HS; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-              tmem_st_x16(tmem_addr(tO, lane_base, 0), ov);
-            }
+              for (int h = 0; h < HW; ++h)
+                ov[t * HW + h] = __float_as_uint(__uint_as_float(ov[t * HW + h]) * (alpha[h] * beta));
+            st_o(tO, ov);
             tmem_st_wait();
           }
         }
@@ -1063,58 +1088,54 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           mbar_arrive(p_ready + sb);
         }
         // a warp that gave up here stops arriving; the vote of the next tile
-        // (or the vote below) ends the loop for everyone
+        // (or the vote below) ends the loop for the warpgroup
         ok = wt;
         // (every thread, so that the barrier in store_q is met)
         if (i == 0 && w2 < n_items) store_q((kq + 1) & 1, qn);
       }
-      if (!(ok = softmax_sync_and(ok))) {
+      if (!(ok = softmax_sync_and(ok, bar_id))) {
         if (lane == 0) give_up();
         break;
       }
-      // ---- the split's output: O^T / l, and its LSE
+      // ---- the split's output for this warpgroup's heads: O^T / l, and the LSE
 #pragma unroll
-      for (int h = 0; h < HS; ++h) {
+      for (int h = 0; h < HW; ++h) {
         float xs = lt[h];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, off);
-        if (lane == 0) sRed[quad * H + h] = xs;
+        if (lane == 0) sRedW[quad * H + h] = xs;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      softmax_sync(bar_id);
       // all four warps take the same way out: the next item has barriers
       ok = softmax_sync_and(
-          __all_sync(0xffffffffu, mbar_wait(pv_done + ((gt - 1) & 1), ((gt - 1) >> 1) & 1, abort_flag)));
+          __all_sync(0xffffffffu, mbar_wait(pv_done + ((gt - 1) & 1), ((gt - 1) >> 1) & 1, abort_flag)), bar_id);
       if (!ok) {
         if (lane == 0) give_up();
         break;
       }
       tc_fence_after();
-      uint32_t ov[Lay::kOCols];
-      float osum[HS];
-      if constexpr (FP8) {
-        ld_o(tO, ov);
-        // the terms' sum times 2^(E - 126 - 6), in two exact steps
-        const int e = E - 126 - kDecPScaleLog2, e1 = e / 2;
-        const float f1 = exp2i(e1), f2 = exp2i(e - e1);
+      constexpr int NT = FP8 ? Lay::kPTerms : 1;
+      uint32_t ov[NT * HW];
+      ld_o(tO, ov);
+      float osum[HW];
+      // FP8: the terms' sum times 2^(E - 126 - 6), in two exact steps
+      const int e = E - 126 - kDecPScaleLog2, e1 = e / 2;
+      const float f1 = FP8 ? exp2i(e1) : 1.f, f2 = FP8 ? exp2i(e - e1) : 1.f;
 #pragma unroll
-        for (int h = 0; h < HS; ++h) {
-          float s = 0.f;
+      for (int h = 0; h < HW; ++h) {
+        float s = 0.f;
 #pragma unroll
-          for (int t = 0; t < Lay::kPTerms; ++t) s += __uint_as_float(ov[t * H + h]);
-          osum[h] = (s * f1) * f2;
-        }
-      } else {
-        tmem_ld_x16(tmem_addr(tO, lane_base, 0), ov);
-#pragma unroll
-        for (int h = 0; h < HS; ++h) osum[h] = __uint_as_float(ov[h]);
+        for (int t = 0; t < NT; ++t) s += __uint_as_float(ov[t * HW + h]);
+        osum[h] = (s * f1) * f2;
       }
       const long long row0 = static_cast<long long>(it.b) * p.Hq + static_cast<long long>(it.g) * group;
 #pragma unroll
-      for (int h = 0; h < HS; ++h) {
-        if (h < group) {
-          const float l = sRed[h] + sRed[H + h] + sRed[2 * H + h] + sRed[3 * H + h];
-          p.o_part[((row0 + h) * p.n_splits + it.split) * D + r] = osum[h] / l;
-          if (r == 0) p.lse_part[(row0 + h) * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
+      for (int h = 0; h < HW; ++h) {
+        const int hh = h0 + h;
+        if (hh < group) {
+          const float l = sRedW[h] + sRedW[H + h] + sRedW[2 * H + h] + sRedW[3 * H + h];
+          p.o_part[((row0 + hh) * p.n_splits + it.split) * D + r] = osum[h] / l;
+          if (r == 0) p.lse_part[(row0 + hh) * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
         }
       }
       // O^T buffer kq & 1 read: P V of item kq + 2 may write it
