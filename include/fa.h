@@ -182,10 +182,13 @@ int fa_kv_quantize_fp8(const void* x, void* x8, float* scale, long long rows, in
 
 /*
  * One decoding step (as fa_decode) over an E4M3 K/V cache produced by
- * fa_kv_quantize_fp8: the cache stays compressed in HBM and is dequantised in
- * shared memory; the products run in f16 with f32 accumulation, the softmax
- * in f32 ("Attention 算子优化…", section 六).  The result is the attention of
- * q over the dequantised cache k8 * k_scale, v8 * v_scale.
+ * fa_kv_quantize_fp8: the cache stays compressed in HBM ("Attention 算子优化…",
+ * section 六) and the tensor cores read its K and V tiles as they arrive, in
+ * E4M3 x E4M3 products against the query and the probabilities, each written
+ * as three E4M3 terms (about 2^-12 relative, as accurate as a 16-bit
+ * operand); the per-token scales, the softmax and the accumulation are f32.
+ * The result is the attention of q over the dequantised cache k8 * k_scale,
+ * v8 * v_scale.
  *
  *   k8, v8    [T, Hkv, d] E4M3 codes, 16-byte aligned                 (in)
  *   k_scale, v_scale  [T, Hkv] f32 per-token scales, 4-byte aligned   (in)
