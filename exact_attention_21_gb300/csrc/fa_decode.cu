@@ -400,18 +400,21 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 // GQA group (padded to 16) as the MMA's N dimension:
 //     S^T = K_tile Q^T       M = 128 keys,  N = 16 heads, K = d   (TMEM, f32)
 //     O^T += V_tile^T P^T    M = d = 128,   N = 16 heads, K = 128 keys
-// so the threads only turn 16 scores per key into probabilities.  Roles:
-//   warp 0     TMA producer of the K / V stages.
-//   warp 1     TMEM allocator and P V issuer (one thread).
-//   warps 2-5  softmax warpgroup: thread = key row of S^T (TMEM lane) for the
-//              probabilities, and = dimension row of O^T for the rescale and
-//              the split's output.
-//   warp 6     S^T issuer (one thread).
-// S^T is double-buffered in TMEM, so S^T of tile i+1 runs while the softmax
-// works on tile i; P^T (K-major: 16 head rows x 128 keys) is double-buffered
-// in shared memory.  The running max of a head only moves when a tile's max
-// exceeds it by more than a slack (log2 units); any common reference gives
-// the same merge, so this is exact and O^T is rarely rescaled.
+// so the threads only turn 16 scores per key into probabilities.  The kernel
+// is persistent (one CTA per SM over its (split, K/V head, sequence) items).
+// Roles:
+//   warp 0      TMA producer of the K / V stages.
+//   warp 1      TMEM allocator and P V issuer (one thread).
+//   warps 2-5,  two softmax warpgroups, half of the heads each: thread = key
+//   warps 7-10  row of S^T (TMEM lane) for the probabilities, and = dimension
+//               row of O^T for the rescale and the split's output.
+//   warp 6      S^T issuer (one thread).
+// S^T has three TMEM buffers, so S^T runs up to three tiles ahead of the
+// softmax (into the next item too); O^T has two, one per item in flight;
+// P^T (K-major: 16 head rows x 128 keys) is double-buffered in shared
+// memory.  The running max of a head only moves when a tile's max exceeds it
+// by more than a slack (log2 units); any common reference gives the same
+// merge, so this is exact and O^T is rarely rescaled.
 //
 // With the FP8 cache S^T reads the E4M3 K tile as it arrived, in a
 // kind::f8f6f4 MMA: each head's query is scaled by s_q = 448 / max|q| and
