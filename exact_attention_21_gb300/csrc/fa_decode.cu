@@ -526,17 +526,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
-// One work item of the persistent kernel: split w % n_splits of K/V head
-// (w / n_splits) % Hkv of sequence w / (n_splits Hkv).  False for a split past
-// the end of its sequence's cache (the combine skips it) and for a sequence
-// with bad offsets or length (a status bit).
+// One work item of the persistent kernel: split w / (B Hkv) of K/V head
+// w % Hkv of sequence (w / Hkv) % B.  Split-major, so that the items a CTA
+// takes (blockIdx.x + j gridDim.x) spread over all split positions: with
+// caches of unequal length only the first splits of the short ones exist.
+// False for a split past the end of its sequence's cache (the combine skips
+// it) and for a sequence with bad offsets or length (a status bit).
 struct DecItem {
   long long seq0;
   int split, g, b, L, t0, nt;
 };
 __device__ __forceinline__ bool decode_item(const DecodeParams& p, long long w, DecItem& it) {
-  it.split = static_cast<int>(w % p.n_splits);
-  const long long rest = w / p.n_splits;
+  const long long heads = static_cast<long long>(p.B) * p.Hkv;
+  it.split = static_cast<int>(w / heads);
+  const long long rest = w % heads;
   it.g = static_cast<int>(rest % p.Hkv);
   it.b = static_cast<int>(rest / p.Hkv);
   if (!decode_bounds(p, it.b, it.seq0, it.L)) return false;
