@@ -831,11 +831,12 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     float* sRedW = sRed + wg * 4 * kDecHeads;
     int* sRedE = reinterpret_cast<int*>(smem + Lay::kOffRedE) + wg * 4;
     float* sInvSq = reinterpret_cast<float*>(smem + Lay::kOffInvSq) + wg * 2 * kDecHeads;
-    // P^T rows of the padded heads are read by the MMA but never used: zero
-    // them once (all of both buffers), before the first P^T is released
-    if (wg == 0) {
+    // P^T rows of the padded heads (row % 16 >= HS, in both buffers and every
+    // 16-row group) are read by the MMA but never written or used: zero them
+    // once, before the first P^T is released
+    if (wg == 0 && HS < kDecHeads) {
       for (int j = r; j < 2 * Lay::kPBytes / 16; j += 128)
-        reinterpret_cast<uint4*>(smem + Lay::kOffP)[j] = make_uint4(0u, 0u, 0u, 0u);
+        if ((j / 8) % kDecHeads >= HS) reinterpret_cast<uint4*>(smem + Lay::kOffP)[j] = make_uint4(0u, 0u, 0u, 0u);
       fence_proxy_async_smem();
     }
     // this warpgroup's columns of an O^T buffer: kPTerms groups of HW (FP8)
