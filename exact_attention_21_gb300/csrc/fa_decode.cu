@@ -426,7 +426,8 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 // 六: the cache stays FP8 in HBM, softmax and accumulation in f32): a
 // kind::f8f6f4 MMA of V^T (MN-major) with P^T written as three E4M3 terms in
 // the same way, so the stage is the only copy of the tile on chip; the terms
-// carry a weight to about 2^-12 relative, as an f16 P would.  The per-token
+// hold a weight w to 2^-12 relative for w >= 4 and to 2^-10 absolute below
+// (half E4M3's subnormal step), finer than a bf16 P.  The per-token
 // scales fold into the per-key work of the softmax
 // threads: s_k multiplies the key's scores, s_v its probabilities before
 // they are split into terms (the row sum keeps the unscaled probabilities).

@@ -185,8 +185,8 @@ int fa_kv_quantize_fp8(const void* x, void* x8, float* scale, long long rows, in
  * fa_kv_quantize_fp8: the cache stays compressed in HBM ("Attention 算子优化…",
  * section 六) and the tensor cores read its K and V tiles as they arrive, in
  * E4M3 x E4M3 products against the query and the probabilities, each written
- * as three E4M3 terms (about 2^-12 relative, as accurate as a 16-bit
- * operand); the per-token scales, the softmax and the accumulation are f32.
+ * as three E4M3 terms (2^-12 relative for the larger elements, finer than
+ * bf16); the per-token scales, the softmax and the accumulation are f32.
  * The result is the attention of q over the dequantised cache k8 * k_scale,
  * v8 * v_scale.
  *
