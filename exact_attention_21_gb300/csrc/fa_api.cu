@@ -243,7 +243,7 @@ const char* fa_last_error_string(void) { return g_err; }
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
            long long T, float scale, int causal, const int* cu_seqlens, void* stream) {
   g_err[0] = '\0';
-  Shape s;
+  Shape s{};
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, &s);
   if (rc) return rc;
   if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
@@ -286,7 +286,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
                       long long T, float scale, int causal, const int* cu_seqlens, void* workspace,
                       size_t workspace_bytes, bool deterministic, void* stream) {
-  Shape s;
+  Shape s{};
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, &s);
   if (rc) return rc;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
@@ -365,7 +365,7 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
     if (!pg.seqlens || !aligned(pg.block_table, 4) || !aligned(pg.seqlens, 4))
       return fail(FA_ERR_INVALID_ARG, "block_table and seqlens must be non-null and 4-byte aligned");
   }
-  Shape s;
+  Shape s{};
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, 0, paged ? pg.seqlens : cu_seqlens_k, &s);
   if (rc) return rc;
   if (Hq / Hkv > 16) return fail(FA_ERR_UNSUPPORTED, "decode supports up to 16 query heads per K/V head");
