@@ -104,8 +104,9 @@ EncodeTiledFn encode_fn() {
 // word; done once per device.
 int device_state(DeviceState** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return fail(FA_ERR_LAUNCH, "cudaGetDevice failed");
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return fail(FA_ERR_LAUNCH, "cudaGetDevice failed");
+  if (dev >= kMaxDevices)
+    return fail(FA_ERR_INVALID_ARG, "device index %d exceeds the library limit of %d", dev, kMaxDevices);
   std::lock_guard<std::mutex> lock(g_dev_mu);
   DeviceState& st = g_dev[dev];
   if (st.checked == 0) {
@@ -240,9 +241,12 @@ extern "C" {
 
 const char* fa_last_error_string(void) { return g_err; }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
-           long long T, float scale, int causal, const int* cu_seqlens, void* stream) {
-  g_err[0] = '\0';
+}  // extern "C"
+
+// Shared by fa_fwd and fa_fwd_counted (tile_count == nullptr: no counting).
+static int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                      int N, int d, long long T, float scale, int causal, const int* cu_seqlens,
+                      long long* tile_count, void* stream) {
   Shape s{};
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, &s);
   if (rc) return rc;
@@ -270,9 +274,31 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.causal = causal;
   p.n_qtiles = s.n_tiles;
   p.scale_log2 = scale * 1.4426950408889634f;
+  if (tile_count != nullptr) {
+    if (!aligned(tile_count, 8)) return fail(FA_ERR_INVALID_ARG, "tile_counts must be 8-byte aligned");
+    const cudaError_t z = cudaMemsetAsync(tile_count, 0, sizeof(long long) * B, static_cast<cudaStream_t>(stream));
+    if (z != cudaSuccess) return fail(FA_ERR_LAUNCH, "zeroing tile_counts failed: %s", cudaGetErrorString(z));
+    p.tile_count = reinterpret_cast<unsigned long long*>(tile_count);
+  }
   int e = fa::launch_fwd(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;
+}
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+           long long T, float scale, int causal, const int* cu_seqlens, void* stream) {
+  g_err[0] = '\0';
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, nullptr, stream);
+}
+
+int fa_fwd_counted(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                   int d, long long T, float scale, int causal, const int* cu_seqlens, long long* tile_counts,
+                   void* stream) {
+  g_err[0] = '\0';
+  if (!tile_counts) return fail(FA_ERR_INVALID_ARG, "null tile_counts");
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, tile_counts, stream);
 }
 
 size_t fa_bwd_workspace_size(int Hq, long long T, int d) {
@@ -285,7 +311,7 @@ size_t fa_bwd_workspace_size(int Hq, long long T, int d) {
 static int bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dout,
                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
                       long long T, float scale, int causal, const int* cu_seqlens, void* workspace,
-                      size_t workspace_bytes, bool deterministic, void* stream) {
+                      size_t workspace_bytes, bool deterministic, long long* tile_count, void* stream) {
   Shape s{};
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, &s);
   if (rc) return rc;
@@ -328,6 +354,12 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   p.n_kvtiles = s.n_tiles;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  if (tile_count != nullptr) {
+    if (!aligned(tile_count, 8)) return fail(FA_ERR_INVALID_ARG, "tile_counts must be 8-byte aligned");
+    const cudaError_t z = cudaMemsetAsync(tile_count, 0, sizeof(long long) * B, static_cast<cudaStream_t>(stream));
+    if (z != cudaSuccess) return fail(FA_ERR_LAUNCH, "zeroing tile_counts failed: %s", cudaGetErrorString(z));
+    p.tile_count = reinterpret_cast<unsigned long long*>(tile_count);
+  }
   int e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, deterministic, static_cast<cudaStream_t>(stream));
   if (e == -1) return fail(FA_ERR_UNSUPPORTED, "backward kernel unavailable for d = %d", d);
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString((cudaError_t)e));
@@ -488,7 +520,17 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream) {
   g_err[0] = '\0';
   return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace,
-                    workspace_bytes, false, stream);
+                    workspace_bytes, false, nullptr, stream);
+}
+
+int fa_bwd_counted(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, long long T, float scale,
+                   int causal, const int* cu_seqlens, void* workspace, size_t workspace_bytes,
+                   long long* tile_counts, void* stream) {
+  g_err[0] = '\0';
+  if (!tile_counts) return fail(FA_ERR_INVALID_ARG, "null tile_counts");
+  return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace,
+                    workspace_bytes, false, tile_counts, stream);
 }
 
 int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -497,7 +539,7 @@ int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void
                          size_t workspace_bytes, void* stream) {
   g_err[0] = '\0';
   return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace,
-                    workspace_bytes, true, stream);
+                    workspace_bytes, true, nullptr, stream);
 }
 
 int fa_selftest_wait_timeout(int limit_ms, void* stream) {

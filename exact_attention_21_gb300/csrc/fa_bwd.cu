@@ -122,13 +122,14 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   };
   struct Unit {
     long long seq0;
-    int L, g, k0, i0, per_head, nsteps;
+    int L, g, k0, i0, per_head, nsteps, sq;
   };
   auto unit_at = [&](int u, Unit& w) -> bool {
     w.g = u % p.Hkv;
     const int rest = u / p.Hkv;
     const int kt = rest / p.B;
-    if (!sequence_bounds(p.cu, rest % p.B, p.N, p.T, w.seq0, w.L, p.status)) return false;
+    w.sq = rest % p.B;
+    if (!sequence_bounds(p.cu, w.sq, p.N, p.T, w.seq0, w.L, p.status)) return false;
     w.k0 = kt * kTile;
     if (w.k0 >= w.L) return false;
     w.i0 = first_q_tile_for(kt, causal);
@@ -354,7 +355,14 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if ((role != 0 || DQ) && !(ok = mbar_wait(kv_full, uc & 1, abort_flag))) break;
         tc_fence_after();
         if (role == 2) {
-          for (int nl = 0; nl < w.nsteps && ok; ++nl) ok = issue_next(n0 + nl);
+          int issued = 0;
+          for (int nl = 0; nl < w.nsteps && ok; ++nl) {
+            ok = issue_next(n0 + nl);
+            issued += ok ? 1 : 0;
+          }
+          // tile pairs whose S^T this thread issued for the unit
+          if (p.tile_count != nullptr && issued > 0)
+            atomicAdd(p.tile_count + w.sq, static_cast<unsigned long long>(issued));
         } else {
           if (ok && role == 1) ok = issue_next(n0);
           if (ok && role == 1 && w.nsteps > 1) ok = issue_next(n0 + 1);

@@ -234,6 +234,7 @@ fa_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       constexpr uint32_t id_mnmn = idesc_bf16_f32(kTile, D, true, true);      // MN-major A x MN-major B
       const uint32_t sKa = smem_u32(sK), sVa = smem_u32(sV), sDSa = smem_u32(sDS), sDOa = smem_u32(sDO);
       bool ok = mbar_wait(kv_full, 0, abort_flag);
+      int issued = 0;  // steps whose S^T this thread issued
       for (int n = 0; n < nsteps && ok; ++n) {
         const int st = n % NQ;
         const uint32_t sQa = smem_u32(stage_q(st));
@@ -248,6 +249,7 @@ fa_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                   kk > 0);
         }
         umma_commit(s_full);
+        ++issued;
         // dP^T = V dO^T into the region the previous dQ has been read out of
         if (!(ok = mbar_wait(do_full, n & 1, abort_flag))) break;
         if (DQ && n >= 1 && !(ok = mbar_wait(dq_free, (n - 1) & 1, abort_flag))) break;
@@ -285,6 +287,8 @@ fa_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           umma_commit(dq_full);
         }
       }
+      if (p.tile_count != nullptr && issued > 0)
+        atomicAdd(p.tile_count + s, static_cast<unsigned long long>(issued));
       if (ok) umma_commit(epi);
       if (!ok) give_up();
       umma_commit(drain);

@@ -59,6 +59,9 @@ struct FwdParams {
   int B, Hq, Hkv, N, group, causal, n_qtiles;
   int group_pairs;    // (sequence, head) pairs per scheduling group
   float scale_log2;   // scale * log2(e)
+  // null, or device [B]: the S-issuing thread adds the (query tile, key tile)
+  // pairs whose S it computed, per sequence (summed over query heads)
+  unsigned long long* tile_count;
 };
 
 struct BwdParams {
@@ -75,6 +78,9 @@ struct BwdParams {
   long long T;
   int B, Hq, Hkv, N, group, causal, n_kvtiles;
   float scale, scale_log2;
+  // null, or device [B]: the S^T-issuing thread adds the (key tile, query
+  // tile) pairs whose S^T it computed, per sequence (summed over query heads)
+  unsigned long long* tile_count;
 };
 
 struct DecodeParams {

@@ -111,7 +111,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   auto unit_of = [&](int k) { return k * G + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x)); };
   struct Unit {
     long long seq0;
-    int L, h, qt, q0, nkv, kvh;
+    int L, h, qt, q0, nkv, kvh, sq;
   };
   auto unit_at = [&](int u, Unit& w) -> bool {
     const int gi = u / (kGroup * p.n_qtiles);  // only the last group can be short
@@ -121,6 +121,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     w.qt = p.n_qtiles - 1 - r / gp;
     w.h = pair % p.Hq;
     const int sq = pair / p.Hq;
+    w.sq = sq;
     if (!sequence_bounds(p.cu, sq, p.N, p.T, w.seq0, w.L, p.status)) return false;
     w.q0 = w.qt * kTile;
     if (w.q0 >= w.L) return false;
@@ -264,7 +265,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (!(ok = mbar_wait(q_full + qb, (uc / Lay::kQBufs) & 1, abort_flag))) break;
         ++uc;
         const uint64_t qd = q_desc + static_cast<uint64_t>((qb * Lay::kTileBytes) >> 4);
-        for (int j = 0; j < w.nkv; ++j, ++g) {
+        int j = 0;
+        for (; j < w.nkv; ++j, ++g) {
           const int b = g % NB, ks = g % NK;
           if (!(ok = mbar_wait(k_full + ks, (g / NK) & 1, abort_flag))) break;
           // buffer b still holds the P of score tile g-NB until P V has read it
@@ -279,6 +281,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           umma_commit(s_full + b);
           umma_commit(k_empty + ks);
         }
+        // tile pairs whose S this thread issued for the unit
+        if (p.tile_count != nullptr && j > 0) atomicAdd(p.tile_count + w.sq, static_cast<unsigned long long>(j));
         if (ok) umma_commit(q_empty + qb);
       }
       if (!ok) give_up();

@@ -36,11 +36,17 @@ void* g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
 // Device address of this device's copy of the scratch array; looked up once
-// per device, with that device current.
+// per device, with that device current, and kept for the life of the process
+// (a cudaDeviceReset unloads the module and leaves the kept address stale).
 int scratch_for_current_device(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
     return fa::record_error(FA_ERR_LAUNCH, "fa_bwd_noalloc: cudaGetDevice failed");
+  if (dev >= kMaxDevices) {
+    char msg[120];
+    snprintf(msg, sizeof msg, "fa_bwd_noalloc: device index %d exceeds the library limit of %d", dev, kMaxDevices);
+    return fa::record_error(FA_ERR_INVALID_ARG, msg);
+  }
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;

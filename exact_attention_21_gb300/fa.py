@@ -23,7 +23,7 @@ FA_ERR_LAUNCH = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_UNSUPPORTED = 5
 
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_deterministic", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
+EXPORTS = ("fa_fwd", "fa_fwd_counted", "fa_bwd", "fa_bwd_counted", "fa_bwd_deterministic", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
            "fa_decode_paged", "fa_decode_paged_fp8", "fa_decode_workspace_size", "fa_kv_quantize_fp8",
            "fa_selftest_wait_timeout", "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
 
@@ -50,6 +50,11 @@ def lib():
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp,
                              ctypes.c_size_t, vp]
         L.fa_bwd.restype = i32
+        L.fa_fwd_counted.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp, vp]
+        L.fa_fwd_counted.restype = i32
+        L.fa_bwd_counted.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp,
+                                     vp, ctypes.c_size_t, vp, vp]
+        L.fa_bwd_counted.restype = i32
         L.fa_bwd_deterministic.argtypes = list(L.fa_bwd.argtypes)
         L.fa_bwd_deterministic.restype = i32
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32,
@@ -111,6 +116,23 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal
     _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                         B, Hq, Hkv, N, d, T, float(scale), int(causal), _ptr(cu_seqlens), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_fwd_counted(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, tile_counts, stream=None):
+    """:func:`fa_fwd`, and the (query tile, key tile) pairs the kernel computed
+    per sequence (summed over query heads) into ``tile_counts`` (int64 [B])."""
+    _check(lib().fa_fwd_counted(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, T, float(scale),
+                                int(causal), _ptr(cu_seqlens), _ptr(tile_counts), _stream(stream)))
+
+
+def fa_bwd_counted(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, workspace,
+                   tile_counts, stream=None):
+    """:func:`fa_bwd`, and the (key tile, query tile) pairs the gradient kernel
+    computed per sequence (summed over query heads) into ``tile_counts``."""
+    _check(lib().fa_bwd_counted(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                _ptr(dv), B, Hq, Hkv, N, d, T, float(scale), int(causal), _ptr(cu_seqlens),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(tile_counts),
+                                _stream(stream)))
 
 
 def fa_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens,

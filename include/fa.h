@@ -44,7 +44,8 @@
  *     caller.
  *
  * Errors: every function returns 0 (FA_OK) or an FA_ERR_* code and never
- * prints or aborts.  Argument errors are found on the host before any launch.
+ * prints or aborts.  Devices with an index of 64 or more are rejected
+ * (FA_ERR_INVALID_ARG).  Argument errors are found on the host before any launch.
  * fa_last_error_string() describes the most recent failure of the calling
  * thread.  Device-side conditions (a bounded wait that ran out, bad packed
  * offsets) are latched in a device word that fa_stream_status() reads.
@@ -125,6 +126,32 @@ int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void
                          const float* lse, void* dq, void* dk, void* dv,
                          int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
                          const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_fwd and fa_bwd with the kernels' own count of the work they did: the
+ * thread that issues the score products adds, for each sequence, the number
+ * of (query tile, key tile) pairs whose scores it computed, summed over the
+ * query heads, into tile_counts[sequence].  Under the causal mask the tiles
+ * entirely above the diagonal are skipped ("Attention 算子优化…", section 四:
+ * about half the tiles lie wholly under the mask), so with 128 x 128 tiles a
+ * sequence of L tokens counts Hq * sum_{i < ceil(L/128)} min(i + 1, ceil(L/128))
+ * pairs (Hq * ceil(L/128)^2 without the mask), the value fa_tile_counts gives
+ * per query head.  This measures what the kernels processed, not what the
+ * host expects them to.
+ *
+ *   tile_counts  device int64 [B], 8-byte aligned (out): zeroed on `stream`
+ *                by the call, then accumulated by the kernel.
+ *   Other arguments, results and errors as for fa_fwd / fa_bwd.  The outputs
+ *   are the same as fa_fwd's / fa_bwd's; only the counts are added.
+ */
+int fa_fwd_counted(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
+                   const int* cu_seqlens, long long* tile_counts, void* stream);
+int fa_bwd_counted(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv,
+                   int B, int Hq, int Hkv, int N, int d, long long T, float scale, int causal,
+                   const int* cu_seqlens, void* workspace, size_t workspace_bytes,
+                   long long* tile_counts, void* stream);
 
 /* Bytes of workspace fa_bwd needs: the row dots D (f32 [Hq, T]) and the f32 dQ
  * accumulator ([T, Hq, d]), each rounded up to 256 bytes.  Returns 0 for
@@ -265,7 +292,9 @@ int fa_tile_counts(int B, const int* lengths, int causal, long long* out);
  *     process exits.
  *   - The first call on each device looks up that device's copy of the array
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the rest of the
+ *     process: after a cudaDeviceReset of that device the array is unusable
+ *     (as is the library's device status word, looked up the same way).
  *   - All calls share the one array and it keeps what the last call left in
  *     it; each call re-initialises what must start at zero.  Calls whose
  *     kernels overlap on the GPU (different streams, no ordering) race on the
