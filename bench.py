@@ -84,7 +84,7 @@ class ClockSampler:
     def mark_off(self):
         self.t_off = time.time()
 
-    def stop(self):
+    def stop_rows(self):
         if self.proc is not None:
             time.sleep(0.12)
             self.proc.terminate()
@@ -92,9 +92,16 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        return list(self.rows)
+
+    def stop(self):
+        return self.summarise(self.stop_rows(), self.t_on, self.t_off)
+
+    @staticmethod
+    def summarise(rows, t_on, t_off):
         sm, mx, reasons = [], [], set()
-        for t, line in self.rows:
-            if self.t_on is None or not (self.t_on - 0.06 <= t <= self.t_off + 0.06):
+        for t, line in rows:
+            if t_on is None or not (t_on - 0.06 <= t <= t_off + 0.06):
                 continue
             parts = [p.strip() for p in line.split(",")]
             try:
@@ -111,17 +118,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_entry(path, workload, kernel):
-    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    summary (profiles/traffic.json), or None."""
+def profile_entry(path, workload, kernel, key):
+    """Field `key` of the committed ncu summary entry (profiles/traffic.json)
+    for `kernel` on `workload`, or None."""
     if not path or not os.path.exists(path):
         return None
     with open(path) as f:
         entries = json.load(f).get("entries", [])
     for e in entries:
         if e.get("workload") == workload and e.get("kernel") == kernel:
-            return e.get("bytes_per_launch")
+            return e.get(key)
     return None
+
+
+def traffic_entry(path, workload, kernel):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/traffic.json), or None."""
+    return profile_entry(path, workload, kernel, "bytes_per_launch")
 
 
 def step_stats(step_ms):
@@ -236,7 +249,7 @@ def bench_ours(args, world, rank, local):
                 for n in outs}
     h2d = sum(t.numel() * t.element_size() for t in pin.values())
     d2h = sum(t.numel() * t.element_size() for t in res_host.values())
-    e2e_steps = max(4, args.steps // 4)
+    e2e_steps = max(20, args.steps)
     sets = []
     for b in range(2):
         sset = {n: torch.empty_like(pin[n], device=dev) for n in pin}
@@ -344,11 +357,114 @@ def bench_ours(args, world, rank, local):
     tr = traffic_entry(args.traffic_file, w.name, kern)
     if tr is not None:
         line["roofline"]["traffic"] = tr
+    pt = profile_entry(args.traffic_file, w.name, kern, "pipe_tensor_pct")
+    if pt is not None:
+        line["roofline"]["pipe_tensor_pct"] = pt
+    if not args.no_per_config and w.name == DEFAULT_WORKLOAD:
+        del sets, pin, res_host, q, k, v, o, lse, host
+        if w.backward:
+            del do, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config_lines(args, rank, dev, stream, flush, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     if pg:
         pg.destroy_process_group()
     return line if rank == 0 else None
+
+
+# The other workloads of the headline table, measured in the default run with
+# the pages' protocol: 20 warm-ups, then timed runs (at least 50, and enough
+# for a few clock samples), L2 flushed before each, median and P90.
+PER_CONFIG = ("fwd_b1_h1_n256_d64", "fwd_b4_h16_n2048_d64", "fwd_b2_h32_n4096_d128_causal",
+              "fwd_varlen8_hq32_hkv8_d128_causal", "decode_b64_hq64_hkv8_n4096_d128")
+
+
+def per_config_lines(args, rank, dev, stream, flush, peaks):
+    import torch
+
+    import exact_attention_21_gb300.fa as fa
+    from exact_attention_21_gb300.inputs import WORKLOADS, make_inputs
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.15)
+    out = {}
+    for name in PER_CONFIG:
+        w = WORKLOADS[name]
+        host = make_inputs(w, seed=rank, with_do=False)
+        d, T, Hq, Hkv = w.d, w.T, w.Hq, w.Hkv
+        cu = host["cu_seqlens"].to(dev) if w.varlen else None
+        B, N = (len(w.seq_lengths), w.N) if w.varlen else (w.B, w.N)
+        q, k, v = (host[n].to(dev) for n in ("q", "k", "v"))
+        del host
+        o = torch.empty_like(q)
+        if w.decode:
+            lse = torch.empty(Hq, B, dtype=torch.float32, device=dev)
+            ws = torch.empty(fa.fa_decode_workspace_size(B, Hq, d, N), dtype=torch.uint8, device=dev)
+
+            def run():
+                fa.fa_decode(q, k, v, o, lse, B, Hq, Hkv, N, d, T, w.scale, cu, ws, stream)
+        else:
+            lse = torch.empty(Hq, T, dtype=torch.float32, device=dev)
+
+            def run():
+                fa.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, T, w.scale, w.causal, cu, stream)
+        for _ in range(20):
+            run()
+        fa.fa_stream_status(stream)
+        # size the timed loop: at least 50 runs and about 0.3 s under load
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            flush.fill_(1.0)
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        per_iter_s = e0.elapsed_time(e1) * 1e-3 / 5
+        n = int(min(5000, max(50, 0.3 / max(per_iter_s, 1e-6))))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        t_on = time.time()
+        for i in range(n):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            run()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_off = time.time()
+        fa.fa_stream_status(stream)
+        ms = sorted(a.elapsed_time(b) for a, b in evs)
+        med, p90 = statistics.median(ms), ms[min(n - 1, int(0.9 * n))]
+        entry = {"runs": n, "us_median": round(med * 1e3, 2), "us_p90": round(p90 * 1e3, 2)}
+        if w.decode:
+            nbytes = w.decode_bytes()
+            gbs = nbytes / (med * 1e-3) / 1e9
+            entry.update(kernel="fa_decode (split kernel + combine)", bytes=nbytes, gbs=round(gbs, 1),
+                         frac_of_hbm=round(gbs / peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]), 4))
+        else:
+            flops = w.fwd_flops()
+            nbytes = 2 * T * d * (2 * Hq + 2 * Hkv) + 4 * Hq * T
+            tf = flops / (med * 1e-3) / 1e12
+            entry.update(kernel="fa_fwd_kernel", gflop=round(flops / 1e9, 3), tflops=round(tf, 1),
+                         frac=round(tf / peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]), 4),
+                         frac_of_sustained=round(
+                             tf / peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"]), 4),
+                         bytes=nbytes, gbs=round(nbytes / (med * 1e-3) / 1e9, 1))
+        pt = profile_entry(args.traffic_file, name, entry["kernel"], "pipe_tensor_pct")
+        if pt is not None:
+            entry["pipe_tensor_pct"] = pt
+        entry["window"] = (t_on, t_off)
+        out[name] = entry
+        del q, k, v, o, lse
+        if w.decode:
+            del ws
+        torch.cuda.empty_cache()
+    rows = sampler.stop_rows()
+    for entry in out.values():
+        t_on, t_off = entry.pop("window")
+        entry["clocks"] = ClockSampler.summarise(rows, t_on, t_off)
+    return out
 
 
 DECODE_METRIC = "attention decode step, K/V cache bytes read per second (1xGB300)"
@@ -636,6 +752,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-config forward / decode lines of the default run")
     ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "traffic.json"))
     args = ap.parse_args()
     if args.warmup < 3:
