@@ -9,6 +9,7 @@ from .attention import (  # noqa: F401
     attention_decode,
     attention_decode_paged,
     attention_forward,
+    attention_forward_paged,
     attention_forward_rows,
     cu_from_lengths,
     tile_counts,

@@ -52,6 +52,11 @@ notes):
   ``block_table[b, 0], block_table[b, 1], ...``, and its first ``seqlens[b]``
   logical tokens are its cache.  Table entries past the cache and page
   contents past it are not read.
+* Paged prefill (``attention_forward_paged``, the same section's page table
+  for a prompt's forward pass): a sequence's queries are its newest tokens and
+  its keys are the first ``seqlens_k`` logical tokens of its pages, so when
+  the cache holds an earlier part of the sequence the causal mask is aligned
+  at the newest token (query i sits at position Lk - Lq + i).
 * Layout: tokens-major ``[T, H, d]`` for q/k/v/o and their gradients, ``[Hq, T]``
   for the LSE; sequence s covers tokens ``cu_seqlens[s] .. cu_seqlens[s+1]-1``.
 
@@ -72,6 +77,7 @@ __all__ = [
     "attention_decode",
     "attention_decode_paged",
     "attention_forward",
+    "attention_forward_paged",
     "attention_forward_rows",
     "attention_backward",
     "tile_counts",
@@ -250,6 +256,64 @@ def attention_decode_paged(q, k_pages, v_pages, block_table, seqlens, scale):
     k = np.concatenate(ks, axis=0)
     v = np.concatenate(vs, axis=0)
     return attention_decode(q, k, v, cu_from_lengths(lens), scale)
+
+
+def _gather_pages(pages, table_row, L):
+    """The first L logical rows of a sequence whose logical page j is physical
+    page table_row[j] of ``pages`` [num_pages, page_size, H, d]."""
+    page = pages.shape[1]
+    n = (L + page - 1) // page
+    if n > len(table_row):
+        raise ValueError("block table too short for the cache length")
+    if n == 0:
+        return pages[:0, 0]
+    return np.concatenate([pages[int(table_row[j])] for j in range(n)], axis=0)[:L]
+
+
+def attention_forward_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seqlens_k, scale, causal):
+    """Prefill over a paged K/V cache: O and LSE of packed queries (fp64).
+
+    q: [Tq, Hq, d]; sequence b's queries are rows cu_seqlens_q[b] ..
+    cu_seqlens_q[b+1]-1 (Lq of them), its newest tokens.  Its keys and values
+    are the first seqlens_k[b] = Lk logical tokens of its pages in
+    k_pages, v_pages [num_pages, page_size, Hkv, d], logical page j being
+    physical page block_table[b, j]; when Lk > Lq the first Lk - Lq of them
+    are an earlier, cached part of the sequence.  Query i of the sequence is
+    the token at position Lk - Lq + i, so under the causal mask it sees keys
+    j <= Lk - Lq + i (the mask aligned at the newest token; with Lk = Lq this
+    is the ordinary mask).  A row with no visible key gives O = 0 and
+    LSE = -inf.  Returns o [Tq, Hq, d] and lse [Hq, Tq].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_pages = np.asarray(k_pages, dtype=np.float64)
+    v_pages = np.asarray(v_pages, dtype=np.float64)
+    table = np.asarray(block_table, dtype=np.int64)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    lens_k = np.asarray(seqlens_k, dtype=np.int64)
+    Tq, Hq, d = q.shape
+    Hkv = k_pages.shape[2]
+    if Hq % Hkv != 0 or k_pages.shape[3] != d or v_pages.shape != k_pages.shape:
+        raise ValueError("q [Tq,Hq,d] and pages [num_pages,page_size,Hkv,d] with Hq a multiple of Hkv expected")
+    if cu[0] != 0 or cu[-1] != Tq or np.any(np.diff(cu) < 0) or len(lens_k) != len(cu) - 1:
+        raise ValueError("cu_seqlens_q must rise from 0 to Tq over B + 1 entries, seqlens_k have B entries")
+    group = Hq // Hkv
+    o = np.zeros((Tq, Hq, d), dtype=np.float64)
+    lse = np.full((Hq, Tq), -np.inf, dtype=np.float64)
+    for b in range(len(lens_k)):
+        a, e = int(cu[b]), int(cu[b + 1])
+        Lq, Lk = e - a, int(lens_k[b])
+        if Lq == 0:
+            continue
+        K = _gather_pages(k_pages, table[b], Lk)
+        V = _gather_pages(v_pages, table[b], Lk)
+        q_pos = (Lk - Lq) + np.arange(Lq)
+        for h in range(Hq):
+            kv = h // group
+            S = _scores(q[a:e, h, :], K[:, kv, :], scale, causal, q_pos, Lk)
+            P, lse_rows = _safe_softmax(S)
+            o[a:e, h, :] = P @ V[:, kv, :]
+            lse[h, a:e] = lse_rows
+    return o, lse
 
 
 def attention_backward(q, k, v, do, cu_seqlens, scale, causal, return_rowsum=False):

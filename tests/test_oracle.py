@@ -542,3 +542,127 @@ def test_paged_decode_reads_the_right_pages():
     o3, _ = oracle.attention_decode_paged(q, kp, vp, t_tail, lengths, 0.5)
     assert np.abs(o1[0] - o3[0]).max() > 1e-3
     np.testing.assert_array_equal(o1[1], o3[1])
+
+
+# ---------------------------------------------------------------- paged prefill
+
+def _prefill_pages(seq_kv, page, Hkv, d, seed):
+    """Lays per-sequence K/V arrays (list of [Lk, Hkv, d]) out as a shuffled
+    page pool with garbage in every unused row and junk table entries."""
+    r = np.random.default_rng(seed)
+    npg = [(len(kv) + page - 1) // page for kv in seq_kv]
+    total = sum(npg) + 3
+    phys = r.permutation(total)
+    pool = r.standard_normal((total, page, Hkv, d)) * 50
+    table = np.full((len(seq_kv), max(npg + [1]) + 1), -3, dtype=np.int64)
+    nxt = 0
+    for b, kv in enumerate(seq_kv):
+        for j in range(npg[b]):
+            pg = phys[nxt]
+            nxt += 1
+            table[b, j] = pg
+            rows = kv[j * page:(j + 1) * page]
+            pool[pg, :len(rows)] = rows
+    return pool, table
+
+
+def _prefill_case(Lk, Lq, Hq=4, Hkv=2, d=8, page=4, seed=50):
+    """Full per-sequence q, k, v (all Lk tokens) and the paged inputs of the
+    chunk made of each sequence's last Lq tokens."""
+    r = np.random.default_rng(seed)
+    qs = [r.standard_normal((L, Hq, d)) for L in Lk]
+    ks = [r.standard_normal((L, Hkv, d)) for L in Lk]
+    vs = [r.standard_normal((L, Hkv, d)) for L in Lk]
+    kp, table = _prefill_pages(ks, page, Hkv, d, seed + 1)
+    # the value pool uses the same pages as the key pool
+    vp = np.random.default_rng(seed + 2).standard_normal(kp.shape) * 50
+    for b, vv in enumerate(vs):
+        for j in range((len(vv) + page - 1) // page):
+            rows = vv[j * page:(j + 1) * page]
+            vp[table[b, j], :len(rows)] = rows
+    q_chunk = np.concatenate([q[len(q) - lq:] for q, lq in zip(qs, Lq)], axis=0)
+    return qs, ks, vs, kp, vp, table, q_chunk, oracle.cu_from_lengths(Lq)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("page", [1, 4, 16])
+def test_paged_prefill_without_prefix_equals_packed_forward(causal, page):
+    """Lk = Lq: the paged prefill is the packed forward over the same keys."""
+    L = [37, 0, 16, 5, 64]
+    qs, ks, vs, kp, vp, table, qc, cu = _prefill_case(L, L, page=page, seed=51)
+    o, l = oracle.attention_forward_paged(qc, kp, vp, table, cu, L, 0.3, causal)
+    k = np.concatenate(ks, axis=0)
+    v = np.concatenate(vs, axis=0)
+    o_ref, l_ref = F(qc, k, v, cu, 0.3, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l, l_ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("Lq", [[1, 5, 3], [7, 12, 30], [40, 17, 9]])
+def test_paged_prefill_with_cached_prefix_equals_rows_of_full_causal(Lq):
+    """Chunked prefill: the chunk of the newest Lq tokens, with the first
+    Lk - Lq tokens already in the cache, gives exactly the last Lq rows of
+    causal attention over the whole sequence (which pins the mask alignment:
+    a mask aligned at the first token would differ)."""
+    Lk = [40, 17, 30]
+    qs, ks, vs, kp, vp, table, qc, cu = _prefill_case(Lk, Lq, seed=52)
+    o, l = oracle.attention_forward_paged(qc, kp, vp, table, cu, Lk, 0.4, True)
+    for b in range(len(Lk)):
+        o_full, l_full = F(qs[b], ks[b], vs[b], [0, Lk[b]], 0.4, True)
+        a, e = int(cu[b]), int(cu[b + 1])
+        np.testing.assert_allclose(o[a:e], o_full[Lk[b] - Lq[b]:], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(l[:, a:e], l_full[:, Lk[b] - Lq[b]:], rtol=1e-12, atol=1e-13)
+    # top-left alignment (query i sees keys j <= i) is a different result
+    if any(lq < lk for lq, lk in zip(Lq, Lk)):
+        wrong, _ = F(qc, np.concatenate([k[:lq] for k, lq in zip(ks, Lq)], axis=0),
+                       np.concatenate([v[:lq] for v, lq in zip(vs, Lq)], axis=0), cu, 0.4, True)
+        assert np.abs(wrong - o).max() > 1e-3
+
+
+def test_paged_prefill_single_query_equals_paged_decode():
+    """Lq = 1 at the end of the cache is one decoding step (every key visible),
+    with or without the mask."""
+    Lk = [9, 33, 1]
+    qs, ks, vs, kp, vp, table, qc, cu = _prefill_case(Lk, [1, 1, 1], seed=53)
+    for causal in (False, True):
+        o, l = oracle.attention_forward_paged(qc, kp, vp, table, cu, Lk, 0.5, causal)
+        o_ref, l_ref = oracle.attention_decode_paged(qc.reshape(3, 4, 8), kp, vp, table, Lk, 0.5)
+        np.testing.assert_allclose(o, o_ref.reshape(3, 4, 8), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(l, l_ref, rtol=1e-12, atol=1e-13)
+
+
+def test_paged_prefill_non_causal_rows_are_decode_steps():
+    """Without the mask each query row sees the whole cache: row i equals a
+    decoding step of that query over the sequence's Lk keys."""
+    Lk, Lq = [23, 8], [5, 8]
+    qs, ks, vs, kp, vp, table, qc, cu = _prefill_case(Lk, Lq, seed=54)
+    o, l = oracle.attention_forward_paged(qc, kp, vp, table, cu, Lk, 0.3, False)
+    for b in range(2):
+        a, e = int(cu[b]), int(cu[b + 1])
+        cache_cu = oracle.cu_from_lengths([Lk[b]] * (e - a))
+        kk = np.concatenate([ks[b]] * (e - a), axis=0)
+        vv = np.concatenate([vs[b]] * (e - a), axis=0)
+        o_ref, l_ref = DEC(qc[a:e], kk, vv, cache_cu, 0.3)
+        np.testing.assert_allclose(o[a:e], o_ref, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(l[:, a:e], l_ref, rtol=1e-12, atol=1e-13)
+
+
+def test_paged_prefill_rows_without_visible_keys_and_page_swaps():
+    """Causal with fewer cached keys than queries: the first Lq - Lk rows see
+    no key (O = 0, LSE = -inf).  Swapping the partly filled last page with a
+    full one changes that sequence's result and no other."""
+    Lk, Lq = [3, 12], [6, 12]
+    qs, ks, vs, kp, vp, table, qc, cu = _prefill_case(Lk, [3, 12], seed=55)
+    q6 = np.concatenate([np.random.default_rng(56).standard_normal((3, 4, 8)), qc], axis=0)
+    cu6 = oracle.cu_from_lengths(Lq)
+    o, l = oracle.attention_forward_paged(q6, kp, vp, table, cu6, Lk, 0.3, True)
+    assert np.all(o[:3] == 0.0) and np.all(np.isneginf(l[:, :3]))
+    assert np.all(np.isfinite(l[:, 3:]))
+    t2 = table.copy()
+    t2[1, [0, 2]] = t2[1, [2, 0]]  # sequence 1: 12 rows in pages of 4, all full
+    o2, _ = oracle.attention_forward_paged(q6, kp, vp, t2, cu6, Lk, 0.3, True)
+    np.testing.assert_array_equal(o2[:6], o[:6])
+    assert np.abs(o2[6:] - o[6:]).max() > 1e-3  # causal: key order matters
+    o3, _ = oracle.attention_forward_paged(q6, kp, vp, t2, cu6, Lk, 0.3, False)
+    o4, _ = oracle.attention_forward_paged(q6, kp, vp, table, cu6, Lk, 0.3, False)
+    np.testing.assert_allclose(o3[6:], o4[6:], rtol=1e-12, atol=1e-13)  # no mask: a key set
