@@ -293,6 +293,59 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, nullptr, stream);
 }
 
+int fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                 const int* cu_seqlens_q, const int* seqlens_k, void* o, float* lse, int B, int Hq, int Hkv,
+                 int max_seqlen_q, int d, long long Tq, float scale, int causal, int page_size, int num_pages,
+                 int max_pages, void* stream) {
+  g_err[0] = '\0';
+  if (!block_table || !cu_seqlens_q || !seqlens_k)
+    return fail(FA_ERR_INVALID_ARG, "block_table, cu_seqlens_q and seqlens_k must be non-null");
+  if (page_size != 8 && page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+    return fail(FA_ERR_INVALID_ARG, "page_size must be 8, 16, 32, 64 or 128 (got %d)", page_size);
+  if (num_pages < 1 || max_pages < 1) return fail(FA_ERR_INVALID_ARG, "num_pages and max_pages must be >= 1");
+  if (static_cast<long long>(max_pages) * page_size > (1ll << 30) ||
+      static_cast<long long>(num_pages) * page_size > (1ll << 31) - 1)
+    return fail(FA_ERR_INVALID_ARG, "page pool or page table too large");
+  if (!aligned(block_table, 4) || !aligned(seqlens_k, 4))
+    return fail(FA_ERR_INVALID_ARG, "block_table and seqlens_k must be 4-byte aligned");
+  Shape s{};
+  int rc = check_shape(B, Hq, Hkv, max_seqlen_q, d, Tq, scale, causal, cu_seqlens_q, &s);
+  if (rc) return rc;
+  if (!q || !k_pages || !v_pages || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(o, 16))
+    return fail(FA_ERR_INVALID_ARG, "q, k_pages, v_pages, o must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  DeviceState* dev = nullptr;
+  if ((rc = device_state(&dev))) return rc;
+  const long long rows = static_cast<long long>(num_pages) * page_size;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_map(&tq, q, Tq, Hq, d, "q")) || (rc = make_map(&tk, k_pages, rows, Hkv, d, "k_pages", page_size)) ||
+      (rc = make_map(&tv, v_pages, rows, Hkv, d, "v_pages", page_size)))
+    return rc;
+  fa::FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.cu = cu_seqlens_q;
+  p.status = dev->status;
+  p.T = Tq;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = max_seqlen_q;
+  p.group = Hq / Hkv;
+  p.causal = causal;
+  p.n_qtiles = s.n_tiles;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.block_table = block_table;
+  p.seqlens_k = seqlens_k;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  int e = fa::launch_fwd(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString((cudaError_t)e));
+  return FA_OK;
+}
+
 int fa_fwd_counted(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
                    int d, long long T, float scale, int causal, const int* cu_seqlens, long long* tile_counts,
                    void* stream) {

@@ -62,6 +62,12 @@ struct FwdParams {
   // null, or device [B]: the S-issuing thread adds the (query tile, key tile)
   // pairs whose S it computed, per sequence (summed over query heads)
   unsigned long long* tile_count;
+  // paged K/V (prefill over a paged cache): sequence b's keys are the first
+  // seqlens_k[b] logical tokens of its pages, logical page j being physical
+  // page block_table[b * max_pages + j] of the pool; null for contiguous K/V
+  const int* block_table;
+  const int* seqlens_k;
+  int page_size, max_pages, num_pages;
 };
 
 struct BwdParams {

@@ -88,7 +88,10 @@ struct FwdLayout {
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // P values stay below 2^8 between rescales
 
-template <int D>
+// PAGED: K and V are read through a page table (prefill over a paged cache),
+// the keys of a sequence may outnumber its queries (a cached earlier part),
+// and the causal mask is aligned at the newest token.
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(FwdLayout<D>::kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -112,6 +115,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   struct Unit {
     long long seq0;
     int L, h, qt, q0, nkv, kvh, sq;
+    int Lk, off;  // keys of the sequence; query i sits at key position off + i
   };
   auto unit_at = [&](int u, Unit& w) -> bool {
     const int gi = u / (kGroup * p.n_qtiles);  // only the last group can be short
@@ -125,7 +129,23 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (!sequence_bounds(p.cu, sq, p.N, p.T, w.seq0, w.L, p.status)) return false;
     w.q0 = w.qt * kTile;
     if (w.q0 >= w.L) return false;
-    w.nkv = kv_tiles_for(w.qt, w.L, causal);
+    if constexpr (PAGED) {
+      const int lk = __ldg(p.seqlens_k + sq);
+      if (lk < 0 || lk > p.max_pages * p.page_size) {
+        atomicOr(p.status, kStatusBadOffsets);
+        return false;
+      }
+      w.Lk = lk;
+      w.off = lk - w.L;
+      const int n_kt = (lk + kTile - 1) / kTile;
+      // causal: the tile's last query row sees keys up to off + that row
+      const int last = w.off + min(w.q0 + kTile - 1, w.L - 1);
+      w.nkv = !causal ? n_kt : (last < 0 ? 0 : min(n_kt, last / kTile + 1));
+    } else {
+      w.Lk = w.L;
+      w.off = 0;
+      w.nkv = kv_tiles_for(w.qt, w.L, causal);
+    }
     w.kvh = w.h / p.group;
     return true;
   };
@@ -192,7 +212,82 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     *abort_flag = 1;
   };
 
-  if (warp == 0 || warp == 3) {
+  if (PAGED && (warp == 0 || warp == 3)) {
+    // ------------------------------------------------------------ TMA producers, paged K/V
+    // The whole warp walks the units: lane 0 waits for ring slots and posts
+    // byte counts, then lane j copies page j of the key tile (one box of
+    // page_size rows per 64-column chunk, 1 KB-aligned in the slot for
+    // page_size >= 8, so the 128-byte swizzle pattern runs on across boxes).
+    const bool is_k = warp == 0;  // warp 0: Q and K; warp 3: V
+    if (lane == 0) {
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+      } else {
+        tma_prefetch_desc(&tm_v);
+      }
+    }
+    const int ps = p.page_size, pages_per_tile = kTile / ps;
+    int k_uses[NK] = {}, v_uses[NV] = {}, q_uses[2] = {};
+    int jg = 0, uc = 0;  // key tiles and units so far
+    bool ok = true;
+    for (int k = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++k)) {
+      Unit w;
+      if (!unit_at(u, w)) continue;
+      if (is_k) {
+        const int qb = uc % Lay::kQBufs, qn = uc / Lay::kQBufs;
+        if (lane == 0) {
+          if (qn >= 1) ok = mbar_wait(q_empty + qb, (qn - 1) & 1, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(q_full + qb, Lay::kTileBytes);
+            for (int c = 0; c < Lay::kChunks; ++c)
+              tma_load_3d(sQ + qb * Lay::kTileBytes + c * Lay::kChunkBytes, &tm_q, q_full + qb, c * 64, w.h,
+                          static_cast<int>(w.seq0 + w.q0));
+          }
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        ++q_uses[qb];
+      }
+      ++uc;
+      for (int j = 0; j < w.nkv; ++j, ++jg) {
+        const int slot = is_k ? jg % NK : jg % NV;
+        uint64_t* full = is_k ? k_full + slot : v_full + slot;
+        if (lane == 0) {
+          const int nst = is_k ? NK : NV;
+          if (jg >= nst) ok = mbar_wait((is_k ? k_empty : v_empty) + slot, ((jg / nst) - 1) & 1, abort_flag);
+          if (ok) mbar_arrive_expect_tx(full, Lay::kTileBytes);
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        if (lane < pages_per_tile) {
+          // pages past the cache hold keys that are masked: page 0 is read
+          const int lp = j * pages_per_tile + lane;
+          int phys = 0;
+          if (lp * ps < w.Lk) {
+            phys = __ldg(p.block_table + static_cast<long long>(w.sq) * p.max_pages + lp);
+            if (phys < 0 || phys >= p.num_pages) {
+              atomicOr(p.status, kStatusBadOffsets);
+              phys = 0;
+            }
+          }
+          uint8_t* dst = (is_k ? sK : sV) + slot * Lay::kTileBytes + lane * ps * 128;
+          for (int c = 0; c < Lay::kChunks; ++c)
+            tma_load_3d(dst + c * Lay::kChunkBytes, is_k ? &tm_k : &tm_v, full, c * 64, w.kvh, phys * ps);
+        }
+        if (is_k) ++k_uses[slot]; else ++v_uses[slot];
+      }
+    }
+    if (lane == 0) {
+      if (!ok) give_up();
+      // Every copy this warp issued has landed before the CTA may exit.
+      int never = 0;
+      for (int i = 0; i < Lay::kQBufs; ++i)
+        if (q_uses[i]) mbar_wait(q_full + i, (q_uses[i] - 1) & 1, &never);
+      for (int i = 0; i < NK; ++i)
+        if (k_uses[i]) mbar_wait(k_full + i, (k_uses[i] - 1) & 1, &never);
+      for (int i = 0; i < NV; ++i)
+        if (v_uses[i]) mbar_wait(v_full + i, (v_uses[i] - 1) & 1, &never);
+    }
+  } else if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ TMA producers
     if (lane == 0) {
       const bool is_k = warp == 0;  // warp 0: Q and K; warp 3: V
@@ -360,8 +455,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tmem_ld_x64(tmem_addr(tS, lane_base, half * 64), sr);
         float* x = reinterpret_cast<float*>(sr);
         const int k0 = j * kTile + half * 64;
-        if ((causal && j == w.qt) || (k0 + 64 > w.L)) {
-          const int lim = causal ? min(qpos + 1, w.L) : w.L;  // visible keys: [0, lim)
+        // visible keys of this row: [0, lim)
+        const bool need_mask = PAGED ? ((causal && k0 + 63 > w.off + w.q0) || (k0 + 64 > w.Lk))
+                                     : ((causal && j == w.qt) || (k0 + 64 > w.L));
+        if (need_mask) {
+          const int lim = PAGED ? (causal ? min(w.off + qpos + 1, w.Lk) : w.Lk) : (causal ? min(qpos + 1, w.L) : w.L);
 #pragma unroll
           for (int i = 0; i < 64; ++i)
             if (k0 + i >= lim) x[i] = -INFINITY;
@@ -472,6 +570,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int cc = 0; cc < D / 64; ++cc)
           tmem_ld_x32(tmem_addr(tmem + Lay::kColO, lane_base, half * (D / 2) + cc * 32), ov + 32 * cc);
       }
+      if constexpr (PAGED) {
+        // a row with no visible key (more queries than keys under the mask)
+        // has nothing accumulated in O: its output is 0
+        if (!(lt > 0.f)) {
+#pragma unroll
+          for (int t = 0; t < D / 2; ++t) ov[t] = 0u;
+        }
+      }
       // O is in registers: the next unit's P V may start overwriting it
       tc_fence_before();
       mbar_arrive(o_free);
@@ -565,11 +671,12 @@ static int simulate_group_pairs(const FwdParams& p, int G, int d) {
 }
 
 // Host-side launch for one head dimension; returns a cudaError_t value.
-template <int D>
+template <int D, bool PAGED>
 int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                  cudaStream_t stream) {
   using Lay = FwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_fwd_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -578,13 +685,15 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   const int grid = static_cast<int>(units < sms ? units : sms);  // one CTA per SM, persistent
   FwdParams q = p;
   q.group_pairs = choose_group_pairs(p, grid, D);
-  fa_fwd_kernel<D><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tq, tk, tv, q);
+  fa_fwd_kernel<D, PAGED><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tq, tk, tv, q);
   return cudaGetLastError();
 }
 
 int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                cudaStream_t stream) {
-  return d == 64 ? launch_fwd_d<64>(tq, tk, tv, p, stream) : launch_fwd_d<128>(tq, tk, tv, p, stream);
+  if (p.block_table != nullptr)
+    return d == 64 ? launch_fwd_d<64, true>(tq, tk, tv, p, stream) : launch_fwd_d<128, true>(tq, tk, tv, p, stream);
+  return d == 64 ? launch_fwd_d<64, false>(tq, tk, tv, p, stream) : launch_fwd_d<128, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace fa

@@ -23,7 +23,7 @@ FA_ERR_LAUNCH = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_UNSUPPORTED = 5
 
-EXPORTS = ("fa_fwd", "fa_fwd_counted", "fa_bwd", "fa_bwd_counted", "fa_bwd_deterministic", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
+EXPORTS = ("fa_fwd", "fa_fwd_counted", "fa_fwd_paged", "fa_bwd", "fa_bwd_counted", "fa_bwd_deterministic", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
            "fa_decode_paged", "fa_decode_paged_fp8", "fa_decode_workspace_size", "fa_kv_quantize_fp8",
            "fa_selftest_wait_timeout", "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
 
@@ -50,6 +50,9 @@ def lib():
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp,
                              ctypes.c_size_t, vp]
         L.fa_bwd.restype = i32
+        L.fa_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, i32, i32,
+                                   i32, vp]
+        L.fa_fwd_paged.restype = i32
         L.fa_fwd_counted.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp, vp, vp]
         L.fa_fwd_counted.restype = i32
         L.fa_bwd_counted.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp,
@@ -116,6 +119,30 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, T, scale, causal
     _check(lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                         B, Hq, Hkv, N, d, T, float(scale), int(causal), _ptr(cu_seqlens), _ptr(workspace),
                         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def fa_fwd_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seqlens_k, o, lse, max_seqlen_q, page_size, scale,
+                 causal, stream=None):
+    """Prefill over a paged K/V cache into caller-allocated ``o`` [Tq,Hq,d] and
+    ``lse`` [Hq,Tq]; the pools are [num_pages * page_size, Hkv, d]."""
+    Tq, Hq, d = q.shape
+    Hkv = k_pages.shape[1]
+    B, max_pages = block_table.shape
+    num_pages = k_pages.shape[0] // page_size
+    _check(lib().fa_fwd_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(cu_seqlens_q),
+                              _ptr(seqlens_k), _ptr(o), _ptr(lse), B, Hq, Hkv, max_seqlen_q, d, Tq, float(scale),
+                              int(causal), page_size, num_pages, max_pages, _stream(stream)))
+
+
+def attention_forward_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seqlens_k, max_seqlen_q, page_size,
+                            causal, scale=None, stream=None):
+    """Allocates O and LSE and runs :func:`fa_fwd_paged`."""
+    Tq, Hq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, Tq, dtype=torch.float32, device=q.device)
+    fa_fwd_paged(q, k_pages, v_pages, block_table, cu_seqlens_q, seqlens_k, o, lse, max_seqlen_q, page_size,
+                 d ** -0.5 if scale is None else scale, causal, stream)
+    return o, lse
 
 
 def fa_fwd_counted(q, k, v, o, lse, B, Hq, Hkv, N, d, T, scale, causal, cu_seqlens, tile_counts, stream=None):

@@ -40,7 +40,7 @@ class Workload:
     backward: bool = False
     decode: bool = False  # one new query per sequence against a K/V cache of the lengths above
     fp8: bool = False     # decoding over an E4M3 cache with per-token f32 scales
-    page_size: int = 0    # decoding over a paged cache with pages of this many tokens (0: packed)
+    page_size: int = 0    # K/V in a paged cache with pages of this many tokens (0: contiguous)
 
     @property
     def seq_lengths(self) -> list:
@@ -110,6 +110,11 @@ WORKLOADS = {
     # the same step with the cache in 16-token pages scattered over a pool
     "decode_paged16_b64_hq64_hkv8_n4096_d128": Workload(
         "decode_paged16_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True, False, 16),
+    # prefill of the packed workload's sequences and heads with K/V in 16-token
+    # pages scattered over a pool (no cached prefix: keys = queries)
+    "fwd_paged16_varlen8_hq32_hkv8_d128_causal": Workload(
+        "fwd_paged16_varlen8_hq32_hkv8_d128_causal", 8, 32, 8, max(VARLEN_LENGTHS), 128, True, VARLEN_LENGTHS,
+        False, False, False, 16),
     # the packed workload's sequences and heads, one new token each
     "decode_varlen8_hq32_hkv8_d128": Workload(
         "decode_varlen8_hq32_hkv8_d128", 8, 32, 8, max(VARLEN_LENGTHS), 128, False, VARLEN_LENGTHS, False,
@@ -199,4 +204,9 @@ def make_inputs(w: Workload, seed=0, with_do=None):
         with_do = w.backward
     t = make_qkv(w.T, w.Hq, w.Hkv, w.d, seed=seed, with_do=with_do)
     t["cu_seqlens"] = cu_seqlens_of(w.seq_lengths)
+    if w.page_size:
+        # prefill over a paged cache: the same k, v laid out in pages
+        t["k_pages"], t["v_pages"], t["block_table"] = make_paged_cache(t["k"], t["v"], w.seq_lengths, w.page_size,
+                                                                       seed=seed)
+        t["seqlens"] = torch.tensor(w.seq_lengths, dtype=torch.int32)
     return t

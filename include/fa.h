@@ -128,6 +128,45 @@ int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void
                          const int* cu_seqlens, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Forward pass (prefill) over a paged K/V cache ("Attention 算子优化…",
+ * section 五, PagedAttention: the cache is a pool of fixed-size pages and each
+ * sequence reaches its pages through a page table, so its K/V need not be
+ * contiguous).  The queries are packed as in fa_fwd's packed mode; sequence b
+ * has Lq = cu_seqlens_q[b+1] - cu_seqlens_q[b] queries, its newest tokens,
+ * and Lk = seqlens_k[b] keys: logical key j is row
+ *     block_table[b * max_pages + j / page_size] * page_size + j % page_size
+ * of the pool.  Lk may exceed Lq (an earlier part of the sequence already in
+ * the cache, e.g. chunked prefill or a cached prompt prefix): query i is then
+ * the token at position Lk - Lq + i, and under the causal mask it sees keys
+ * j <= Lk - Lq + i (the mask aligned at the newest token; Lk = Lq gives the
+ * ordinary mask).  A query row that sees no key (causal with Lk < Lq) gets
+ * O = 0 and LSE = -inf.  Tiles wholly under the mask are skipped.
+ *
+ *   q         [Tq, Hq, d] bf16, 16-byte aligned                     (in)
+ *   k_pages, v_pages  [num_pages * page_size, Hkv, d] bf16 page pool,
+ *             16-byte aligned (in).  Pool rows that hold no key of any
+ *             sequence may hold anything finite: they are read (and
+ *             multiplied by zero probabilities) when they share a page or a
+ *             128-key tile with live keys.
+ *   block_table  device int32 [B, max_pages]                        (in)
+ *   cu_seqlens_q device int32 [B + 1] query offsets, as in fa_fwd    (in)
+ *   seqlens_k    device int32 [B]: keys of each sequence, at most
+ *                max_pages * page_size                              (in)
+ *   o [Tq, Hq, d] bf16, lse [Hq, Tq] f32                             (out)
+ *   max_seqlen_q  longest query chunk (grid sizing); Tq = cu_seqlens_q[B].
+ *   page_size     8, 16, 32, 64 or 128 tokens.
+ *   Other arguments as for fa_fwd.  A length out of range, or a table entry
+ *   inside a cache that is not a page of the pool, is detected on the device:
+ *   that sequence's result is not valid (a bad length skips it, a bad entry
+ *   reads page 0 instead) and the next fa_stream_status() reports
+ *   FA_ERR_INVALID_ARG.
+ */
+int fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                 const int* cu_seqlens_q, const int* seqlens_k, void* o, float* lse,
+                 int B, int Hq, int Hkv, int max_seqlen_q, int d, long long Tq, float scale, int causal,
+                 int page_size, int num_pages, int max_pages, void* stream);
+
+/*
  * fa_fwd and fa_bwd with the kernels' own count of the work they did: the
  * thread that issues the score products adds, for each sequence, the number
  * of (query tile, key tile) pairs whose scores it computed, summed over the
