@@ -75,7 +75,8 @@ struct BwdLayout {
   static constexpr int kOffDS = kOffV + kTileBytes;
   static constexpr int kOffRing = kOffDS + kDSBufs * kDSBytes;
   // -LSE log2 e and -D of the step's 128 queries, f32, in slot n % 2: the
-  // score warpgroups read them during step n only
+  // score warpgroups read them during step n only.  Interleaved by query
+  // pair, {-LSE q, -LSE q+1, -D q, -D q+1}, so one 16-byte load serves a pair.
   static constexpr int kOffStats = kOffRing + kStages * kStageBytes;
   static constexpr int kStatBytes = 2 * kTile * 4;
   static constexpr int kOffBar = kOffStats + 2 * kStatBytes;
@@ -265,8 +266,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
           for (int t = 0; t < kTile / 32; ++t) {
             // stored negated: -LSE * log2 e and -D (queries past the end: P = 0)
-            stats[lane + 32 * t] = -lv[t] * kLog2e;
-            stats[kTile + lane + 32 * t] = -dv[t];
+            const int qq = lane + 32 * t;
+            stats[(qq >> 1) * 4 + (qq & 1)] = -lv[t] * kLog2e;
+            stats[(qq >> 1) * 4 + 2 + (qq & 1)] = -dv[t];
           }
         }
         mbar_arrive(qdo_full + st);
@@ -448,8 +450,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (!(ok = mbar_wait(qdo_full + st, (n / NS) & 1, abort_flag))) break;
       tc_fence_after();
       const int q0 = step_qtile(w, nl) * kTile;
-      const float2* nlse2 = reinterpret_cast<const float2*>(step_stats(n)) + half * 32;
-      const float2* ndot2 = nlse2 + kTile / 2;
+      const float4* nst4 = reinterpret_cast<const float4*>(step_stats(n)) + half * 32;
       // Keys past the sequence end and keys after the query (diagonal tile,
       // causal) get P = 0: query columns below zero_below are zeroed.
       // Queries past the end carry -LSE = -inf, so their P is 0 already.
@@ -470,7 +471,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const bool mask_chunk = zero_below > col0;
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          const float2 nl2 = nlse2[cl * 8 + t], nd = ndot2[cl * 8 + t];
+          const float4 s4 = nst4[cl * 8 + t];
+          const float2 nl2 = make_float2(s4.x, s4.y), nd = make_float2(s4.z, s4.w);
           const float2 x = fma2(make_float2(__uint_as_float(sv[2 * t]), __uint_as_float(sv[2 * t + 1])), c2, nl2);
           float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (mask_chunk) {
@@ -552,8 +554,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (!(ok = mbar_wait(dq_full + (n & 1), (n >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       uint32_t v[D];
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) tmem_ld_x32(tmem_addr(region(n), lane_base, Lay::kColDQ + cc * 32), v + 32 * cc);
+      tmem_ld_x64(tmem_addr(region(n), lane_base, Lay::kColDQ), v);
       tc_fence_before();
       mbar_arrive(dq_free + (n & 1));
       const int h = step_head(w, nl), q0 = step_qtile(w, nl) * kTile;
