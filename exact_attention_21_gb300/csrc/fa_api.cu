@@ -15,8 +15,8 @@
 #include "fa_common.cuh"
 
 namespace fa {
-int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-               cudaStream_t stream);
+int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+               const FwdParams& p, cudaStream_t stream);
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool deterministic,
                cudaStream_t stream);
@@ -256,9 +256,9 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
   if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
   DeviceState* dev = nullptr;
   if ((rc = device_state(&dev))) return rc;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((rc = make_map(&tq, q, T, Hq, d, "q")) || (rc = make_map(&tk, k, T, Hkv, d, "k")) ||
-      (rc = make_map(&tv, v, T, Hkv, d, "v")))
+      (rc = make_map(&tv, v, T, Hkv, d, "v")) || (rc = make_map(&to, o, T, Hq, d, "o")))
     return rc;
   fa::FwdParams p{};
   p.o = o;
@@ -280,7 +280,7 @@ static int fwd_common(const void* q, const void* k, const void* v, void* o, floa
     if (z != cudaSuccess) return fail(FA_ERR_LAUNCH, "zeroing tile_counts failed: %s", cudaGetErrorString(z));
     p.tile_count = reinterpret_cast<unsigned long long*>(tile_count);
   }
-  int e = fa::launch_fwd(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  int e = fa::launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;
 }
@@ -318,9 +318,9 @@ int fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, const 
   DeviceState* dev = nullptr;
   if ((rc = device_state(&dev))) return rc;
   const long long rows = static_cast<long long>(num_pages) * page_size;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((rc = make_map(&tq, q, Tq, Hq, d, "q")) || (rc = make_map(&tk, k_pages, rows, Hkv, d, "k_pages", page_size)) ||
-      (rc = make_map(&tv, v_pages, rows, Hkv, d, "v_pages", page_size)))
+      (rc = make_map(&tv, v_pages, rows, Hkv, d, "v_pages", page_size)) || (rc = make_map(&to, o, Tq, Hq, d, "o")))
     return rc;
   fa::FwdParams p{};
   p.o = o;
@@ -341,7 +341,7 @@ int fa_fwd_paged(const void* q, const void* k_pages, const void* v_pages, const 
   p.page_size = page_size;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
-  int e = fa::launch_fwd(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  int e = fa::launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "forward launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;
 }

@@ -67,7 +67,11 @@ struct FwdLayout {
   static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
   static constexpr int kOffX = kOffV + kStagesV * kTileBytes;  // row-max exchange [2 parity][2 halves][128]
   static constexpr int kOffL = kOffX + 2 * 2 * kTile * 4;      // final row-sum exchange [2 parity][2 halves][128]
-  static constexpr int kOffBar = kOffL + 2 * 2 * kTile * 4;
+  // d = 64: two 128 x 64 bf16 tiles (128-byte swizzle) in which a unit's
+  // output is staged for one TMA store; d = 128 has no room and stores rows
+  static constexpr int kStageBufs = D == 64 ? 2 : 0;
+  static constexpr int kOffStage = kOffL + 2 * 2 * kTile * 4;
+  static constexpr int kOffBar = kOffStage + kStageBufs * kTileBytes;
   static constexpr int kSBufs = 3;
   // d = 64: the two softmax warpgroups keep separate statistics for their key
   // halves and P V accumulates each half in its own O (TMEM has room for two
@@ -77,7 +81,7 @@ struct FwdLayout {
   static constexpr int kThreads = kSplit ? 416 : 384;  // warp 12: second P V issuer
   // q_full[2], q_empty[2], k_full[], k_empty[], v_full[], v_empty[], s_full[3], s_free[3],
   // p_full[2][3], pv_done[2][2], xchg, o_final, o_free, drain
-  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 4 * kSBufs + 4 + 4;
+  static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 4 * kSBufs + 4 + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
@@ -94,7 +98,7 @@ constexpr float kRescaleSlack = 8.f;  // P values stay below 2^8 between rescale
 template <int D, bool PAGED>
 __global__ void __launch_bounds__(FwdLayout<D>::kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using Lay = FwdLayout<D>;
   constexpr int NK = Lay::kStagesK, NV = Lay::kStagesV;
 
@@ -157,6 +161,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint8_t* sV = smem + Lay::kOffV;
   float* xmax = reinterpret_cast<float*>(smem + Lay::kOffX);
   float* xsum = reinterpret_cast<float*>(smem + Lay::kOffL);
+  uint8_t* sStage = smem + Lay::kOffStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* q_empty = q_full + 2;
@@ -173,6 +178,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* o_final = xchg + 1;
   uint64_t* o_free = o_final + 1;
   uint64_t* drain = o_free + 1;
+  uint64_t* stage_full = drain + 1;  // every softmax thread has written its rows of a staged tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
 
@@ -195,6 +201,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(o_final, npv);
     mbar_init(o_free, 256);
     mbar_init(drain, npv + 1);
+    mbar_init(stage_full, 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -440,10 +447,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     int g = 0, uc = 0, xp = 0;  // score tiles, units and exchange phases so far
+    int nst = 0;  // units whose output went through a staging tile
+    const bool store_issuer = warp == 4 && lane == 0;
     bool ok = true;
-    for (int k = 0, u = unit_of(0); u < n_units && ok; u = unit_of(++k)) {
-      Unit w;
-      if (!unit_at(u, w)) continue;
+    int k = 0, u = unit_of(0);
+    Unit w;
+    for (; u < n_units; u = unit_of(++k))
+      if (unit_at(u, w)) break;
+    while (u < n_units && ok) {
       const int qpos = w.q0 + r;
       float m = -INFINITY, l = 0.f;  // reference max (log2 units) and this half's row sum against it
       for (int j = 0; j < w.nkv; ++j, ++g) {
@@ -533,8 +544,21 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_arrive(p_full + (Lay::kSplit ? half * NB : 0) + b);
       }
       if (!ok) break;
-      // ---- epilogue of this unit
+      // ---- epilogue of this unit.  The next unit is looked up first, while
+      // the last P V of this one completes.
+      Unit wn;
+      int kn = k + 1, un = unit_of(kn);
+      for (; un < n_units; un = unit_of(++kn))
+        if (unit_at(un, wn)) break;
+      // d = 64, whole tile (no row of another sequence in it): the output
+      // goes through a staging tile and one TMA store.  Staging buffer
+      // nst % 2 was last stored two staged units ago; the issuing thread
+      // checks that store has read it before the exchange below, which every
+      // softmax thread passes before writing.
+      const bool staged = Lay::kStageBufs > 0 && w.q0 + kTile <= w.L && w.seq0 + w.q0 + kTile <= p.T;
+      if (staged && store_issuer && nst >= 2) bulk_wait_group_read1();
       if (!(ok = mbar_wait(o_final, uc & 1, abort_flag))) break;
+      const int sb = nst & 1;
       ++uc;
       // combine the two halves' row sums (split: and reference maxima)
       xsum[(xp & 1) * kTile * 2 + half * kTile + r] = l;
@@ -591,15 +615,39 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int t = 0; t < 16; ++t)
           pk[t] = pack_bf16x2(__uint_as_float(ov[32 * cc + 2 * t]) * inv_l, __uint_as_float(ov[32 * cc + 2 * t + 1]) * inv_l);
-        if (row_ok) {
+        if (Lay::kStageBufs > 0 && staged) {
+          // row r of the 128-byte-swizzled tile: this half's four 16-byte units
+          uint8_t* srow = sStage + sb * Lay::kTileBytes + r * 128;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int unit16 = half * 4 + t;
+            *reinterpret_cast<uint4*>(srow + ((unit16 ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+          }
+        } else if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
           for (int t = 0; t < 4; ++t) dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
         }
       }
+      if (Lay::kStageBufs > 0 && staged) {
+        fence_proxy_async_smem();
+        mbar_arrive(stage_full);
+        if (store_issuer) {
+          if (!(ok = mbar_wait(stage_full, nst & 1, abort_flag))) break;
+          tma_store_3d(&tm_o, sStage + sb * Lay::kTileBytes, 0, w.h, static_cast<int>(w.seq0 + w.q0));
+          bulk_commit_group();
+        }
+        ++nst;
+      }
       if (row_ok && half == 0)
         p.lse[static_cast<long long>(w.h) * p.T + tok] = lt > 0.f ? (m + lg2_approx(lt)) * kLn2 : -INFINITY;
+      w = wn;
+      k = kn;
+      u = un;
     }
+    // every staged output tile has been written before the CTA exits
+    if (store_issuer) bulk_wait_group0();
     if (!ok) give_up();
   }
 
@@ -672,8 +720,8 @@ static int simulate_group_pairs(const FwdParams& p, int G, int d) {
 
 // Host-side launch for one head dimension; returns a cudaError_t value.
 template <int D, bool PAGED>
-int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                 cudaStream_t stream) {
+int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                 const FwdParams& p, cudaStream_t stream) {
   using Lay = FwdLayout<D>;
   cudaError_t e =
       cudaFuncSetAttribute(fa_fwd_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
@@ -685,15 +733,17 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   const int grid = static_cast<int>(units < sms ? units : sms);  // one CTA per SM, persistent
   FwdParams q = p;
   q.group_pairs = choose_group_pairs(p, grid, D);
-  fa_fwd_kernel<D, PAGED><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tq, tk, tv, q);
+  fa_fwd_kernel<D, PAGED><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tq, tk, tv, to, q);
   return cudaGetLastError();
 }
 
-int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-               cudaStream_t stream) {
+int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+               const FwdParams& p, cudaStream_t stream) {
   if (p.block_table != nullptr)
-    return d == 64 ? launch_fwd_d<64, true>(tq, tk, tv, p, stream) : launch_fwd_d<128, true>(tq, tk, tv, p, stream);
-  return d == 64 ? launch_fwd_d<64, false>(tq, tk, tv, p, stream) : launch_fwd_d<128, false>(tq, tk, tv, p, stream);
+    return d == 64 ? launch_fwd_d<64, true>(tq, tk, tv, to, p, stream)
+                   : launch_fwd_d<128, true>(tq, tk, tv, to, p, stream);
+  return d == 64 ? launch_fwd_d<64, false>(tq, tk, tv, to, p, stream)
+                 : launch_fwd_d<128, false>(tq, tk, tv, to, p, stream);
 }
 
 }  // namespace fa
