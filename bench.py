@@ -377,7 +377,8 @@ def bench_ours(args, world, rank, local):
 # the pages' protocol: 20 warm-ups, then timed runs (at least 50, and enough
 # for a few clock samples), L2 flushed before each, median and P90.
 PER_CONFIG = ("fwd_b1_h1_n256_d64", "fwd_b4_h16_n2048_d64", "fwd_b2_h32_n4096_d128_causal",
-              "fwd_varlen8_hq32_hkv8_d128_causal", "decode_b64_hq64_hkv8_n4096_d128")
+              "fwd_varlen8_hq32_hkv8_d128_causal", "decode_b64_hq64_hkv8_n4096_d128",
+              "decode_b64_hq64_hkv8_n4096_d64", "decode_varlen8_hq32_hkv8_d128")
 
 
 def per_config_lines(args, rank, dev, stream, flush, peaks):

@@ -466,11 +466,16 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
     return fail(FA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
   DeviceState* dev = nullptr;
   if ((rc = device_state(&dev))) return rc;
+  // d = 64 with an even number of K/V heads and at most 8 query heads per K/V
+  // head: adjacent K/V heads are paired, [T, Hkv, 64] read as [T, Hkv / 2, 128],
+  // and the 128-row tensor-core kernel runs on the pairs
+  const bool pair = !fp8 && d == 64 && Hkv % 2 == 0 && Hq / Hkv <= 8;
+  const int Hmap = pair ? Hkv / 2 : Hkv, dmap = pair ? 128 : d;
   CUtensorMap tk, tv;
   const int box = paged ? pg.page_size : fa::kTile;
   if (fp8) {
     if ((rc = make_map_u8(&tk, k, T, Hkv, d, "k", box)) || (rc = make_map_u8(&tv, v, T, Hkv, d, "v", box))) return rc;
-  } else if ((rc = make_map(&tk, k, T, Hkv, d, "k", box)) || (rc = make_map(&tv, v, T, Hkv, d, "v", box))) {
+  } else if ((rc = make_map(&tk, k, T, Hmap, dmap, "k", box)) || (rc = make_map(&tv, v, T, Hmap, dmap, "v", box))) {
     return rc;
   }
   fa::DecodeParams p{};
@@ -492,7 +497,12 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   p.Hkv = Hkv;
   p.N = N;
   p.group = Hq / Hkv;
-  p.split_tiles = decode_split_tiles(B, Hkv, s.n_tiles, T, !paged && cu_seqlens_k != nullptr, dev->sms);
+  if (pair) {
+    p.pair = 1;
+    p.Hkv = Hkv / 2;
+    p.group = 2 * (Hq / Hkv);
+  }
+  p.split_tiles = decode_split_tiles(B, p.Hkv, s.n_tiles, T, !paged && cu_seqlens_k != nullptr, dev->sms);
   p.n_splits = (s.n_tiles + p.split_tiles - 1) / p.split_tiles;
   p.sms = dev->sms;
   const size_t rows = static_cast<size_t>(B) * Hq * p.n_splits;

@@ -108,6 +108,10 @@ struct DecodeParams {
   int split_tiles;    // 128-key tiles per split
   int sms;            // multiprocessors: CTAs of the persistent decode kernel
   float scale_log2;   // scale * log2(e)
+  // 1: head dimension 64 run by the 128-row tensor-core kernel on pairs of
+  // adjacent K/V heads (Hkv and group above are then per pair: Hkv / 2 pairs,
+  // 2 x the GQA group of query heads per pair); 0 otherwise
+  int pair;
 };
 
 }  // namespace fa

@@ -855,13 +855,17 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       for (int t = 0; t < (FP8 ? Lay::kPTerms : 1); ++t) tmem_st_cols<HW>(tmem_addr(tO, lane_base, t * H + h0), ov + t * HW);
     };
     // An item's query: thread r holds dims 16 (r % 8) .. +15 of head r / 8
-    // (two 16-byte units; 0 past the group), fetched an item ahead.
+    // (two 16-byte units; 0 past the group), fetched an item ahead.  Pairs of
+    // 64-dim K/V heads: a query head of the first K/V head of the pair holds
+    // its 64 dims in dims 0..63 and zeros above, one of the second head in
+    // 64..127 and zeros below, so each score reads only its own head's key.
     auto fetch_q = [&](const DecItem& it, uint4 (&qa)[2]) {
-      const int h = r / 8;
-      if (h < group && (FP8 || wg == 0)) {
+      const int h = r / 8, sub = r % 8;
+      const bool live = h < group && (FP8 || wg == 0) && (!p.pair || (sub >= 4) == (2 * h >= group));
+      if (live) {
+        const long long qrow = static_cast<long long>(it.b) * p.Hq + it.g * group + h;
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                          (static_cast<long long>(it.b) * p.Hq + it.g * group + h) * D +
-                                                          16 * (r % 8));
+                                                          (p.pair ? qrow * 64 + 16 * (sub & 3) : qrow * D + 16 * sub));
         qa[0] = __ldg(src);
         qa[1] = __ldg(src + 1);
       } else {
@@ -1142,7 +1146,13 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const int hh = h0 + h;
         if (hh < group) {
           const float l = sRedW[h] + sRedW[H + h] + sRedW[2 * H + h] + sRedW[3 * H + h];
-          p.o_part[((row0 + hh) * p.n_splits + it.split) * D + r] = osum[h] / l;
+          if (!p.pair) {
+            p.o_part[((row0 + hh) * p.n_splits + it.split) * D + r] = osum[h] / l;
+          } else if ((r >= 64) == (2 * hh >= group)) {
+            // O^T rows of this query head's own K/V head; the other 64 rows
+            // mix in the other head's values and are dropped
+            p.o_part[((row0 + hh) * p.n_splits + it.split) * 64 + (r & 63)] = osum[h] / l;
+          }
           if (r == 0) p.lse_part[(row0 + hh) * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
         }
       }
@@ -1250,11 +1260,15 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(p.B) * p.Hq;
-  fa_decode_combine_kernel<128><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
+  if (p.pair)
+    fa_decode_combine_kernel<64><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
+  else
+    fa_decode_combine_kernel<128><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+  if (d == 64 && p.pair) return launch_decode_tc<false>(tk, tv, p, stream);
   if (d == 64) return launch_decode_d<64>(tk, tv, p, stream);
   if (d == 128) return launch_decode_tc<false>(tk, tv, p, stream);
   return -1;

@@ -104,6 +104,9 @@ WORKLOADS = {
     # step reads 1.07 GB of K/V cache.
     "decode_b64_hq64_hkv8_n4096_d128": Workload(
         "decode_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True),
+    # the same step at head dimension 64 (0.54 GB of cache)
+    "decode_b64_hq64_hkv8_n4096_d64": Workload(
+        "decode_b64_hq64_hkv8_n4096_d64", 64, 64, 8, 4096, 64, False, (), False, True),
     # the same step over an E4M3 cache (per-token scales)
     "decode_fp8_b64_hq64_hkv8_n4096_d128": Workload(
         "decode_fp8_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True, True),

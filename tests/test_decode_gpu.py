@@ -82,6 +82,28 @@ def test_decode_long_cache_many_splits(cuda_device, d):
     check(1, 4, 1, d, [20000], batched=True, seed=7)
 
 
+@pytest.mark.parametrize("heads", [(2, 2), (4, 2), (8, 4), (16, 2), (64, 8)])
+def test_decode_d64_head_pairs(cuda_device, heads):
+    """d = 64 with an even number of K/V heads and groups of 1-8: adjacent K/V
+    heads are paired and run on the tensor-core kernel (each query head's
+    scores and output come only from its own K/V head), ragged lengths."""
+    Hq, Hkv = heads
+    check(3, Hq, Hkv, 64, [1, 700, 129], seed=40 + Hq)
+
+
+@pytest.mark.parametrize("heads", [(3, 3), (32, 2), (9, 1)])
+def test_decode_d64_cuda_core_fallback(cuda_device, heads):
+    """d = 64 that cannot be paired (odd Hkv, or a group above 8): the
+    CUDA-core split kernel."""
+    Hq, Hkv = heads
+    check(2, Hq, Hkv, 64, [300, 1000], seed=50 + Hq)
+
+
+def test_decode_d64_many_items_per_cta(cuda_device):
+    lengths = [int(x) for x in np.random.default_rng(32).integers(0, 700, size=160)]
+    check(len(lengths), 8, 2, 64, lengths, seed=32)
+
+
 def test_decode_wide_scores_stay_finite(cuda_device):
     """Queries scaled by 8: nearly one-hot weights (see the forward's test for
     the bf16 rounding allowance on |O| of 4-5)."""
@@ -115,7 +137,8 @@ def test_decode_matches_last_row_of_the_forward(cuda_device):
     assert (l_d - l_f[:, last]).abs().max().item() <= 2e-3
 
 
-@pytest.mark.parametrize("name", ["decode_varlen8_hq32_hkv8_d128", "decode_b64_hq64_hkv8_n4096_d128"])
+@pytest.mark.parametrize("name", ["decode_varlen8_hq32_hkv8_d128", "decode_b64_hq64_hkv8_n4096_d128",
+                                  "decode_b64_hq64_hkv8_n4096_d64"])
 def test_decode_workload(cuda_device, name):
     """Full-size decoding workloads; the 64-sequence one is checked on three
     whole sequences (every head) against the oracle, the packed one in full."""
