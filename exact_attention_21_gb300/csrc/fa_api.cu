@@ -454,7 +454,9 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   int rc = check_shape(B, Hq, Hkv, N, d, T, scale, 0, paged ? pg.seqlens : cu_seqlens_k, &s);
   if (rc) return rc;
   if (Hq / Hkv > 16) return fail(FA_ERR_UNSUPPORTED, "decode supports up to 16 query heads per K/V head");
-  if (fp8 && d != 128) return fail(FA_ERR_UNSUPPORTED, "the E4M3 cache is supported for d = 128");
+  if (fp8 && d != 128 && !(d == 64 && Hkv % 2 == 0 && Hq / Hkv <= 8))
+    return fail(FA_ERR_UNSUPPORTED,
+                "the E4M3 cache is supported for d = 128, and for d = 64 with an even Hkv and Hq / Hkv <= 8");
   if (!q || !k || !v || !o || !lse || !workspace || (fp8 && !v_scale)) return fail(FA_ERR_INVALID_ARG, "null pointer");
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
     return fail(FA_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned");
@@ -469,12 +471,13 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   // d = 64 with an even number of K/V heads and at most 8 query heads per K/V
   // head: adjacent K/V heads are paired, [T, Hkv, 64] read as [T, Hkv / 2, 128],
   // and the 128-row tensor-core kernel runs on the pairs
-  const bool pair = !fp8 && d == 64 && Hkv % 2 == 0 && Hq / Hkv <= 8;
+  const bool pair = d == 64 && Hkv % 2 == 0 && Hq / Hkv <= 8;
   const int Hmap = pair ? Hkv / 2 : Hkv, dmap = pair ? 128 : d;
   CUtensorMap tk, tv;
   const int box = paged ? pg.page_size : fa::kTile;
   if (fp8) {
-    if ((rc = make_map_u8(&tk, k, T, Hkv, d, "k", box)) || (rc = make_map_u8(&tv, v, T, Hkv, d, "v", box))) return rc;
+    if ((rc = make_map_u8(&tk, k, T, Hmap, dmap, "k", box)) || (rc = make_map_u8(&tv, v, T, Hmap, dmap, "v", box)))
+      return rc;
   } else if ((rc = make_map(&tk, k, T, Hmap, dmap, "k", box)) || (rc = make_map(&tv, v, T, Hmap, dmap, "v", box))) {
     return rc;
   }

@@ -856,14 +856,22 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     };
     // An item's query: thread r holds dims 16 (r % 8) .. +15 of head r / 8
     // (two 16-byte units; 0 past the group), fetched an item ahead.  Pairs of
-    // 64-dim K/V heads: a query head of the first K/V head of the pair holds
-    // its 64 dims in dims 0..63 and zeros above, one of the second head in
-    // 64..127 and zeros below, so each score reads only its own head's key.
+    // 64-dim K/V heads: softmax warpgroup j serves K/V head 2 g + j of pair g,
+    // its slot s (of HW) query head (2 g + j) G + s for s < G (G = group / 2);
+    // a query of the first head holds its 64 dims in dims 0..63 and zeros
+    // above, one of the second head in 64..127 and zeros below, so each score
+    // reads only its own head's key.
+    auto pair_qrow = [&](const DecItem& it, int slot) {  // -1: an unused slot
+      const int half = slot / HW, s2 = slot % HW, G = group / 2;
+      return half < 2 && s2 < G ? static_cast<long long>(it.b) * p.Hq + static_cast<long long>(2 * it.g + half) * G + s2
+                                : -1ll;
+    };
     auto fetch_q = [&](const DecItem& it, uint4 (&qa)[2]) {
       const int h = r / 8, sub = r % 8;
-      const bool live = h < group && (FP8 || wg == 0) && (!p.pair || (sub >= 4) == (2 * h >= group));
+      const long long qrow =
+          p.pair ? pair_qrow(it, h) : (h < group ? static_cast<long long>(it.b) * p.Hq + it.g * group + h : -1ll);
+      const bool live = qrow >= 0 && (FP8 || wg == 0) && (!p.pair || (sub >= 4) == (h >= HW));
       if (live) {
-        const long long qrow = static_cast<long long>(it.b) * p.Hq + it.g * group + h;
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
                                                           (p.pair ? qrow * 64 + 16 * (sub & 3) : qrow * D + 16 * sub));
         qa[0] = __ldg(src);
@@ -881,13 +889,18 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // time.  One copy group per tile, empty or not; bit j of pf: slot j holds
     // copies.
     constexpr int kAhead = Lay::kScaleAhead;
+    // index of the per-token scales of key kpos for this warpgroup's K/V head
+    auto scale_index = [&](const DecItem& t, int kpos) {
+      const long long row = decode_row(p, t.b, t.seq0, kpos, t.L);
+      return p.pair ? row * (2 * p.Hkv) + 2 * t.g + wg : row * p.Hkv + t.g;
+    };
     float2* sScale = reinterpret_cast<float2*>(smem + Lay::kOffScale) + wg * kAhead * kTile;
     uint32_t pf = 0;
     auto issue_scales = [&](const DecItem& t, int i, uint32_t slot) {
       pf &= ~(1u << slot);
       const int kpos = (t.t0 + i) * kTile + r;
       if (i < t.nt && kpos < t.L) {
-        const long long si = decode_row(p, t.b, t.seq0, kpos, t.L) * p.Hkv + t.g;
+        const long long si = scale_index(t, kpos);
         cp_async_4(&sScale[slot * kTile + r].x, p.k_scale + si);
         cp_async_4(&sScale[slot * kTile + r].y, p.v_scale + si);
         pf |= 1u << slot;
@@ -942,7 +955,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
               sk = s2.x;
               sv = s2.y;
             } else {  // a tile the ring did not reach (items shorter than the ring)
-              const long long si = decode_row(p, it.b, it.seq0, kpos, it.L) * p.Hkv + it.g;
+              const long long si = scale_index(it, kpos);
               sk = __ldg(p.k_scale + si);
               sv = __ldg(p.v_scale + si);
             }
@@ -1144,16 +1157,17 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll
       for (int h = 0; h < HW; ++h) {
         const int hh = h0 + h;
-        if (hh < group) {
+        if (p.pair || hh < group) {
           const float l = sRedW[h] + sRedW[H + h] + sRedW[2 * H + h] + sRedW[3 * H + h];
           if (!p.pair) {
             p.o_part[((row0 + hh) * p.n_splits + it.split) * D + r] = osum[h] / l;
-          } else if ((r >= 64) == (2 * hh >= group)) {
-            // O^T rows of this query head's own K/V head; the other 64 rows
-            // mix in the other head's values and are dropped
-            p.o_part[((row0 + hh) * p.n_splits + it.split) * 64 + (r & 63)] = osum[h] / l;
+            if (r == 0) p.lse_part[(row0 + hh) * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
+          } else if (const long long qr = pair_qrow(it, hh); qr >= 0) {
+            // O^T rows of this warpgroup's own K/V head; the other 64 rows mix
+            // in the other head's values and are dropped
+            if ((r >= 64) == (wg == 1)) p.o_part[(qr * p.n_splits + it.split) * 64 + (r & 63)] = osum[h] / l;
+            if (r == 0) p.lse_part[qr * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
           }
-          if (r == 0) p.lse_part[(row0 + hh) * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
         }
       }
       // O^T buffer kq & 1 read: P V of item kq + 2 may write it
@@ -1276,7 +1290,7 @@ int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const Dec
 
 int launch_decode_fp8(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                       cudaStream_t stream) {
-  if (d == 128) return launch_decode_tc<true>(tk, tv, p, stream);
+  if (d == 128 || (d == 64 && p.pair)) return launch_decode_tc<true>(tk, tv, p, stream);
   return -1;
 }
 

@@ -110,6 +110,9 @@ WORKLOADS = {
     # the same step over an E4M3 cache (per-token scales)
     "decode_fp8_b64_hq64_hkv8_n4096_d128": Workload(
         "decode_fp8_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True, True),
+    # the d = 64 step over an E4M3 cache
+    "decode_fp8_b64_hq64_hkv8_n4096_d64": Workload(
+        "decode_fp8_b64_hq64_hkv8_n4096_d64", 64, 64, 8, 4096, 64, False, (), False, True, True),
     # the same step with the cache in 16-token pages scattered over a pool
     "decode_paged16_b64_hq64_hkv8_n4096_d128": Workload(
         "decode_paged16_b64_hq64_hkv8_n4096_d128", 64, 64, 8, 4096, 128, False, (), False, True, False, 16),

@@ -258,7 +258,9 @@ int fa_kv_quantize_fp8(const void* x, void* x8, float* scale, long long rows, in
  *
  *   k8, v8    [T, Hkv, d] E4M3 codes, 16-byte aligned                 (in)
  *   k_scale, v_scale  [T, Hkv] f32 per-token scales, 4-byte aligned   (in)
- *   Other arguments as for fa_decode; d must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ *   Other arguments as for fa_decode.  d = 128; or d = 64 with an even Hkv
+ *   and Hq / Hkv <= 8 (two adjacent K/V heads then form one 128-byte row of
+ *   the cache); FA_ERR_UNSUPPORTED otherwise.
  */
 int fa_decode_fp8(const void* q, const void* k8, const void* v8, const float* k_scale, const float* v_scale,
                   void* o, float* lse, int B, int Hq, int Hkv, int N, int d, long long T, float scale,
@@ -290,7 +292,7 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
 /*
  * fa_decode_paged over an E4M3 page pool (codes from fa_kv_quantize_fp8 and
  * f32 per-token scales k_scale, v_scale [num_pages * page_size, Hkv], laid
- * out like the pool).  d must be 128.
+ * out like the pool).  Head dimensions as for fa_decode_fp8.
  */
 int fa_decode_paged_fp8(const void* q, const void* k8_pages, const void* v8_pages, const float* k_scale,
                         const float* v_scale, const int* block_table, const int* seqlens, void* o, float* lse, int B,

@@ -79,12 +79,35 @@ def assert_fp8_close(o, lse, o_ref, lse_ref):
     return err.max(), err.mean()
 
 
-def check(B, Hq, Hkv, lengths, batched=False, seed=0):
+def check(B, Hq, Hkv, lengths, batched=False, seed=0, d=128):
     T = int(sum(lengths))
-    t = make_decode_qkv(B, Hq, T, Hkv, 128, seed=seed)
+    t = make_decode_qkv(B, Hq, T, Hkv, d, seed=seed)
     o, lse = run_decode_fp8(t, lengths=None if batched else lengths, N=lengths[0] if batched else None)
-    o_ref, lse_ref = oracle_decode_fp8(t, oracle.cu_from_lengths(lengths), 128 ** -0.5)
+    o_ref, lse_ref = oracle_decode_fp8(t, oracle.cu_from_lengths(lengths), d ** -0.5)
     return assert_fp8_close(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("heads", [(2, 2), (4, 2), (16, 2), (64, 8)])
+@pytest.mark.parametrize("N", [1, 129, 1000])
+def test_decode_fp8_d64_head_pairs(cuda_device, heads, N):
+    """d = 64 over an E4M3 cache: adjacent K/V heads paired into 128-byte rows,
+    each softmax warpgroup using its own head's per-token scales."""
+    check(3, heads[0], heads[1], [N] * 3, batched=True, seed=N + heads[0], d=64)
+
+
+def test_decode_fp8_d64_packed_ragged_and_many_items(cuda_device):
+    check(9, 8, 2, [5, 1, 300, 128, 129, 0, 640, 77, 2000], seed=6, d=64)
+    lengths = [int(x) for x in np.random.default_rng(33).integers(0, 700, size=160)]
+    check(len(lengths), 8, 2, lengths, seed=33, d=64)
+
+
+def test_decode_fp8_d64_unpaired_is_unsupported(cuda_device):
+    """Odd Hkv (or a group above 8) at d = 64: no E4M3 kernel, a clear error."""
+    fa = fa_module()
+    t = make_decode_qkv(2, 3, 200, 3, 64, seed=8)
+    with pytest.raises(fa.FAError) as e:
+        run_decode_fp8(t, lengths=[100, 100])
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("N", [1, 129, 1000])

@@ -60,12 +60,13 @@ def test_paged_decode(cuda_device, d, page):
     assert_fwd_close(o, lse, o_ref, lse_ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("page", [16, 128])
-def test_paged_decode_fp8(cuda_device, page):
+def test_paged_decode_fp8(cuda_device, page, d):
     lengths = [5, 1, 300, 129, 0, 640, 2000]
-    q, kp, vp, table = paged_case(lengths, 32, 4, 128, page, seed=page)
+    q, kp, vp, table = paged_case(lengths, 32, 4, d, page, seed=page + d)
     o, lse = run(q, kp, vp, table, lengths, page, fp8=True)
-    o_ref, lse_ref = oracle_paged(q, kp, vp, table, lengths, page, 128, fp8=True)
+    o_ref, lse_ref = oracle_paged(q, kp, vp, table, lengths, page, d, fp8=True)
     err = np.abs(o - o_ref)
     assert np.isfinite(o).all() and err.max() <= FWD_MAX_ABS
     assert err.mean() <= FWD_MEAN_ABS + 2.0 ** -9 * np.abs(o_ref).mean()
