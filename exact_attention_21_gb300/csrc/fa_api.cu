@@ -213,6 +213,26 @@ int check_shape(int B, int Hq, int Hkv, int N, int d, long long T, float scale, 
 // each CTA costs its tiles plus about one tile of start-up (barrier set-up and
 // the latency of its first loads).  Picks the split length with the lowest
 // modelled time; packed caches are modelled as sequences of the mean length.
+// Packed caches numbered compactly (every item exists and the CTAs take
+// consecutive ones): the split length with the smallest modelled time of the
+// busiest CTA, ceil(items / SMs) items of the split's tiles plus about half a
+// tile each, where the items are estimated from the total cached tokens T
+// (each sequence's last tile and last split counted as half on average).
+int decode_split_tiles_compact(int B, int Hkv, int max_tiles, long long T, int sms) {
+  const double tiles = static_cast<double>(T) / fa::kTile + 0.5 * B;
+  int best = 1;
+  double best_time = 0.0;
+  for (int st = 1; st <= std::max(max_tiles, 1); ++st) {
+    const double items = Hkv * (tiles / st + 0.5 * B);
+    const double time = std::ceil(items / sms) * (std::min<double>(st, tiles / B) + 0.5);
+    if (st == 1 || time < best_time) {
+      best = st;
+      best_time = time;
+    }
+  }
+  return best;
+}
+
 int decode_split_tiles(int B, int Hkv, int max_tiles, long long T, bool packed, int sms) {
   const double mean_tiles =
       packed ? std::max(1.0, static_cast<double>(T) / B / fa::kTile) : static_cast<double>(max_tiles);
@@ -505,7 +525,12 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
     p.Hkv = Hkv / 2;
     p.group = 2 * (Hq / Hkv);
   }
-  p.split_tiles = decode_split_tiles(B, p.Hkv, s.n_tiles, T, !paged && cu_seqlens_k != nullptr, dev->sms);
+  // packed caches of up to the kernel's prefix size: compact item numbering
+  const bool packed = !paged && cu_seqlens_k != nullptr;
+  const bool tc = d == 128 || pair;
+  p.compact = (tc && packed && B <= (fp8 ? 192 : 1024)) ? 1 : 0;
+  p.split_tiles = p.compact ? decode_split_tiles_compact(B, p.Hkv, s.n_tiles, T, dev->sms)
+                            : decode_split_tiles(B, p.Hkv, s.n_tiles, T, packed, dev->sms);
   p.n_splits = (s.n_tiles + p.split_tiles - 1) / p.split_tiles;
   p.sms = dev->sms;
   const size_t rows = static_cast<size_t>(B) * Hq * p.n_splits;

@@ -112,6 +112,10 @@ struct DecodeParams {
   // adjacent K/V heads (Hkv and group above are then per pair: Hkv / 2 pairs,
   // 2 x the GQA group of query heads per pair); 0 otherwise
   int pair;
+  // 1: the (split, K/V head, sequence) items are numbered compactly through a
+  // prefix of each sequence's split count, built in shared memory at kernel
+  // start (packed caches of unequal length); 0: split-major over n_splits
+  int compact;
 };
 
 }  // namespace fa

@@ -478,7 +478,10 @@ struct DecTcLayout {
   // full[], empty[], q_ready, s_full[3], p_ready[3], pv_done[2], drain, o_free[2]
   static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16 + 1024;
+  // compact item numbering: split-count prefix of up to kPrefixMaxB sequences
+  static constexpr int kPrefixMaxB = FP8 ? 192 : 1024;
+  static constexpr int kOffPrefix = kOffMisc + 16;
+  static constexpr int kBytes = kOffPrefix + (kPrefixMaxB + 1) * 4 + 1024;
   // warp 0 loads, warp 1 issues P V, warps 2-5 and 7-10 run the softmax
   // (two warpgroups, half of the heads each) and warp 6 issues S^T: a single
   // thread issuing both products would start one of these narrow MMAs only
@@ -537,7 +540,28 @@ struct DecItem {
   long long seq0;
   int split, g, b, L, t0, nt;
 };
-__device__ __forceinline__ bool decode_item(const DecodeParams& p, long long w, DecItem& it) {
+// Compact numbering (prefix != null): item w is K/V head w % Hkv of the
+// (w / Hkv)-th (sequence, split) pair, sequence-major; prefix[b] counts the
+// splits of the sequences before b (prefix[B]: all of them), so every item
+// exists and consecutive CTAs take consecutive items.
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, const int* prefix, long long w, DecItem& it) {
+  if (prefix != nullptr) {
+    const int j = static_cast<int>(w / p.Hkv);
+    it.g = static_cast<int>(w % p.Hkv);
+    int lo = 0, hi = p.B;  // prefix[lo] <= j < prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= j) lo = mid; else hi = mid;
+    }
+    it.b = lo;
+    it.split = j - prefix[lo];
+    if (!decode_bounds(p, it.b, it.seq0, it.L)) return false;
+    const int seq_tiles = (it.L + kTile - 1) / kTile;
+    it.t0 = it.split * p.split_tiles;
+    if (it.t0 >= seq_tiles) return false;
+    it.nt = min(p.split_tiles, seq_tiles - it.t0);
+    return true;
+  }
   const long long heads = static_cast<long long>(p.B) * p.Hkv;
   it.split = static_cast<int>(w / heads);
   const long long rest = w % heads;
@@ -552,9 +576,10 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, long long w, 
 }
 // This CTA's first item at or after w (its items are blockIdx.x + j gridDim.x)
 // that has work, or n_items.
-__device__ __forceinline__ long long next_item(const DecodeParams& p, long long w, long long n_items, DecItem& it) {
+__device__ __forceinline__ long long next_item(const DecodeParams& p, const int* prefix, long long w, long long n_items,
+                                               DecItem& it) {
   for (; w < n_items; w += gridDim.x)
-    if (decode_item(p, w, it)) return w;
+    if (decode_item(p, prefix, w, it)) return w;
   return n_items;
 }
 
@@ -644,7 +669,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   // persistent: the CTA runs its items back to back; the barrier rings and
   // the S^T / P^T / V buffers run on a tile count over all of them (gt), so
   // the loads and S^T of an item overlap the previous item's epilogue
-  const long long n_items = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
+  long long n_items = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -661,6 +686,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint64_t* o_free = drain + 1;      // O^T buffer j read by the epilogue of an item
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
+  int* sPre = p.compact ? reinterpret_cast<int*>(smem + Lay::kOffPrefix) : nullptr;
   auto stage = [&](uint32_t st) { return smem + st * Lay::kStageBytes; };
   auto pbuf = [&](uint32_t i) { return smem + Lay::kOffP + (i & 1) * Lay::kPBytes; };
   // the K and V tiles of tile i (E4M3 for an FP8 cache)
@@ -690,10 +716,31 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     tmem_alloc(tmem_slot, Lay::kTmemCols);
     tmem_relinquish();
   }
+  if (sPre != nullptr && warp == 2) {
+    // split counts of the sequences, scanned 32 at a time (exclusive prefix)
+    int run = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      int ns = 0;
+      long long s0;
+      int L;
+      if (b < p.B && decode_bounds(p, b, s0, L)) ns = ((L + kTile - 1) / kTile + p.split_tiles - 1) / p.split_tiles;
+      int x = ns;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (b < p.B) sPre[b] = run + x - ns;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) sPre[p.B] = run;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (sPre != nullptr) n_items = static_cast<long long>(sPre[p.B]) * p.Hkv;
   auto give_up = [&]() {
     atomicOr(p.status, kStatusTimeout);
     *abort_flag = 1;
@@ -708,8 +755,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     uint32_t gt = 0;  // tiles issued
     bool ok = true;
     DecItem it;
-    for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
-         w = next_item(p, w + gridDim.x, n_items, it)) {
+    for (long long w = next_item(p, sPre, blockIdx.x, n_items, it); w < n_items && ok;
+         w = next_item(p, sPre, w + gridDim.x, n_items, it)) {
       for (int i = 0; i < it.nt; ++i, ++gt) {
         const uint32_t st = gt % NS;
         // lane 0 waits for the stage and posts the byte count before any copy
@@ -739,8 +786,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       bool ok = true;
       uint32_t gt = 0, kq = 0;  // tiles and items so far
       DecItem it;
-      for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
-           w = next_item(p, w + gridDim.x, n_items, it), ++kq) {
+      for (long long w = next_item(p, sPre, blockIdx.x, n_items, it); w < n_items && ok;
+           w = next_item(p, sPre, w + gridDim.x, n_items, it), ++kq) {
         // O^T buffer kq & 1 was last read by the epilogue of item kq - 2
         if (kq >= 2 && !(ok = mbar_wait(o_free + (kq & 1), ((kq - 2) >> 1) & 1, abort_flag))) break;
         const uint32_t tO = tmem + Lay::kColO + (kq & 1) * Lay::kOCols;
@@ -780,8 +827,8 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       bool ok = true;
       uint32_t gt = 0, kq = 0;  // tiles and items so far
       DecItem it;
-      for (long long w = next_item(p, blockIdx.x, n_items, it); w < n_items && ok;
-           w = next_item(p, w + gridDim.x, n_items, it), ++kq) {
+      for (long long w = next_item(p, sPre, blockIdx.x, n_items, it); w < n_items && ok;
+           w = next_item(p, sPre, w + gridDim.x, n_items, it), ++kq) {
         // the item's query, in buffer kq & 1
         if (!(ok = mbar_wait(q_ready, kq & 1, abort_flag))) break;
         const uint32_t sQa = smem_u32(sQ + (kq & 1) * Lay::kQBytes);
@@ -914,7 +961,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     bool ok = true;
     uint32_t gt = 0, kq = 0;  // tiles and items so far
     DecItem it;
-    long long w = next_item(p, blockIdx.x, n_items, it);
+    long long w = next_item(p, sPre, blockIdx.x, n_items, it);
     if (w < n_items) {
       uint4 qa[2];
       fetch_q(it, qa);
@@ -931,7 +978,7 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       // the next item's query: fetched now, stored once this item's first tile
       // is done, so that S^T can run into the next item ahead of the softmax
       DecItem nx;
-      const long long w2 = next_item(p, w + gridDim.x, n_items, nx);
+      const long long w2 = next_item(p, sPre, w + gridDim.x, n_items, nx);
       uint4 qn[2] = {};
       if (w2 < n_items) fetch_q(nx, qn);
       const uint32_t tO = tmem + Lay::kColO + (kq & 1) * Lay::kOCols;

@@ -62,6 +62,14 @@ def test_decode_many_items_per_cta(cuda_device, heads):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_decode_more_sequences_than_the_compact_table(cuda_device, d):
+    """1100 packed caches (above the 1024 sequences whose split counts the
+    kernel numbers compactly): the split-major numbering, with empty caches."""
+    lengths = [int(x) for x in np.random.default_rng(34).integers(0, 300, size=1100)]
+    check(len(lengths), 4, 2, d, lengths, seed=34)
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_decode_packed_ragged_with_empty_caches(cuda_device, d):
     lengths = [5, 1, 300, 128, 129, 0, 640, 77, 2000]
     o_err = check(len(lengths), 8, 2, d, lengths, seed=5)
