@@ -671,6 +671,10 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   // the loads and S^T of an item overlap the previous item's epilogue
   long long n_items = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
 
+  // the combine kernel, launched as a programmatic dependent, may be scheduled
+  // now: it waits for this whole grid before reading the partial results
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + Lay::kOffQ;
@@ -1239,6 +1243,10 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 // Merges the splits of one (sequence, query head) row per warp.
 template <int D>
 __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
+  // launched as a programmatic dependent of the split kernel: resident early,
+  // it waits here until that grid has finished and its writes are visible (a
+  // no-op after an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int E = D / 32;  // dimensions per lane
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const long long row = static_cast<long long>(blockIdx.x) * 4 + warp;  // b * Hq + h
@@ -1320,12 +1328,21 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
   kern<<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // the combine as a programmatic dependent launch: its CTAs are scheduled
+  // while the split kernel runs and start merging as soon as it completes
   const long long rows = static_cast<long long>(p.B) * p.Hq;
-  if (p.pair)
-    fa_decode_combine_kernel<64><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
-  else
-    fa_decode_combine_kernel<128><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return p.pair ? cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<64>, p)
+                : cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<128>, p);
 }
 
 int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
