@@ -18,7 +18,8 @@ namespace fa {
 int launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                const FwdParams& p, cudaStream_t stream);
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, bool deterministic,
+               const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk, const CUtensorMap& tdv,
+               const BwdParams& p, bool deterministic,
                cudaStream_t stream);
 int launch_decode(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream);
 int launch_decode_fp8(int d, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
@@ -401,10 +402,11 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
   DeviceState* dev = nullptr;
   if ((rc = device_state(&dev))) return rc;
   void* dq_acc = static_cast<char*>(workspace) + (static_cast<size_t>(Hq) * T * 4 + 255) / 256 * 256;
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if ((rc = make_map(&tq, q, T, Hq, d, "q")) || (rc = make_map(&tk, k, T, Hkv, d, "k")) ||
       (rc = make_map(&tv, v, T, Hkv, d, "v")) || (rc = make_map(&tdo, dout, T, Hq, d, "dout")) ||
-      (rc = make_map_f32(&tdq, dq_acc, T, Hq, d, "dq accumulator")))
+      (rc = make_map_f32(&tdq, dq_acc, T, Hq, d, "dq accumulator")) || (rc = make_map(&tdk, dk, T, Hkv, d, "dk")) ||
+      (rc = make_map(&tdv, dv, T, Hkv, d, "dv")))
     return rc;
   fa::BwdParams p{};
   p.o = o;
@@ -433,7 +435,7 @@ static int bwd_common(const void* q, const void* k, const void* v, const void* o
     if (z != cudaSuccess) return fail(FA_ERR_LAUNCH, "zeroing tile_counts failed: %s", cudaGetErrorString(z));
     p.tile_count = reinterpret_cast<unsigned long long*>(tile_count);
   }
-  int e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, p, deterministic, static_cast<cudaStream_t>(stream));
+  int e = fa::launch_bwd(d, tq, tk, tv, tdo, tdq, tdk, tdv, p, deterministic, static_cast<cudaStream_t>(stream));
   if (e == -1) return fail(FA_ERR_UNSUPPORTED, "backward kernel unavailable for d = %d", d);
   if (e != cudaSuccess) return fail(FA_ERR_LAUNCH, "backward launch failed: %s", cudaGetErrorString((cudaError_t)e));
   return FA_OK;

@@ -81,8 +81,8 @@ struct BwdLayout {
   static constexpr int kStatBytes = 2 * kTile * 4;
   static constexpr int kOffBar = kOffStats + 2 * kStatBytes;
   // kv_full, qdo_full[], qdo_empty[], sdp_full[2], ps_ready[2], dp_free, dq_full[2], dq_free[2],
-  // dq_staged, ds_free[3], epi, drain, dk_hi[2], kv_free, acc_free
-  static constexpr int kNumBars = 1 + 2 * kStages + 20;
+  // dq_staged, ds_free[3], epi, drain, dk_hi[2], kv_free, acc_free, epi_staged, epi_read
+  static constexpr int kNumBars = 1 + 2 * kStages + 22;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // no room to round the dynamic shared memory base up to the 1 KB alignment
   // of the 128-byte swizzle: the kernel requires an aligned base (it is, with
@@ -105,7 +105,8 @@ template <int D, bool DQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+              const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+              const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using Lay = BwdLayout<D>;
   constexpr int NS = Lay::kStages;
   const bool causal = p.causal != 0;
@@ -168,6 +169,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* dk_hi = drain + 1;  // dk_hi[n & 1]: dK_n has read queries 64..127
   uint64_t* kv_free = dk_hi + 2;   // the unit's K / V tiles have been read by every product
   uint64_t* acc_free = kv_free + 1;  // the unit's dV / dK have been read out of TMEM
+  uint64_t* epi_staged = acc_free + 1;  // a whole tile's dV / dK staged in shared memory
+  uint64_t* epi_read = epi_staged + 1;  // and read by its bulk stores
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
 
@@ -199,6 +202,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(dk_hi + 1, 1);
     mbar_init(kv_free, 3);   // the three MMA threads, once per unit
     mbar_init(acc_free, 256);
+    mbar_init(epi_staged, 256);
+    mbar_init(epi_read, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -226,6 +231,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_dq);
+      tma_prefetch_desc(&tm_dk);
+      tma_prefetch_desc(&tm_dv);
     }
     int uses[NS] = {};
     bool ok = true;
@@ -436,7 +443,20 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     bool ok = true;
-    int n = 0, uc = 0;  // steps and units so far
+    int n = 0, uc = 0, ue = 0;  // steps, units and whole-tile stores so far
+    bool pending = false;       // the last whole-tile stores may still be reading their staging
+    // Wait until the stores of the last whole tile have read their staging
+    // (the thread that issued them waits for its bulk group, then lets the
+    // others go on).
+    auto staging_read = [&]() -> bool {
+      if (!pending) return true;
+      pending = false;
+      if (warp == 2 && lane == 0) {
+        bulk_wait_group_read0();
+        mbar_arrive(epi_read);
+      }
+      return __all_sync(0xffffffffu, mbar_wait(epi_read, (ue - 1) & 1, abort_flag));
+    };
     for (int k = 0, un = unit_of(0); un < n_units && ok; un = unit_of(++k)) {
     Unit w;
     if (!unit_at(un, w)) continue;
@@ -493,6 +513,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // warp stays together for the TMEM loads that follow).
         if (DQ && cl == 0 && n >= Lay::kDSBufs)
           ok = __all_sync(0xffffffffu, mbar_wait(ds_free + n % Lay::kDSBufs, (n / Lay::kDSBufs - 1) & 1, abort_flag));
+        if (DQ && cl == 0 && ok) ok = staging_read();
         // dS^T row r into the 128B-swizzled tile (query-contiguous rows; the
         // 16-byte unit u holds queries 8 u .. 8 u + 7 of this 64-query half).
 #pragma unroll
@@ -510,13 +531,55 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     if (ok) ok = mbar_wait(epi, uc & 1, abort_flag);
     if (!ok) break;
-    {
+    // first warpgroup stores dV, second dK (scaled)
+    const uint32_t col = half == 0 ? Lay::kColDV : Lay::kColDK;
+    const float mul = half == 0 ? 1.f : p.scale;
+    if (k0 + kTile <= L) {
+      // A whole tile: staged as a 128B-swizzled 128 x 64 bf16 box per
+      // warpgroup in the dS^T buffer of the next step (free once the reduces
+      // it staged have read it), then written by two bulk tensor stores, so
+      // that the rows go out as whole 128-byte lines.
+      if (DQ && n >= Lay::kDSBufs)
+        ok = __all_sync(0xffffffffu, mbar_wait(ds_free + n % Lay::kDSBufs, (n / Lay::kDSBufs - 1) & 1, abort_flag));
+      if (ok) ok = staging_read();
+      if (!ok) break;
+      uint8_t* stage = sDS + (n % Lay::kDSBufs) * Lay::kDSBytes;
+      uint8_t* row = stage + half * Lay::kChunkBytes + r * 128;
       tc_fence_after();
-      // first warpgroup stores dV, second stores dK (scaled)
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem_addr(tmem, lane_base, col + cc * 32), v);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(v[8 * t + 2 * e]) * mul, __uint_as_float(v[8 * t + 2 * e + 1]) * mul);
+          const int u = cc * 4 + t;
+          *reinterpret_cast<uint4*>(row + ((u ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      // dV and dK are read out of TMEM: the next unit may restart them
+      tc_fence_before();
+      mbar_arrive(acc_free);
+      fence_proxy_async_smem();
+      mbar_arrive(epi_staged);
+      if (warp == 2 && lane == 0 && (ok = mbar_wait(epi_staged, ue & 1, abort_flag))) {
+        const int row0 = static_cast<int>(seq0 + k0);
+        tma_store_3d(&tm_dv, stage, 0, w.g, row0);
+        tma_store_3d(&tm_dk, stage + Lay::kChunkBytes, 0, w.g, row0);
+        bulk_commit_group();
+      }
+      // the stores run on while the next unit starts; the buffer takes
+      // dS^T (or the next tile's staging) only once they have read it
+      ++ue;
+      pending = true;
+    } else {
+      // the sequence's last, ragged tile: row by row, rows past the end skipped
+      tc_fence_after();
       const bool row_ok = kpos < L;
       const long long tok = seq0 + kpos;
-      const uint32_t col = half == 0 ? Lay::kColDV : Lay::kColDK;
-      const float mul = half == 0 ? 1.f : p.scale;
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? p.dv : p.dk) + (tok * p.Hkv + w.g) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -532,12 +595,14 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int t = 0; t < 4; ++t) o4[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
         }
       }
+      // dV and dK are in registers and stored: the next unit may restart them
+      tc_fence_before();
+      mbar_arrive(acc_free);
     }
-    // dV and dK are in registers and stored: the next unit may restart them
-    tc_fence_before();
-    mbar_arrive(acc_free);
     ++uc;
     }
+    // no bulk store may still be writing when the CTA exits
+    if (warp == 2 && lane == 0) bulk_wait_group0();
     if (!ok) give_up();
   } else if (DQ) {
     // ------------------------------------------------------------ dQ warpgroup
@@ -659,7 +724,8 @@ int launch_bwd_dq_det(int d, const CUtensorMap& tq, const CUtensorMap& tk, const
 // order), so no sum depends on the order in which CTAs run.
 template <int D>
 int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                 const CUtensorMap& tdq, const BwdParams& p, bool deterministic, cudaStream_t stream) {
+                 const CUtensorMap& tdq, const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
+                 bool deterministic, cudaStream_t stream) {
   const long long rows = p.T * p.Hq;
   const long long pre_blocks = (rows * 8 + 255) / 256;
   fa_bwd_rowdot_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, stream>>>(p);
@@ -676,7 +742,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long units = static_cast<long long>(p.n_kvtiles) * p.B * p.Hkv;
     const int grid = static_cast<int>(units < sms ? units : sms);
-    kern<<<grid, kBwdThreads, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+    kern<<<grid, kBwdThreads, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     e = cudaGetLastError();
   } else {
     e = static_cast<cudaError_t>(launch_bwd128_main(tq, tk, tv, tdo, tdq, p, !deterministic, stream));
@@ -689,9 +755,10 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 }
 
 int launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-               const CUtensorMap& tdq, const BwdParams& p, bool deterministic, cudaStream_t stream) {
-  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, p, deterministic, stream);
-  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, p, deterministic, stream);
+               const CUtensorMap& tdq, const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
+               bool deterministic, cudaStream_t stream) {
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, tdq, tdk, tdv, p, deterministic, stream);
+  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, tdq, tdk, tdv, p, deterministic, stream);
   return -1;
 }
 
