@@ -477,11 +477,17 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const int zero_below = !key_ok ? kTile : ((causal && q0 == k0) ? r : 0);
       uint8_t* ds_row = sDS + (n % Lay::kDSBufs) * Lay::kDSBytes + half * Lay::kChunkBytes + r * 128;
       const uint32_t reg = region(n);
+      // S^T and dP^T of chunk cl + 1 load while chunk cl is computed
+      uint32_t sv[2][16], dpv[2][16];
+      tmem_ld_x16_pair(tmem_addr(reg, lane_base, half * 64), sv[0], tmem_addr(tmem, lane_base, Lay::kColDP + half * 64),
+                       dpv[0]);
 #pragma unroll
       for (int cl = 0; cl < 4; ++cl) {
         const int col0 = half * 64 + cl * 16;  // first query column of this chunk
-        uint32_t sv[16], dpv[16];
-        tmem_ld_x16_pair(tmem_addr(reg, lane_base, col0), sv, tmem_addr(tmem, lane_base, Lay::kColDP + col0), dpv);
+        const int cb = cl & 1;
+        if (cl < 3)
+          tmem_ld_x16_pair_nowait(tmem_addr(reg, lane_base, col0 + 16), sv[cb ^ 1],
+                                  tmem_addr(tmem, lane_base, Lay::kColDP + col0 + 16), dpv[cb ^ 1]);
         if (cl == 3) {
           // dP^T fully read: the next step's dP^T may overwrite it
           tc_fence_before();
@@ -493,14 +499,15 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int t = 0; t < 8; ++t) {
           const float4 s4 = nst4[cl * 8 + t];
           const float2 nl2 = make_float2(s4.x, s4.y), nd = make_float2(s4.z, s4.w);
-          const float2 x = fma2(make_float2(__uint_as_float(sv[2 * t]), __uint_as_float(sv[2 * t + 1])), c2, nl2);
+          const float2 x =
+              fma2(make_float2(__uint_as_float(sv[cb][2 * t]), __uint_as_float(sv[cb][2 * t + 1])), c2, nl2);
           float2 pv = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (mask_chunk) {
             if (col0 + 2 * t < zero_below) pv.x = 0.f;
             if (col0 + 2 * t + 1 < zero_below) pv.y = 0.f;
           }
           const float2 dd =
-              mul2(pv, add2(make_float2(__uint_as_float(dpv[2 * t]), __uint_as_float(dpv[2 * t + 1])), nd));
+              mul2(pv, add2(make_float2(__uint_as_float(dpv[cb][2 * t]), __uint_as_float(dpv[cb][2 * t + 1])), nd));
           pk[t] = pack_bf16x2(pv.x, pv.y);
           dsk[t] = pack_bf16x2(dd.x, dd.y);
         }
@@ -522,6 +529,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           *reinterpret_cast<uint4*>(ds_row + ((uu ^ (r & 7)) << 4)) =
               make_uint4(dsk[4 * u2], dsk[4 * u2 + 1], dsk[4 * u2 + 2], dsk[4 * u2 + 3]);
         }
+        if (cl < 3) tmem_ld_wait_x16_pair(sv[cb ^ 1], dpv[cb ^ 1]);
       }
       if (!ok) break;
       tmem_st_wait();
