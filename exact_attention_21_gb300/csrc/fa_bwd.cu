@@ -34,7 +34,8 @@
 //   warps 2..9   two score warpgroups: thread = key row (TMEM lane); the
 //                first takes query columns 0..63, the second 64..127; P^T to
 //                TMEM (bf16), dS^T to TMEM and (for dQ) shared memory; the
-//                unit's dV / dK epilogue.
+//                unit's dV / dK epilogue (a whole key tile staged in shared
+//                memory and written by two TMA bulk stores).
 //   warps 10..13 dQ warpgroup: dQ tile TMEM -> swizzled shared memory (the
 //                step's dS^T buffer, free once the dQ product has read it) ->
 //                two TMA bulk reduce-adds (f32) into the global accumulator.
