@@ -1264,16 +1264,50 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
   const int ns = (tiles + p.split_tiles - 1) / p.split_tiles;
   const float* lp = p.lse_part + row * p.n_splits;
   const float* op = p.o_part + row * p.n_splits * D + lane * E;
-  float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, lp[s]);
-  float den = 0.f, acc[E];
+  // Eight splits at a time: all their loads are issued before any is used
+  // (one memory round trip per eight splits, not one per split), then they
+  // join a running merge: acc and den are kept relative to the running
+  // max mx and rescaled when it grows.
+  constexpr int kBatch = 8;
+  float mx = -INFINITY, den = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float w = expf(lp[s] - mx);
-    den += w;
+  for (int s0 = 0; s0 < ns; s0 += kBatch) {
+    float lv[kBatch], ov[kBatch][E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, op[static_cast<long long>(s) * D + e], acc[e]);
+    for (int j = 0; j < kBatch; ++j) {
+      const int sj = s0 + j;
+      lv[j] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ov[j][e] = 0.f;
+      if (sj < ns) {
+        lv[j] = __ldg(lp + sj);
+        const float* src = op + static_cast<long long>(sj) * D;
+        if constexpr (E == 4) {
+          const float4 v4 = __ldg(reinterpret_cast<const float4*>(src));
+          ov[j][0] = v4.x; ov[j][1] = v4.y; ov[j][2] = v4.z; ov[j][3] = v4.w;
+        } else {
+          const float2 v2 = __ldg(reinterpret_cast<const float2*>(src));
+          ov[j][0] = v2.x; ov[j][1] = v2.y;
+        }
+      }
+    }
+    float m2 = mx;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) m2 = fmaxf(m2, lv[j]);
+    if (m2 == -INFINITY) continue;  // nothing finite yet
+    const float sc = expf(mx - m2);  // 0 while mx is still -inf
+    den *= sc;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const float w = expf(lv[j] - m2);  // 0 for the padding entries
+      den += w;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, ov[j][e], acc[e]);
+    }
+    mx = m2;
   }
   const float inv = ns > 0 ? 1.f / den : 0.f;
   uint32_t pk[E / 2];
