@@ -211,9 +211,11 @@ int check_shape(int B, int Hq, int Hkv, int N, int d, long long T, float scale, 
 
 // 128-key tiles per decode split.  Decode CTAs are resident one per SM, so a
 // grid of (split, K/V head, sequence) CTAs runs in ceil(CTAs / SMs) waves, and
-// each CTA costs its tiles plus about one tile of start-up (barrier set-up and
-// the latency of its first loads).  Picks the split length with the lowest
-// modelled time; packed caches are modelled as sequences of the mean length.
+// each CTA costs its tiles plus item_cost tiles of start-up (barrier set-up
+// and the latency of its first loads; measured at about four tiles for an
+// item of paired d = 64 heads, whose query and output cover two heads, and
+// one otherwise).  Picks the split length with the lowest modelled time;
+// packed caches are modelled as sequences of the mean length.
 // Packed caches numbered compactly (every item exists and the CTAs take
 // consecutive ones): the split length with the smallest modelled time of the
 // busiest CTA, ceil(items / SMs) items of the split's tiles plus about half a
@@ -234,7 +236,7 @@ int decode_split_tiles_compact(int B, int Hkv, int max_tiles, long long T, int s
   return best;
 }
 
-int decode_split_tiles(int B, int Hkv, int max_tiles, long long T, bool packed, int sms) {
+int decode_split_tiles(int B, int Hkv, int max_tiles, long long T, bool packed, int sms, double item_cost) {
   const double mean_tiles =
       packed ? std::max(1.0, static_cast<double>(T) / B / fa::kTile) : static_cast<double>(max_tiles);
   int best = 1;
@@ -243,7 +245,7 @@ int decode_split_tiles(int B, int Hkv, int max_tiles, long long T, bool packed, 
     const long long per_seq = static_cast<long long>(std::ceil(mean_tiles / st));
     const long long ctas = static_cast<long long>(B) * Hkv * per_seq;
     const long long waves = (ctas + sms - 1) / sms;
-    const double time = static_cast<double>(waves) * (std::min<double>(st, mean_tiles) + 1.0);
+    const double time = static_cast<double>(waves) * (std::min<double>(st, mean_tiles) + item_cost);
     if (st == 1 || time < best_time) {
       best = st;
       best_time = time;
@@ -532,7 +534,7 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   const bool tc = d == 128 || pair;
   p.compact = (tc && packed && B <= (fp8 ? 192 : 1024)) ? 1 : 0;
   p.split_tiles = p.compact ? decode_split_tiles_compact(B, p.Hkv, s.n_tiles, T, dev->sms)
-                            : decode_split_tiles(B, p.Hkv, s.n_tiles, T, packed, dev->sms);
+                            : decode_split_tiles(B, p.Hkv, s.n_tiles, T, packed, dev->sms, pair ? 4.0 : 1.0);
   p.n_splits = (s.n_tiles + p.split_tiles - 1) / p.split_tiles;
   p.sms = dev->sms;
   const size_t rows = static_cast<size_t>(B) * Hq * p.n_splits;
