@@ -536,6 +536,9 @@ static int decode_common(const void* q, const void* k, const void* v, const floa
   p.split_tiles = p.compact ? decode_split_tiles_compact(B, p.Hkv, s.n_tiles, T, dev->sms)
                             : decode_split_tiles(B, p.Hkv, s.n_tiles, T, packed, dev->sms, pair ? 4.0 : 1.0);
   p.n_splits = (s.n_tiles + p.split_tiles - 1) / p.split_tiles;
+  // one split per row of a batched cache (every sequence has N >= 1 keys):
+  // the tensor-core kernel writes O and the LSE itself and no combine runs
+  p.direct = (tc && !paged && cu_seqlens_k == nullptr && p.n_splits == 1) ? 1 : 0;
   p.sms = dev->sms;
   const size_t rows = static_cast<size_t>(B) * Hq * p.n_splits;
   p.o_part = static_cast<float*>(workspace);

@@ -116,6 +116,10 @@ struct DecodeParams {
   // prefix of each sequence's split count, built in shared memory at kernel
   // start (packed caches of unequal length); 0: split-major over n_splits
   int compact;
+  // 1: one split per (sequence, K/V head) and every sequence non-empty
+  // (batched caches): the split kernel writes O and the LSE itself and no
+  // combine runs; 0: partial results for the combine
+  int direct;
 };
 
 }  // namespace fa

@@ -1210,14 +1210,28 @@ fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const int hh = h0 + h;
         if (p.pair || hh < group) {
           const float l = sRedW[h] + sRedW[H + h] + sRedW[2 * H + h] + sRedW[3 * H + h];
+          const float lse = (m[h] + log2f(l)) * 0.6931471805599453f;
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
           if (!p.pair) {
-            p.o_part[((row0 + hh) * p.n_splits + it.split) * D + r] = osum[h] / l;
-            if (r == 0) p.lse_part[(row0 + hh) * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
+            const long long row = row0 + hh;  // b Hq + h
+            if (p.direct) {
+              // the only split of the row: the output itself (bf16) and the LSE ([Hq, B])
+              o[row * D + r] = __float2bfloat16_rn(osum[h] / l);
+              if (r == 0) p.lse[(row % p.Hq) * p.B + row / p.Hq] = lse;
+            } else {
+              p.o_part[(row * p.n_splits + it.split) * D + r] = osum[h] / l;
+              if (r == 0) p.lse_part[row * p.n_splits + it.split] = lse;
+            }
           } else if (const long long qr = pair_qrow(it, hh); qr >= 0) {
             // O^T rows of this warpgroup's own K/V head; the other 64 rows mix
             // in the other head's values and are dropped
-            if ((r >= 64) == (wg == 1)) p.o_part[(qr * p.n_splits + it.split) * 64 + (r & 63)] = osum[h] / l;
-            if (r == 0) p.lse_part[qr * p.n_splits + it.split] = (m[h] + log2f(l)) * 0.6931471805599453f;
+            if (p.direct) {
+              if ((r >= 64) == (wg == 1)) o[qr * 64 + (r & 63)] = __float2bfloat16_rn(osum[h] / l);
+              if (r == 0) p.lse[(qr % p.Hq) * p.B + qr / p.Hq] = lse;
+            } else {
+              if ((r >= 64) == (wg == 1)) p.o_part[(qr * p.n_splits + it.split) * 64 + (r & 63)] = osum[h] / l;
+              if (r == 0) p.lse_part[qr * p.n_splits + it.split] = lse;
+            }
           }
         }
       }
@@ -1362,6 +1376,7 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
   kern<<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.direct) return cudaSuccess;  // the split kernel wrote O and the LSE
   // the combine as a programmatic dependent launch: its CTAs are scheduled
   // while the split kernel runs and start merging as soon as it completes
   const long long rows = static_cast<long long>(p.B) * p.Hq;
