@@ -51,6 +51,16 @@ def test_decode_batched(cuda_device, d, N):
     check(3, 8, 2, d, [N] * 3, batched=True, seed=N)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [200, 256])
+def test_decode_batched_one_split_per_row(cuda_device, d, N):
+    """Many short batched caches (64 sequences of two tiles, Hq64/Hkv8): the
+    split model gives each (sequence, K/V head) a single split, so the split
+    kernel writes O and the LSE itself and no combine runs (d = 64 on head
+    pairs, d = 128 unpaired)."""
+    check(64, 64, 8, d, [N] * 64, batched=True, seed=N + d)
+
+
 @pytest.mark.parametrize("heads", [(8, 2), (32, 2)])
 def test_decode_many_items_per_cta(cuda_device, heads):
     """Many more (split, K/V head, sequence) items than SMs, of mixed and
