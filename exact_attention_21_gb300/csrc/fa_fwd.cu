@@ -16,6 +16,12 @@
 // smaller reference (values up to 2^kRescaleSlack) and O, l need no rescale.
 // The merge rule holds for any common reference, so the result is the same
 // exact attention; this only skips O rescales that would multiply by nearly 1.
+// With the key columns split between the two softmax warpgroups (d = 64),
+// each keeps its own reference, and after a unit's first tile P is taken
+// against it before any row max: the tile is kept when its row sum stays
+// within 2^kRescaleSlack (so every p does), which is exactly when the max
+// test would have kept the reference; otherwise the tile is redone with the
+// row max.  Same P, same result, without the max in the common case.
 //
 // The kernel is persistent: one CTA per SM walks work units (128-row query
 // tile, query head, sequence) in heavy-first order, keeping its TMEM,
@@ -91,6 +97,7 @@ struct FwdLayout {
 
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.f;  // P values stay below 2^8 between rescales
+constexpr float kFastLimit = 256.f;   // 2^kRescaleSlack
 
 // PAGED: K and V are read through a page table (prefill over a paged cache),
 // the keys of a sequence may outnumber its queries (a cached earlier part),
@@ -474,6 +481,38 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
           for (int i = 0; i < 64; ++i)
             if (k0 + i >= lim) x[i] = -INFINITY;
+        }
+        // Split halves, after a unit's first tile: P against the current
+        // reference first, without the row max.  The tile is kept when its row
+        // sum stays within 2^slack (then every p does, the bound the lazy
+        // rescale keeps); otherwise (also a NaN sum: no reference yet) the
+        // warp redoes the tile below with the row max, overwriting P.
+        if (Lay::kSplit && j > 0) {
+          const float2 nm0 = make_float2(-m, -m);
+          float2 fs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              const float2 e = fma2(make_float2(x[cc * 32 + 2 * t], x[cc * 32 + 2 * t + 1]), c2, nm0);
+              const float2 pv = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+              fs2[t & 3] = add2(fs2[t & 3], pv);
+              pk[t] = pack_bf16x2(pv.x, pv.y);
+            }
+            tmem_st_x16(tmem_addr(tS, lane_base, 64 * half + cc * 16), pk);
+          }
+          const float2 f01 = add2(fs2[0], fs2[1]), f23 = add2(fs2[2], fs2[3]);
+          const float fsum = (f01.x + f01.y) + (f23.x + f23.y);
+          if (!__any_sync(0xffffffffu, !(fsum <= kFastLimit))) {
+            l += fsum;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(p_full + (Lay::kSplit ? half * NB : 0) + b);
+            continue;
+          }
+          tmem_st_wait();  // the redo below stores P to the same columns
         }
         float mx[4] = {fmaxf(x[0], x[1]), fmaxf(x[2], x[3]), fmaxf(x[4], x[5]), fmaxf(x[6], x[7])};
 #pragma unroll
