@@ -16,12 +16,15 @@
 // smaller reference (values up to 2^kRescaleSlack) and O, l need no rescale.
 // The merge rule holds for any common reference, so the result is the same
 // exact attention; this only skips O rescales that would multiply by nearly 1.
-// With the key columns split between the two softmax warpgroups (d = 64),
-// each keeps its own reference, and after a unit's first tile P is taken
-// against it before any row max: the tile is kept when its row sum stays
-// within 2^kRescaleSlack (so every p does), which is exactly when the max
-// test would have kept the reference; otherwise the tile is redone with the
-// row max.  Same P, same result, without the max in the common case.
+// After a unit's first tile, P is taken against the current reference
+// before any row max: the tile is kept when its row sum stays within
+// 2^kRescaleSlack (so every p does), which is exactly when the max test
+// would have kept the reference; otherwise the tile is redone with the row
+// max.  Same P, same result, without the max in the common case.  With the
+// key columns split between the two softmax warpgroups (d = 64) each keeps
+// its own reference and decides per warp; with one shared reference per row
+// (d = 128) the 256 softmax threads take one decision per tile through the
+// exchange barrier the row max would have used.
 //
 // The kernel is persistent: one CTA per SM walks work units (128-row query
 // tile, query head, sequence) in heavy-first order, keeping its TMEM,
@@ -89,7 +92,9 @@ struct FwdLayout {
   // p_full[2][3], pv_done[2][2], xchg, o_final, o_free, drain
   static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 4 * kSBufs + 4 + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  // misc: TMEM slot, abort flag (d = 128: and three per-phase "some row left
+  // the rescale bound" flags)
+  static constexpr int kBytes = kOffMisc + (kSplit ? 16 : 32) + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColO = 384, kColO1 = 448;  // kColO1: second half's O (d = 64)
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
@@ -188,6 +193,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* stage_full = drain + 1;  // every softmax thread has written its rows of a staged tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
+  int* any_out = reinterpret_cast<int*>(smem + Lay::kOffMisc + 8);  // [3]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -210,6 +216,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(drain, npv + 1);
     mbar_init(stage_full, 256);
     *abort_flag = 0;
+    if constexpr (!Lay::kSplit) any_out[0] = any_out[1] = any_out[2] = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -431,8 +438,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           } else {
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              umma_ts(tmem + Lay::kColO, a_tm + kk * 8, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_o,
-                      (j > 0 || kk > 0));
+              umma_ts(tmem + Lay::kColO, a_tm + (kk / 4) * 64 + (kk % 4) * 8,
+                      vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_o, (j > 0 || kk > 0));
           }
           umma_commit(s_free + b);
           umma_commit(v_empty + vs);
@@ -454,6 +461,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const float c = p.scale_log2;
     const float2 c2 = make_float2(c, c);
     int g = 0, uc = 0, xp = 0;  // score tiles, units and exchange phases so far
+    int fp = 0;                 // tiles that took P against the kept reference first (d = 128)
     int nst = 0;  // units whose output went through a staging tile
     const bool store_issuer = warp == 4 && lane == 0;
     bool ok = true;
@@ -487,7 +495,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // sum stays within 2^slack (then every p does, the bound the lazy
         // rescale keeps); otherwise (also a NaN sum: no reference yet) the
         // warp redoes the tile below with the row max, overwriting P.
-        if (Lay::kSplit && j > 0) {
+        if (j > 0) {
           const float2 nm0 = make_float2(-m, -m);
           float2 fs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                            make_float2(0.f, 0.f)};
@@ -505,7 +513,22 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
           const float2 f01 = add2(fs2[0], fs2[1]), f23 = add2(fs2[2], fs2[3]);
           const float fsum = (f01.x + f01.y) + (f23.x + f23.y);
-          if (!__any_sync(0xffffffffu, !(fsum <= kFastLimit))) {
+          bool keep;
+          if constexpr (Lay::kSplit) {
+            keep = !__any_sync(0xffffffffu, !(fsum <= kFastLimit));
+          } else {
+            // both halves share the row's reference: one decision for all 256
+            // threads, through the exchange barrier (flag slot fp % 3; the
+            // slot of two phases on is cleared once every thread has read it)
+            if (!(fsum <= kFastLimit)) atomicOr(any_out + fp % 3, 1);
+            mbar_arrive(xchg);
+            if (!(ok = mbar_wait(xchg, xp & 1, abort_flag))) break;
+            ++xp;
+            keep = *reinterpret_cast<volatile int*>(any_out + fp % 3) == 0;
+            if (half == 0 && r == 0) any_out[(fp + 2) % 3] = 0;
+            ++fp;
+          }
+          if (keep) {
             l += fsum;
             tmem_st_wait();
             tc_fence_before();
@@ -549,11 +572,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             sum2[t & 3] = add2(sum2[t & 3], pv);
             pk[t] = pack_bf16x2(pv.x, pv.y);
           }
-          // P for keys [64 half + 32 cc, +32) goes to columns [32 half + 16 cc, +16)
-          // (every thread of both halves read its scores before the exchange
-          // above), or, split, to [64 half + 16 cc, +16): columns this
-          // thread has read itself.
-          tmem_st_x16(tmem_addr(tS, lane_base, (Lay::kSplit ? 64 : 32) * half + cc * 16), pk);
+          // P for keys [64 half + 32 cc, +32) goes to columns [64 half + 16 cc,
+          // +16): columns this thread has read itself (the P V issuer takes
+          // keys 16 kk .. 16 kk + 15 from column 64 (kk / 4) + 8 (kk % 4)).
+          tmem_st_x16(tmem_addr(tS, lane_base, 64 * half + cc * 16), pk);
         }
         const float2 s01 = add2(sum2[0], sum2[1]), s23 = add2(sum2[2], sum2[3]);
         l = l * alpha + ((s01.x + s01.y) + (s23.x + s23.y));
