@@ -50,6 +50,24 @@ __device__ __forceinline__ bool sequence_bounds(const int* cu, int s, int N, lon
   return true;
 }
 
+// n / d for 0 <= n < 2^31 and a divisor d fixed per launch: (n m) >> s with
+// l = ceil(log2 d), s = 31 + l and m = ceil(2^s / d) < 2^32 (division by
+// invariant integers using multiplication, Granlund and Montgomery), one
+// wide multiply and a shift instead of the division's instruction sequence.
+struct FastDiv {
+  uint32_t m;
+  int s;
+};
+inline FastDiv make_fast_div(int d) {
+  int l = 0;
+  while ((1 << l) < d) ++l;
+  const uint64_t m = ((1ull << (31 + l)) + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d);
+  return FastDiv{static_cast<uint32_t>(m), 31 + l};
+}
+__device__ __forceinline__ int fast_div(int n, FastDiv f) {
+  return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(n)) * f.m) >> f.s);
+}
+
 struct FwdParams {
   void* o;            // bf16 [T, Hq, d]
   float* lse;         // f32 [Hq, T]
@@ -58,6 +76,9 @@ struct FwdParams {
   long long T;
   int B, Hq, Hkv, N, group, causal, n_qtiles;
   int group_pairs;    // (sequence, head) pairs per scheduling group
+  // the divisors of the forward's work-unit lookup: units per scheduling
+  // group (group_pairs x query tiles), group_pairs, Hq, the GQA group
+  FastDiv div_group_units, div_group_pairs, div_hq, div_qgroup;
   float scale_log2;   // scale * log2(e)
   // null, or device [B]: the S-issuing thread adds the (query tile, key tile)
   // pairs whose S it computed, per sequence (summed over query heads)

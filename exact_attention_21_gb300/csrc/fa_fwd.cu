@@ -134,13 +134,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     int Lk, off;  // keys of the sequence; query i sits at key position off + i
   };
   auto unit_at = [&](int u, Unit& w) -> bool {
-    const int gi = u / (kGroup * p.n_qtiles);  // only the last group can be short
+    // (the divisions by launch constants go through precomputed reciprocals)
+    const int gi = fast_div(u, p.div_group_units);  // only the last group can be short
     const int gp = min(kGroup, n_pairs - gi * kGroup);
     const int r = u - gi * kGroup * p.n_qtiles;
-    const int pair = gi * kGroup + r % gp;
-    w.qt = p.n_qtiles - 1 - r / gp;
-    w.h = pair % p.Hq;
-    const int sq = pair / p.Hq;
+    const int rq = gp == kGroup ? fast_div(r, p.div_group_pairs) : r / gp;
+    const int pair = gi * kGroup + (r - rq * gp);
+    w.qt = p.n_qtiles - 1 - rq;
+    const int sq = fast_div(pair, p.div_hq);
+    w.h = pair - sq * p.Hq;
     w.sq = sq;
     if (!sequence_bounds(p.cu, sq, p.N, p.T, w.seq0, w.L, p.status)) return false;
     w.q0 = w.qt * kTile;
@@ -162,7 +164,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       w.off = 0;
       w.nkv = kv_tiles_for(w.qt, w.L, causal);
     }
-    w.kvh = w.h / p.group;
+    w.kvh = fast_div(w.h, p.div_qgroup);
     return true;
   };
 
@@ -794,6 +796,10 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   const int grid = static_cast<int>(units < sms ? units : sms);  // one CTA per SM, persistent
   FwdParams q = p;
   q.group_pairs = choose_group_pairs(p, grid, D);
+  q.div_group_units = make_fast_div(q.group_pairs * q.n_qtiles);
+  q.div_group_pairs = make_fast_div(q.group_pairs);
+  q.div_hq = make_fast_div(q.Hq);
+  q.div_qgroup = make_fast_div(q.group);
   fa_fwd_kernel<D, PAGED><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tq, tk, tv, to, q);
   return cudaGetLastError();
 }
