@@ -33,11 +33,15 @@
 // is triple-buffered: S of the next key tiles is computed while the softmax
 // works on the current one and P V of the previous one runs, and an S never
 // queues behind a P V that is still waiting for its softmax.  Warp roles:
-//   warp 0       TMA producer for Q (per unit) and K_j;
-//   warp 3       TMA producer for V_j.  Separate threads, so a K load never
-//                waits behind a V ring slot that P V has not released yet.
+//   warp 0       TMA producer for Q (per unit) and K_j (lane 0), and at
+//                d = 64 also for V_j (lane 1);
+//   warp 3       TMA producer for V_j (d = 128); at d = 64 the second P V
+//                issuer.  K and V are loaded by separate threads, so a K load
+//                never waits behind a V ring slot that P V has not released.
 //   warp 1       TMEM allocator and S issuer: S_j = Q K_j^T into buffer j % 3.
-//   warp 2       P V issuer: O += P_j V_j (P_j read from TMEM).
+//   warp 2       P V issuer: O += P_j V_j (P_j read from TMEM); at d = 64
+//                keys 0..63 only, keys 64..127 by warp 3 (paged: warp 12,
+//                since the paged producers take whole warps).
 //   warps 4..7   softmax, key columns 0..63 of each score tile;
 //   warps 8..11  softmax, key columns 64..127.
 //                Thread t of each softmax warpgroup owns query row
@@ -87,7 +91,11 @@ struct FwdLayout {
   // 64-column accumulators next to the three score buffers); the halves are
   // merged once per unit.  d = 128: one O, statistics exchanged per key tile.
   static constexpr bool kSplit = D == 64;
-  static constexpr int kThreads = kSplit ? 416 : 384;  // warp 12: second P V issuer
+  // paged d = 64: warp 12 is the second P V issuer (the paged producers
+  // need whole warps); otherwise 12 warps (d = 64: the K and V producers
+  // share warp 0 and warp 3 issues the second P V), so that one scheduler
+  // holds three warps and a thread may use 168 registers
+  static constexpr int threads(bool paged) { return kSplit && paged ? 416 : 384; }
   // q_full[2], q_empty[2], k_full[], k_empty[], v_full[], v_empty[], s_full[3], s_free[3],
   // p_full[2][3], pv_done[2][2], xchg, o_final, o_free, drain
   static constexpr int kNumBars = 4 + 2 * kStagesK + 2 * kStagesV + 4 * kSBufs + 4 + 5;
@@ -108,7 +116,7 @@ constexpr float kFastLimit = 256.f;   // 2^kRescaleSlack
 // the keys of a sequence may outnumber its queries (a cached earlier part),
 // and the causal mask is aligned at the newest token.
 template <int D, bool PAGED>
-__global__ void __launch_bounds__(FwdLayout<D>::kThreads, 1)
+__global__ void __launch_bounds__(FwdLayout<D>::threads(PAGED), 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using Lay = FwdLayout<D>;
@@ -184,6 +192,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   uint64_t* v_full = k_empty + NK;
   uint64_t* v_empty = v_full + NV;
   constexpr int NB = Lay::kSBufs;
+  constexpr bool kMergedProducers = Lay::kSplit && !PAGED;
   uint64_t* s_full = v_empty + NV;
   uint64_t* s_free = s_full + NB;
   uint64_t* p_full = s_free + NB;   // [half (split) or 0][buffer]
@@ -310,10 +319,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int i = 0; i < NV; ++i)
         if (v_uses[i]) mbar_wait(v_full + i, (v_uses[i] - 1) & 1, &never);
     }
-  } else if (warp == 0 || warp == 3) {
+  } else if (warp == 0 || (warp == 3 && !kMergedProducers)) {
     // ------------------------------------------------------------ TMA producers
-    if (lane == 0) {
-      const bool is_k = warp == 0;  // warp 0: Q and K; warp 3: V
+    if (kMergedProducers ? lane < 2 : lane == 0) {
+      // Q and K: warp 0 (lane 0); V: warp 3, or lane 1 of warp 0
+      const bool is_k = kMergedProducers ? lane == 0 : warp == 0;
       if (is_k) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
@@ -408,10 +418,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int never = 0;
       mbar_wait(drain, 0, &never);
     }
-  } else if (warp == 2 || (Lay::kSplit && warp == 12)) {
+  } else if (warp == 2 || (Lay::kSplit && warp == (kMergedProducers ? 3 : 12))) {
     // ------------------------------------------------------------ P V issuer(s)
-    // split: warp 2 accumulates keys 0..63 of every tile into O, warp 12 keys
-    // 64..127 into O1 (two threads also keep two N = 64 products in flight)
+    // split: warp 2 accumulates keys 0..63 of every tile into O, warp 3
+    // (paged: 12) keys 64..127 into O1 (two threads also keep two N = 64
+    // products in flight)
     if (lane == 0) {
       const int hv = warp == 2 ? 0 : 1;
       constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, false, true);
@@ -800,7 +811,7 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   q.div_group_pairs = make_fast_div(q.group_pairs);
   q.div_hq = make_fast_div(q.Hq);
   q.div_qgroup = make_fast_div(q.group);
-  fa_fwd_kernel<D, PAGED><<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tq, tk, tv, to, q);
+  fa_fwd_kernel<D, PAGED><<<grid, Lay::threads(PAGED), Lay::kBytes, stream>>>(tq, tk, tv, to, q);
   return cudaGetLastError();
 }
 
