@@ -9,10 +9,11 @@ workload is B=2, H=16, N=4096, d=64, causal, forward + backward.
 Prints ONE JSON line (rank 0).  ``value`` is algorithmic TFLOP/s of the whole
 job (4 L^2 d per (sequence, head) forward, halved under the causal mask,
 backward 2.5x that) with inputs resident in HBM; L2 is flushed before every
-timed step.  ``e2e`` repeats the measurement through the same C ABI with every
-step's inputs copied from pinned host memory and its gradients (or O) copied
-back inside the timed region, the copies of neighbouring steps overlapping the
-computation as in a training loop.
+timed step (``flush_l2``).  ``e2e`` repeats the measurement through the same C
+ABI with every step's inputs copied from pinned host memory and its gradients
+(or O) copied back inside the timed region, the copies of neighbouring steps
+overlapping the computation as in a training loop.  ``gpu_launches`` is the
+library's own count of the kernels it launched inside the timed region.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this method
 has) on a bounded sample of the same workload.
@@ -37,12 +38,25 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "fwdbwd_b2_h16_n4096_d64_causal"
+L2_NOTE = "flushed before every timed step (256 MiB write, then read back: no dirty line left)"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 THROTTLE_BITS = {  # nvidia-smi clocks_event_reasons bitmask
     0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
     0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
     0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
 }
+
+
+def flush_l2(buf, sink, value):
+    """Evict L2 before a timed step, outside its events: write ``buf`` (256 MiB,
+    twice the 129 MB L2), then read it back.  The write alone leaves L2 full of
+    the flush's own dirty lines, and the timed step would then pay for writing
+    them back to HBM (about 10 us of a 64 x 4096 decoding step); after the read
+    L2 holds clean lines of the flush buffer and none of the step's data."""
+    import torch
+
+    buf.fill_(float(value))
+    torch.sum(buf, dim=0, out=sink)
 
 
 def load_peaks():
@@ -198,7 +212,7 @@ def bench_ours(args, world, rank, local):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = torch.empty(fa.fa_bwd_workspace_size(Hq, T, d), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    launches_per_step = 1 + (3 if w.backward else 0)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def step(ev=None):
         if ev is not None:
@@ -223,9 +237,11 @@ def bench_ours(args, world, rank, local):
         pg.barrier()
     torch.cuda.synchronize()
     sampler.mark_on()
+    launches0 = fa.fa_launch_count()
     for i in range(args.steps):
-        flush.fill_(float(i))  # evicts L2 (256 MiB > 129 MB) outside the timed events
+        flush_l2(flush, sink, i)  # outside the timed events
         step(events[i])
+    launches = fa.fa_launch_count() - launches0
     torch.cuda.synchronize()
     sampler.mark_off()
     if pg:
@@ -336,7 +352,7 @@ def bench_ours(args, world, rank, local):
                    "global_batch": w.B * world, "seq_len": w.N,
                    "fwd_gflop_per_step": round(w.fwd_flops() / 1e9, 3),
                    "bwd_gflop_per_step": round(w.bwd_flops() / 1e9, 3) if w.backward else 0.0,
-                   "l2": "flushed before every timed step (256 MiB write)",
+                   "l2": L2_NOTE,
                    "parallelism": f"replicas x{world}"},
         "fwd_ms": round(fwd_avg, 4),
         "bwd_ms": round(bwd_avg, 4),
@@ -351,7 +367,7 @@ def bench_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "pipelining": "two buffer sets; copies in and out on their own streams overlap the neighbouring steps"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
     tr = traffic_entry(args.traffic_file, w.name, kern)
@@ -365,7 +381,7 @@ def bench_ours(args, world, rank, local):
         if w.backward:
             del do, dq, dk, dv, ws
         torch.cuda.empty_cache()
-        line["per_config"] = per_config_lines(args, rank, dev, stream, flush, peaks)
+        line["per_config"] = per_config_lines(args, rank, dev, stream, flush, sink, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     if pg:
@@ -381,7 +397,7 @@ PER_CONFIG = ("fwd_b1_h1_n256_d64", "fwd_b4_h16_n2048_d64", "fwd_b2_h32_n4096_d1
               "decode_b64_hq64_hkv8_n4096_d64", "decode_varlen8_hq32_hkv8_d128")
 
 
-def per_config_lines(args, rank, dev, stream, flush, peaks):
+def per_config_lines(args, rank, dev, stream, flush, sink, peaks):
     import torch
 
     import exact_attention_21_gb300.fa as fa
@@ -418,7 +434,7 @@ def per_config_lines(args, rank, dev, stream, flush, peaks):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(5):
-            flush.fill_(1.0)
+            flush_l2(flush, sink, 1.0)
             run()
         e1.record(stream)
         torch.cuda.synchronize()
@@ -428,7 +444,7 @@ def per_config_lines(args, rank, dev, stream, flush, peaks):
         torch.cuda.synchronize()
         t_on = time.time()
         for i in range(n):
-            flush.fill_(float(i))
+            flush_l2(flush, sink, i)
             evs[i][0].record(stream)
             run()
             evs[i][1].record(stream)
@@ -498,6 +514,7 @@ def bench_decode(args, world, rank, local):
     lse = torch.empty(Hq, B, dtype=torch.float32, device=dev)
     ws = torch.empty(fa.fa_decode_workspace_size(B, Hq, d, N), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     if w.page_size:
         # the cache lives in pages scattered over a pool, reached through the table
         k, v = host["k_pages"].to(dev), host["v_pages"].to(dev)
@@ -529,11 +546,13 @@ def bench_decode(args, world, rank, local):
         pg.barrier()
     torch.cuda.synchronize()
     sampler.mark_on()
+    launches0 = fa.fa_launch_count()
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush_l2(flush, sink, i)
         events[i][0].record(stream)
         step()
         events[i][1].record(stream)
+    launches = fa.fa_launch_count() - launches0
     torch.cuda.synchronize()
     sampler.mark_off()
     if pg:
@@ -550,7 +569,7 @@ def bench_decode(args, world, rank, local):
     l_host = torch.empty(Hq, B, dtype=torch.float32).pin_memory()
     h2d = q_pin.numel() * q_pin.element_size()
     d2h = o_host.numel() * o_host.element_size() + l_host.numel() * 4
-    e2e_steps = max(3, args.steps // 4)
+    e2e_steps = max(20, args.steps)
 
     def e2e_step():
         q.copy_(q_pin, non_blocking=True)
@@ -561,14 +580,16 @@ def bench_decode(args, world, rank, local):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        flush.fill_(0.0)
+    # each step timed from its query copy to its results on the host side of
+    # the copies, L2 flushed before it outside the events, as for ``value``
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush_l2(flush, sink, i)
+        e2e_ev[i][0].record(stream)
         e2e_step()
-    e1.record(stream)
+        e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps
     fa.fa_stream_status(stream)
     total_ms, e2e_ms = max_over_ranks(pg, [total_ms, e2e_ms], dev)
 
@@ -598,7 +619,7 @@ def bench_decode(args, world, rank, local):
                    "kv_cache_bytes": w.kv_cache_bytes(), "bytes_per_step": nbytes,
                    "gflop_per_step": round(w.decode_flops() / 1e9, 3),
                    "tokens_per_s": round(B * world / (avg_ms * 1e-3), 1),
-                   "l2": "flushed before every timed step (256 MiB write)",
+                   "l2": L2_NOTE,
                    "parallelism": f"replicas x{world}"},
         "step_times": step_stats(step_ms),
         "roofline": {"bound": "hbm", "kernel": "fa_decode" + ("_paged" if w.page_size else "") + ("_fp8" if w.fp8 else "")
@@ -608,7 +629,7 @@ def bench_decode(args, world, rank, local):
                      "frac": round(achieved / peak, 4), "traffic": None},
         "e2e": {"value": round(job_rate(nbytes, 1, world, e2e_ms) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
     tr = traffic_entry(args.traffic_file, w.name, line["roofline"]["kernel"])

@@ -264,6 +264,8 @@ extern "C" {
 
 const char* fa_last_error_string(void) { return g_err; }
 
+unsigned long long fa_launch_count(void) { return fa::launch_counter().load(std::memory_order_relaxed); }
+
 }  // extern "C"
 
 // Shared by fa_fwd and fa_fwd_counted (tile_count == nullptr: no counting).
@@ -646,6 +648,7 @@ int fa_selftest_wait_timeout(int limit_ms, void* stream) {
   DeviceState* dev = nullptr;
   int rc = device_state(&dev);
   if (rc) return rc;
+  fa::note_launch();
   fa::fa_selftest_timeout_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(
       dev->status, static_cast<unsigned long long>(limit_ms) * 1000000ull);
   const cudaError_t e = cudaGetLastError();

@@ -737,6 +737,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
                  bool deterministic, cudaStream_t stream) {
   const long long rows = p.T * p.Hq;
   const long long pre_blocks = (rows * 8 + 255) / 256;
+  note_launch();
   fa_bwd_rowdot_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -751,6 +752,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long units = static_cast<long long>(p.n_kvtiles) * p.B * p.Hkv;
     const int grid = static_cast<int>(units < sms ? units : sms);
+    note_launch();
     kern<<<grid, kBwdThreads, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
     e = cudaGetLastError();
   } else {
@@ -759,6 +761,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   if (e != cudaSuccess) return e;
   if (deterministic) return launch_bwd_dq_det(D, tq, tk, tv, tdo, p, stream);
   const long long n8 = rows * D / 8;
+  note_launch();
   fa_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
   return cudaGetLastError();
 }

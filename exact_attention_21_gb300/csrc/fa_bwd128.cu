@@ -467,6 +467,7 @@ int launch_bwd128_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Hkv, p.n_kvtiles, p.B);
+  note_launch();
   kern<<<grid, 448, Lay::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }

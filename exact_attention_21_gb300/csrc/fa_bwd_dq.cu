@@ -271,6 +271,7 @@ int launch_bwd_dq_det_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
       cudaFuncSetAttribute(fa_bwd_dq_det_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_kvtiles, p.Hq, p.B);  // query tiles: the same count as key tiles
+  note_launch();
   fa_bwd_dq_det_kernel<D><<<grid, 192, Lay::kBytes, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }

@@ -1,11 +1,20 @@
 // Definitions shared by the attention kernels and the host launcher.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 
 #include "ptx.cuh"
 
 namespace fa {
+
+// Kernels this library has launched in the process: every launch site counts
+// itself just before it launches (read by fa_launch_count).
+inline std::atomic<unsigned long long>& launch_counter() {
+  static std::atomic<unsigned long long> count{0};
+  return count;
+}
+inline void note_launch() { launch_counter().fetch_add(1, std::memory_order_relaxed); }
 
 // Query and key tiles are 128 x 128: 128 is the M of one tcgen05 MMA and the
 // number of TMEM lanes, so each query row owns one TMEM lane.

@@ -1343,10 +1343,12 @@ int launch_decode_dg(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
       cudaFuncSetAttribute(fa_decode_split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_splits, p.Hkv, p.B);
+  note_launch();
   fa_decode_split_kernel<D, G><<<grid, 288, Lay::kBytes, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(p.B) * p.Hq;
+  note_launch();
   fa_decode_combine_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
@@ -1373,6 +1375,7 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
   // persistent: one CTA per multiprocessor (or per item, if fewer)
   const long long items = static_cast<long long>(p.n_splits) * p.Hkv * p.B;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(items, std::max(p.sms, 1)));
+  note_launch();
   kern<<<grid, Lay::kThreads, Lay::kBytes, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -1390,6 +1393,7 @@ int launch_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeP
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  note_launch();
   return p.pair ? cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<64>, p)
                 : cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<128>, p);
 }
@@ -1440,9 +1444,11 @@ __global__ void __launch_bounds__(256) fa_quantize_fp8_kernel(const __nv_bfloat1
 int launch_quantize_fp8(int d, const void* x, void* x8, float* scale, long long rows, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
   if (d == 64) {
+    note_launch();
     fa_quantize_fp8_kernel<64><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
                                                            static_cast<uint8_t*>(x8), scale, rows);
   } else if (d == 128) {
+    note_launch();
     fa_quantize_fp8_kernel<128><<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
                                                             static_cast<uint8_t*>(x8), scale, rows);
   } else {

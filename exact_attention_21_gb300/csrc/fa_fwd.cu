@@ -811,6 +811,7 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   q.div_group_pairs = make_fast_div(q.group_pairs);
   q.div_hq = make_fast_div(q.Hq);
   q.div_qgroup = make_fast_div(q.group);
+  note_launch();
   fa_fwd_kernel<D, PAGED><<<grid, Lay::threads(PAGED), Lay::kBytes, stream>>>(tq, tk, tv, to, q);
   return cudaGetLastError();
 }

@@ -25,7 +25,8 @@ FA_ERR_UNSUPPORTED = 5
 
 EXPORTS = ("fa_fwd", "fa_fwd_counted", "fa_fwd_paged", "fa_bwd", "fa_bwd_counted", "fa_bwd_deterministic", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_decode", "fa_decode_fp8",
            "fa_decode_paged", "fa_decode_paged_fp8", "fa_decode_workspace_size", "fa_kv_quantize_fp8",
-           "fa_selftest_wait_timeout", "fa_tile_counts", "fa_stream_status", "fa_last_error_string")
+           "fa_selftest_wait_timeout", "fa_tile_counts", "fa_stream_status", "fa_last_error_string",
+           "fa_launch_count")
 
 
 class FAError(RuntimeError):
@@ -88,6 +89,8 @@ def lib():
         L.fa_stream_status.restype = i32
         L.fa_last_error_string.argtypes = []
         L.fa_last_error_string.restype = ctypes.c_char_p
+        L.fa_launch_count.argtypes = []
+        L.fa_launch_count.restype = ctypes.c_ulonglong
         _lib = L
     return _lib
 
@@ -277,6 +280,11 @@ def fa_selftest_wait_timeout(limit_ms, stream=None):
 def fa_stream_status(stream=None):
     """Synchronises the stream and raises on a latched device-side error."""
     _check(lib().fa_stream_status(_stream(stream)))
+
+
+def fa_launch_count():
+    """Kernels the library has launched in this process so far."""
+    return int(lib().fa_launch_count())
 
 
 # ---------------------------------------------------------------- conveniences

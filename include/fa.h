@@ -370,6 +370,13 @@ int fa_stream_status(void* stream);
 /* Text of the calling thread's most recent error (empty string if none). */
 const char* fa_last_error_string(void);
 
+/* Number of kernels this library has launched in the calling process, counted
+ * on the host at each launch (every entry point above, all devices and
+ * streams together).  The difference of two readings around a region is the
+ * number of this library's kernels launched in it; a call that fails before
+ * launching adds nothing.  Never fails. */
+unsigned long long fa_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif
