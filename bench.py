@@ -580,8 +580,8 @@ def bench_decode(args, world, rank, local):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    # each step timed from its query copy to its results on the host side of
-    # the copies, L2 flushed before it outside the events, as for ``value``
+    # each step is timed from the copy of its query in to the copies of its
+    # results out, with L2 flushed before it outside the events, as for ``value``
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     for i in range(e2e_steps):
         flush_l2(flush, sink, i)
